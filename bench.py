@@ -1,0 +1,572 @@
+"""Benchmark of one paged-decode step on GB300.
+
+A step is one pass of the whole hot path over one batch: copy_blocks (if the
+workload has copy-on-write pairs), reshape_and_cache (if it appends a token)
+and the decode (with its split-K merge).  The default workload is the GQA
+batch-128 decode (128 sequences, 32 query / 8 kv heads, head_dim 128, bf16,
+lognormal lengths); ``--workload`` picks another.
+
+Prints ONE JSON line (rank 0):
+  value      effective KV-read GB/s of the whole job: sum over ranks of the
+             K/V bytes a step must read (every live token, every kv head)
+             divided by the step time (max over ranks)
+  e2e        the same metric through the public API with host buffers: each
+             step copies its inputs from pinned host memory and reads the
+             output back inside the timed region
+  roofline   the decode kernel's achieved bytes/s against measured HBM peak
+  cpu_baseline  the fp64 oracle on the host cores, on a bounded sample
+
+``--impl reference`` times the oracle instead (the only reference this
+method has), on the same workload, metric and unit.
+
+Multi-GPU (torchrun): every rank runs its own replica of the workload on its
+own GPU (sequences are independent; there is no exchange step), so per-GPU
+work is fixed as N grows (weak scaling).  Only the timing is reduced across
+ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "paged decode attn: effective KV-read HBM GB/s, % of GB300 peak; seqs/s"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+DEFAULT_PARTITION = {"tiny": 0, "mha7b": 0, "gqa8b": 0, "long": 512, "parsamp": 0}
+DESCRIPTION = {
+    "tiny": "tiny decode: 4 seqs, 8/8 heads, head_dim 64, fp16, lens U[1,100], 64-block pool, +1 token",
+    "mha7b": "MHA 7B-shaped decode: 64 seqs, 32/32 heads, head_dim 128, fp16, lens U[512,2048]",
+    "gqa8b": ("GQA 8B-shaped decode: 128 seqs, 32/8 heads, head_dim 128, bf16, lens "
+              "lognormal(median 600, sigma 1) clipped [16,4096], +1 token per seq via slot_mapping"),
+    "long": ("long-context split-K decode: 4 seqs, 32/8 heads, head_dim 128, bf16, lens "
+             "{32768,65536,98304,131072}, 512-token partitions + log-sum-exp merge"),
+    "parsamp": ("parallel sampling: 16 prompts x 8 samples, 40/8 heads, head_dim 128, fp16, "
+                "1024 shared prompt tokens + U[0,256] + 1, 112 copy-on-write pairs per step"),
+}
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (timing only)
+# ---------------------------------------------------------------------------
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def dist_init(backend: str):
+    import torch.distributed as dist
+    rank, world, _ = dist_env()
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        os.environ.setdefault("MASTER_PORT", "29511")
+        dist.init_process_group(backend, rank=rank, world_size=world)
+    return rank, world
+
+
+def barrier(device=None):
+    import torch
+    import torch.distributed as dist
+    if dist.is_initialized():
+        if dist.get_backend() == "nccl" and device is not None:
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+    if device is not None and torch.cuda.is_available():
+        torch.cuda.synchronize(device)
+
+
+def dist_max(x: float, device=None) -> float:
+    """Max of a scalar over ranks (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_initialized():
+        return float(x)
+    dev = device if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def dist_sum(x: float, device=None) -> float:
+    import torch
+    import torch.distributed as dist
+    if not dist.is_initialized():
+        return float(x)
+    dev = device if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def replica_seed(base_seed: int, rank: int) -> int:
+    """Each rank draws its own batch (independent sequences, same sizes)."""
+    return base_seed + 7919 * rank
+
+
+# ---------------------------------------------------------------------------
+# workload, peaks, clocks
+# ---------------------------------------------------------------------------
+def make_workload(name: str, seed_offset: int = 0):
+    import synth
+    base = {"tiny": 1001, "mha7b": 1002, "gqa8b": 1003, "long": 1004, "parsamp": 1005}[name]
+    return synth.by_name(name, seed=replica_seed(base, seed_offset))
+
+
+def measured_hbm_peak():
+    """(GB/s, source) from MEASURED_PEAKS.json, else the recipe's fallback."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+            return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def decode_source_hash() -> str:
+    """Hash of the decode kernel sources: ncu counters apply only to this build."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_cache_260_gb300", "csrc")
+    for name in ("pa_decode.cuh", "pa_device.cuh", "pa_internal.h"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str):
+    """DRAM bytes per decode launch from the committed ncu summary, if it was
+    taken on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "decode_dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    src = decode_source_hash()
+    for line in open(path):
+        parts = line.split()
+        if len(parts) >= 3 and not line.startswith("#") and parts[0] == workload and parts[1] == src:
+            return float(parts[2])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock samples taken while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def physical_gpu_index(local_rank: int) -> int:
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    ids = [x.strip() for x in vis.split(",") if x.strip()]
+    if local_rank < len(ids) and ids[local_rank].isdigit():
+        return int(ids[local_rank])
+    return local_rank
+
+
+# ---------------------------------------------------------------------------
+# our arm: the CUDA path through the C ABI
+# ---------------------------------------------------------------------------
+class Step:
+    """Device state of one replica and its decode step (graph-captured)."""
+
+    def __init__(self, w, device, partition_size):
+        import torch
+        import paged_kv_cache_260_gb300 as pa
+        self.pa, self.w, self.dev, self.ps = pa, w, device, partition_size
+        tdt = torch.float16 if w.dtype == "f16" else torch.bfloat16
+        self.tdt = tdt
+
+        def bits(a):
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(tdt).to(device)
+
+        self.q = bits(w.q)
+        self.k = bits(w.k_cache)
+        self.v = bits(w.v_cache)
+        self.tables = torch.from_numpy(w.block_tables).to(device)
+        self.lens = torch.from_numpy(w.seq_lens).to(device)
+        self.out = torch.empty_like(self.q)
+        self.k_new = None if w.k_new is None else bits(w.k_new)
+        self.v_new = None if w.v_new is None else bits(w.v_new)
+        self.slots = None if w.slot_mapping is None else torch.from_numpy(w.slot_mapping).to(device)
+        self.pairs = (None if w.block_mapping is None or len(w.block_mapping) == 0
+                      else torch.from_numpy(w.block_mapping).to(device))
+        self.ws = pa.workspace_for(self.q, self.k, self.tables, partition_size)
+        self.launches_per_step = self._count_launches()
+        self.graph = None
+        self.ev = None
+
+    def _count_launches(self):
+        n = 1                                           # decode kernel
+        n += int(self.pairs is not None)                # copy_blocks
+        n += int(self.slots is not None)                # reshape_and_cache
+        maxlen = self.tables.shape[1] * 16
+        if self.ps == 0 or (self.ps > 0 and maxlen > self.ps):
+            n += 1                                      # log-sum-exp merge
+        return n
+
+    def run(self, ev_pair=None):
+        """Enqueue one step on the current stream; ev_pair brackets the decode."""
+        pa = self.pa
+        if self.pairs is not None:
+            pa.copy_blocks(self.k, self.v, self.pairs)
+        if self.slots is not None:
+            pa.reshape_and_cache(self.k_new, self.v_new, self.k, self.v, self.slots)
+        if ev_pair is not None:
+            ev_pair[0].record()
+        pa.decode(self.out, self.q, self.k, self.v, self.tables, self.lens, self.w.scale,
+                  partition_size=self.ps, workspace=self.ws)
+        if ev_pair is not None:
+            ev_pair[1].record()
+
+    def capture(self, steps_per_graph: int):
+        """Capture `steps_per_graph` steps, with events around each decode."""
+        import torch
+        self.ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(steps_per_graph)]
+        s = torch.cuda.Stream(self.dev)
+        s.wait_stream(torch.cuda.current_stream(self.dev))
+        with torch.cuda.stream(s):
+            for _ in range(2):
+                self.run()
+        torch.cuda.current_stream(self.dev).wait_stream(s)
+        torch.cuda.synchronize(self.dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(steps_per_graph):
+                self.run(self.ev[i])
+        self.graph = g
+
+    def decode_ms(self):
+        """Mean decode duration (ms) over the events of the last graph replay."""
+        return float(np.mean([a.elapsed_time(b) for a, b in self.ev]))
+
+
+def timing_event():
+    import torch
+    try:
+        return torch.cuda.Event(enable_timing=True, external=True)
+    except TypeError:                      # torch without external events
+        return None
+
+
+def pick_steps_per_graph(steps: int, cap: int = 32) -> int:
+    """Largest divisor of `steps` not above `cap`, so K steps are replayed exactly."""
+    for d in range(min(cap, max(1, steps)), 0, -1):
+        if steps % d == 0:
+            return d
+    return 1
+
+
+def cpu_baseline(w, budget_s: float = 12.0):
+    """The fp64 oracle on a bounded sample: whole sequences in order, repeated
+    until ~budget_s of CPU work; returns (GB/s of KV processed, sample text, cores)."""
+    import oracle
+    oracle.build()
+    threads = oracle.num_threads()
+    k, v = w.k_cache.copy(), w.v_cache.copy()
+    t0 = time.perf_counter()
+    if w.block_mapping is not None and len(w.block_mapping):
+        oracle.copy_blocks(k, v, w.block_mapping)
+    if w.slot_mapping is not None:
+        oracle.reshape_and_cache(k, v, w.k_new, w.v_new, w.slot_mapping)
+    per_seq = 2 * w.num_kv_heads * w.head_dim * 2
+    done_bytes, seqs, reps = 0, 0, 0
+    chunk = max(1, threads // 2)
+    while True:
+        for s0 in range(0, w.num_seqs, chunk):
+            sel = list(range(s0, min(w.num_seqs, s0 + chunk)))
+            oracle.decode(w.q, k, v, w.block_tables, w.seq_lens, w.scale, w.dtype, seqs=sel,
+                          threads=threads)
+            done_bytes += int(sum(int(w.seq_lens[s]) for s in sel)) * per_seq
+            seqs += len(sel)
+            if time.perf_counter() - t0 > budget_s:
+                break
+        else:
+            reps += 1
+            if time.perf_counter() - t0 < budget_s:
+                continue
+        break
+    dt = time.perf_counter() - t0
+    sample = (f"fp64 oracle step (copy/reshape once, then decode of {seqs} sequences in order, "
+              f"{reps} full passes) in {dt:.1f} s")
+    return done_bytes / dt / 1e9, sample, threads
+
+
+def e2e_measure(st, steps: int, device):
+    """Public-API step with host buffers: pinned H2D of the step's inputs, the
+    step, D2H of the output; returns (ms per step, h2d bytes, d2h bytes)."""
+    import torch
+    names = ["q", "tables", "lens", "k_new", "v_new", "slots", "pairs"]
+    dev_t = {n: getattr(st, n) for n in names if getattr(st, n) is not None}
+    host_t = {n: t.cpu().pin_memory() for n, t in dev_t.items()}
+    out_h = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_t.values())
+    d2h = out_h.numel() * out_h.element_size()
+
+    def one():
+        for n, t in dev_t.items():
+            t.copy_(host_t[n], non_blocking=True)
+        st.run()
+        out_h.copy_(st.out, non_blocking=True)
+
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize(device)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        one()
+    b.record()
+    torch.cuda.synchronize(device)
+    return a.elapsed_time(b) / steps, h2d, d2h
+
+
+def run_ours(args):
+    import torch
+    rank, world = dist_init("nccl" if torch.cuda.is_available() else "gloo")
+    local = dist_env()[2]
+    device = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(device)
+    from paged_kv_cache_260_gb300 import _build
+    _build.build()
+    import paged_kv_cache_260_gb300 as pa
+    pa.load()
+
+    ps = DEFAULT_PARTITION[args.workload] if args.partition is None else args.partition
+    w = make_workload(args.workload, rank)
+    st = Step(w, device, ps)
+    kv_bytes = w.kv_read_bytes()
+    l2_ok = kv_bytes > 2 * L2_BYTES
+    spg = pick_steps_per_graph(args.steps)
+    use_graph = timing_event() is not None and not args.no_graph
+    if use_graph:
+        st.ev = None
+        st.capture(spg)
+        replays = args.steps // spg
+        for _ in range(max(1, -(-args.warmup // spg))):
+            st.graph.replay()
+    else:
+        ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+        for _ in range(args.warmup):
+            st.run()
+    torch.cuda.synchronize(device)
+    assert pa.get_device_error() == 0, "a kernel recorded an error during warm-up"
+
+    flush = None if l2_ok else torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=device)
+    dec_ms = []
+    with ClockSampler(physical_gpu_index(local)) as clk:
+        barrier(device)
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        if flush is None:
+            t0.record()
+            if use_graph:
+                for _ in range(replays):
+                    st.graph.replay()
+            else:
+                for _ in range(args.steps):
+                    st.run(ev)
+            t1.record()
+            torch.cuda.synchronize(device)
+            elapsed = t0.elapsed_time(t1)
+            dec_ms.append(st.decode_ms() if use_graph else ev[0].elapsed_time(ev[1]))
+        else:
+            # small working set: flush L2 before every step, time the steps only
+            elapsed = 0.0
+            ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(args.steps):
+                flush.zero_()
+                t0.record()
+                st.run(ev)
+                t1.record()
+                torch.cuda.synchronize(device)
+                elapsed += t0.elapsed_time(t1)
+                dec_ms.append(ev[0].elapsed_time(ev[1]))
+        barrier(device)
+    assert pa.get_device_error() == 0, "a kernel recorded an error in the timed region"
+    t_max = dist_max(elapsed, device)
+    ms_per_step = t_max / args.steps
+    total_bytes = dist_sum(kv_bytes, device)
+    total_seqs = dist_sum(w.num_seqs, device)
+    value = total_bytes / (ms_per_step * 1e-3) / 1e9
+    dec = float(np.mean(dec_ms))
+
+    e2e_ms, h2d, d2h = e2e_measure(st, max(20, min(args.steps, 300)), device)
+    e2e_ms = dist_max(e2e_ms, device)
+    peak, peak_src = measured_hbm_peak()
+    achieved = kv_bytes / (dec * 1e-3) / 1e9
+    traffic = ncu_traffic(args.workload)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, sample, cores = cpu_baseline(w)
+        cpu = {"value": v, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample}
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": w.dtype,
+        "data": "synthetic (seeded N(0,1) q/K/V, random block permutation)",
+        "pct_of_hbm_peak": 100.0 * value / world / peak,
+        "seqs_per_s": total_seqs / (ms_per_step * 1e-3),
+        "config": {
+            "workload": DESCRIPTION[args.workload],
+            "name": args.workload,
+            "num_seqs": w.num_seqs, "num_heads": w.num_heads, "num_kv_heads": w.num_kv_heads,
+            "head_dim": w.head_dim, "block_size": 16, "partition_size": ps,
+            "kv_bytes_per_step": kv_bytes,
+            "step": "copy_blocks + reshape_and_cache + decode (+ merge)"[
+                0 if w.block_mapping is not None else 14:],
+            "l2": ("inputs larger than L2 (KV read per step %.0f MB vs 129 MB L2)" % (kv_bytes / 1e6)
+                   if l2_ok else "L2 flushed (256 MB write) before every step; steps timed alone"),
+            "timing": ("CUDA graph of %d steps replayed %d times, CUDA events" % (spg, args.steps // spg)
+                       if use_graph and l2_ok else "CUDA events per step"),
+            "parallelism": "replicas" if world > 1 else "single GPU",
+        },
+        "e2e": {"value": total_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "roofline": {"bound": "hbm", "kernel": "pa_decode (decode kernel + split-K merge)",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs, copy burst)"
+                     if peak_src == "measured" else "fallback 6.8 TB/s",
+                     "algorithmic_bytes_per_launch": kv_bytes, "decode_ms": dec,
+                     "traffic": traffic},
+        "cpu_baseline": cpu,
+        "gpu_launches": st.launches_per_step * args.steps,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_reference(args):
+    """The oracle as the reference arm: each step is a bounded sample of the
+    workload (whole sequences in order) on the host cores."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    w = make_workload(args.workload, 0)
+    threads = oracle.num_threads()
+    per_seq = 2 * w.num_kv_heads * w.head_dim * 2
+    budget = max(0.05, 90.0 / max(1, args.steps + args.warmup))   # seconds per step
+    # sample size: whole sequences, as many as fit the per-step budget (at least one)
+    t0 = time.perf_counter()
+    oracle.decode(w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.scale, w.dtype,
+                  seqs=[0], threads=threads)
+    one = max(1e-4, time.perf_counter() - t0)
+    n = int(max(1, min(w.num_seqs, budget / one)))
+    sel = list(range(n))
+
+    def step():
+        oracle.decode(w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.scale, w.dtype,
+                      seqs=sel, threads=threads)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    b = sum(int(w.seq_lens[s]) for s in sel) * per_seq
+    value = b * args.steps / dt / 1e9
+    sample = f"fp64 oracle decode of sequences 0..{n - 1} of the workload per step"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": DESCRIPTION[args.workload], "name": args.workload},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=list(DESCRIPTION), default="gqa8b")
+    ap.add_argument("--partition", type=int, default=None,
+                    help="-1 no split, 0 balanced split, >0 fixed partition tokens")
+    ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,203 @@
+/*
+ * pagedattn.h -- C ABI of the GB300 (sm_103a) paged-KV-cache kernels.
+ *
+ * The KV cache lives in a pool of fixed 16-token blocks allocated once by the
+ * caller; each sequence reaches its blocks through a block table (logical
+ * block -> physical block), so attention reads K/V indirectly, exactly as an
+ * MMU maps pages to frames ("PagedAttention：vLLM 系统论文" reading notes,
+ * section 核心思想, block-pool figure and the OS-paging table; default block
+ * of 16 tokens also in the vLLM deep notes, section "PagedAttention：操作系统
+ * 启发的设计").
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All pointers are DEVICE pointers, owned by the caller, 16-byte aligned.
+ *    The library never allocates, frees or synchronises; every call only
+ *    enqueues kernels on `stream` (a cudaStream_t passed as void*; NULL is the
+ *    legacy default stream) and returns.
+ *  - dtype: PA_DTYPE_F16 or PA_DTYPE_BF16, the type of q, out and both pools.
+ *    Accumulation is fp32.
+ *  - Pool layout ("HND"): k_cache, v_cache = [num_blocks][num_kv_heads]
+ *    [block_size][head_dim], row-major.  Token t of sequence s lives in
+ *    physical block block_tables[s][t / block_size] at offset
+ *    t % block_size; slot numbers are block * block_size + offset.
+ *  - block_size must be 16; head_dim 64 or 128; num_heads a multiple of
+ *    num_kv_heads with a group G = num_heads / num_kv_heads of 1..8.  Query
+ *    head h reads kv head h / G (grouped-query attention: several query heads
+ *    share one K/V head, ICML tutorial notes, section "Attention 简化与 KV Cache
+ *    优化").
+ *  - Every call returns a pa_status.  Scalars and pointers are checked on the
+ *    host before anything is enqueued.  Device arrays are not read on the
+ *    host; kernels bounds-check every block id, slot and length they use,
+ *    skip the offending access and record a PA_DEVERR_* bit that
+ *    pa_get_device_error() returns.  No kernel traps.
+ */
+#ifndef PAGEDATTN_H
+#define PAGEDATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PAGEDATTN_VERSION 1
+
+enum pa_status {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size or count */
+    PA_ERR_UNSUPPORTED = 2,   /* head_dim, block_size, group or dtype not built */
+    PA_ERR_WORKSPACE = 3,     /* workspace missing or smaller than required */
+    PA_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
+    PA_ERR_DEVICE = 5         /* a kernel recorded an error (see pa_get_device_error) */
+};
+
+enum pa_dtype { PA_DTYPE_F16 = 0, PA_DTYPE_BF16 = 1 };
+
+/* bits recorded by kernels; read and cleared with pa_get_device_error() */
+#define PA_DEVERR_SLOT_RANGE   0x1u  /* reshape_and_cache: slot >= num_blocks*block_size */
+#define PA_DEVERR_BLOCK_RANGE  0x2u  /* copy_blocks: src or dst outside [0, num_blocks) */
+#define PA_DEVERR_TABLE_RANGE  0x4u  /* decode/gather: table entry outside [0, num_blocks) */
+#define PA_DEVERR_SEQLEN_RANGE 0x8u  /* seq_len < 0 or > max_blocks_per_seq*block_size */
+#define PA_DEVERR_TIMEOUT      0x10u /* a bounded wait on a copy expired */
+
+/* PAGEDATTN_VERSION of the loaded library. */
+int pa_version(void);
+
+/* Static, human-readable name of a pa_status. */
+const char *pa_status_string(int status);
+
+/*
+ * Bytes of device workspace pa_decode needs for these sizes (0 when none).
+ * partition_size selects the split-K mode exactly as in pa_decode.  The value
+ * depends on the current device's SM count for partition_size == 0.
+ */
+size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads,
+                                int head_dim, int max_blocks_per_seq,
+                                int partition_size);
+
+/*
+ * Paged decode attention, one query token per sequence.
+ *
+ * For every sequence s and query head h:
+ *     out[s][h] = sum_t softmax_t(scale * q[s][h] . k_t) v_t,   t < seq_lens[s]
+ * with k_t, v_t read through block_tables (the block-table figure of the vLLM
+ * reading notes: attention addresses non-contiguous KV through the table).
+ * The result is the exact softmax attention; scores are never materialised
+ * (online softmax with running max and sum, vLLM deep notes, section
+ * "核心思想：Tiling + Online Softmax").  A sequence of length 0 yields zeros.
+ *
+ *   out          [num_seqs][num_heads][head_dim]        dtype, written
+ *   q            [num_seqs][num_heads][head_dim]        dtype
+ *   k_cache, v_cache  pool, layout above                dtype
+ *   block_tables [num_seqs][max_blocks_per_seq] int32;  entries past a
+ *                sequence's ceil(len/16) blocks are never read
+ *   seq_lens     [num_seqs] int32, 0 <= len <= max_blocks_per_seq * 16
+ *   scale        multiplies q.k (typically 1/sqrt(head_dim))
+ *
+ * Split-K along the sequence (FlashDecoding, ICML tutorial notes, section
+ * "内核优化"), chosen by partition_size:
+ *   -1  no split: one thread block reduces each (sequence, kv head) whole;
+ *    0  balanced split: the grid is sized to the GPU and every thread block
+ *       gets the same number of 16-token tiles; (sequence, kv head) runs cut
+ *       by a tile-range boundary are finished by a log-sum-exp merge;
+ *   >0  fixed partitions of partition_size tokens (a multiple of 16); each
+ *       partition's partial result is merged with the log-sum-exp rule
+ *           M = max_p m_p,  w_p = l_p exp(m_p - M),  o = sum_p w_p o_p / sum_p w_p.
+ *       The partials are left in the workspace, fp32, as three arrays each
+ *       starting at a 256-byte boundary:
+ *           m [num_seqs][num_heads][P_max]  max of the partition's scaled scores
+ *           l [num_seqs][num_heads][P_max]  sum_t exp(score_t - m)
+ *           o [num_seqs][num_heads][P_max][head_dim]  normalised partial output
+ *       P_max = ceil(max_blocks_per_seq * 16 / partition_size); entries of
+ *       partitions past a sequence's end, and of sequences that fit one
+ *       partition, are not written.
+ *
+ * workspace: device buffer of at least pa_decode_workspace_size(...) bytes,
+ * caller-owned, contents need no initialisation.  Calls that share a
+ * workspace must be ordered on one stream.
+ */
+int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
+              const int32_t *block_tables, const int32_t *seq_lens,
+              int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+              int block_size, int max_blocks_per_seq, int num_blocks,
+              float scale, int dtype, int partition_size,
+              void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Write each new token's K and V into its pool slot: for token i with
+ * slot = slot_mapping[i] >= 0, for every kv head h,
+ *     k_cache[slot / 16][h][slot % 16][:] = k_new[i][h][:]   (same for V).
+ * Blocks are handed out on demand, only when a sequence produces a token
+ * that needs a new one, and fill up one token per decode step (forum summary
+ * of the notes repository, section 虚拟内存的启示, design point 2; the
+ * demand-paging row of the OS-paging table in the vLLM reading notes).
+ * Negative slots mark padding tokens and are skipped.  Raw 16-bit copies:
+ * bit-exact, NaN payloads preserved.
+ *
+ *   k_new, v_new  [num_tokens][num_kv_heads][head_dim]  dtype
+ *   slot_mapping  [num_tokens] int64
+ * Slots >= num_blocks*16 are skipped and set PA_DEVERR_SLOT_RANGE.  Two tokens
+ * naming the same slot race (one of them wins).
+ */
+int pa_reshape_and_cache(const void *k_new, const void *v_new,
+                         void *k_cache, void *v_cache,
+                         const int64_t *slot_mapping, int num_tokens,
+                         int num_kv_heads, int head_dim, int block_size,
+                         int num_blocks, int dtype, void *stream);
+
+/*
+ * Copy-on-write of shared blocks: for every pair i,
+ *     k_cache[dst] = k_cache[src], v_cache[dst] = v_cache[src]
+ * whole blocks (every kv head and slot), with (src, dst) =
+ * block_mapping[i][0], block_mapping[i][1].  Blocks shared by reference
+ * count are copied before a sequence writes into them (block sharing for
+ * parallel sampling and beam search, the page-sharing row of the OS-paging
+ * table and section 系统实现要点 of the vLLM reading notes; reference counts
+ * and copy-on-write in the vLLM deep notes, section "PagedAttention：操作系统
+ * 启发的设计").
+ *
+ *   block_mapping [num_pairs][2] int64
+ * No dst may appear twice or equal any src (not checked: such pairs race).
+ * Pairs naming a block outside the pool are skipped and set
+ * PA_DEVERR_BLOCK_RANGE.  Raw 16-bit copies, bit-exact.
+ */
+int pa_copy_blocks(void *k_cache, void *v_cache, const int64_t *block_mapping,
+                   int num_pairs, int num_kv_heads, int head_dim, int block_size,
+                   int num_blocks, int dtype, void *stream);
+
+/*
+ * Debug/test export: materialise each sequence's K and V contiguously,
+ * read through its block table (the same indirection the decode uses):
+ *     k_out[s][h][t][:] = k_cache[block_tables[s][t/16]][h][t%16][:],  t < seq_lens[s]
+ *   k_out, v_out  [num_seqs][num_kv_heads][max_blocks_per_seq*16][head_dim];
+ *   positions t >= seq_lens[s] are not written.  Bit-exact copies.
+ */
+int pa_gather_kv(void *k_out, void *v_out, const void *k_cache, const void *v_cache,
+                 const int32_t *block_tables, const int32_t *seq_lens,
+                 int num_seqs, int num_kv_heads, int head_dim, int block_size,
+                 int max_blocks_per_seq, int num_blocks, int dtype, void *stream);
+
+/*
+ * Check the tables a decode would read: counts, into *bad_count (a device
+ * uint32 the caller zeroes), the entries block_tables[s][b] with
+ * b < ceil(seq_lens[s]/16) outside [0, num_blocks), plus the sequences whose
+ * length is outside [0, max_blocks_per_seq*16].
+ */
+int pa_validate_tables(const int32_t *block_tables, const int32_t *seq_lens,
+                       int num_seqs, int max_blocks_per_seq, int num_blocks,
+                       int block_size, uint32_t *bad_count, void *stream);
+
+/*
+ * Synchronise `stream`, return in *bits the PA_DEVERR_* bits kernels on the
+ * current device have recorded since the last clear, and clear them when
+ * `clear` is non-zero.  Returns PA_ERR_DEVICE when bits is non-zero.
+ */
+int pa_get_device_error(void *stream, uint32_t *bits, int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDATTN_H */

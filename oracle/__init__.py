@@ -122,21 +122,33 @@ def decode(q, k_cache, v_cache, block_tables, seq_lens, scale, dtype: str,
     mb = block_tables.shape[1]
     dt = DTYPES[dtype]
 
+    nt = threads or num_threads()
+    sel = list(range(S)) if seqs is None else [int(s) for s in seqs]
+
     def run(r):
         L.oracle_decode(out, q, k_cache, v_cache, block_tables, seq_lens, Hq, Hkv, D,
                         BLOCK_SIZE, mb, float(scale), dt, r[0], r[1])
 
-    if seqs is not None:
-        rngs = [(int(s), int(s) + 1) for s in seqs]
+    def run_head(sh):
+        # one (sequence, head) at a time, for batches too small to spread by sequence
+        s, h = sh
+        m = np.zeros(1)
+        l = np.zeros(1)
+        L.oracle_attend(out[s, h], m, l, q, k_cache, v_cache, block_tables, mb, Hq, Hkv, D,
+                        BLOCK_SIZE, float(scale), dt, s, h, 0, int(seq_lens[s]))
+
+    if nt > 1 and len(sel) < 2 * nt:
+        tasks, fn = [(s, h) for s in sel for h in range(Hq)], run_head
+    elif seqs is not None:
+        tasks, fn = [(s, s + 1) for s in sel], run
     else:
-        rngs = _ranges(S, 4 * (threads or num_threads()))
-    nt = threads or num_threads()
-    if nt == 1 or len(rngs) == 1:
-        for r in rngs:
-            run(r)
+        tasks, fn = _ranges(S, 4 * nt), run
+    if nt == 1 or len(tasks) == 1:
+        for t in tasks:
+            fn(t)
     else:
         with _cf.ThreadPoolExecutor(nt) as ex:
-            list(ex.map(run, rngs))
+            list(ex.map(fn, tasks))
     return out
 
 

@@ -1,0 +1,454 @@
+// pa_api.cu -- the C ABI declared in include/pagedattn.h: host-side argument
+// checks, per-device state and kernel dispatch.  Nothing here allocates
+// device memory or synchronises, except pa_get_device_error().
+#include <math.h>
+#include <mutex>
+#include <stdint.h>
+
+#include "pa_cache.h"
+#include "pa_internal.h"
+#include "pagedattn.h"
+
+namespace pa {
+
+// Error bits recorded by the kernels (one word per device).
+__device__ uint32_t g_device_error;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    bool ready = false;
+    int num_sms = 0;
+    uint32_t *err = nullptr;   // device address of g_device_error
+    size_t smem_optin = 0;     // largest dynamic shared memory per block
+};
+
+std::mutex g_mutex;
+DeviceState g_dev[kMaxDevices];
+
+struct AttrEntry {
+    const void *func;
+    int device;
+    size_t smem;
+};
+constexpr int kMaxAttr = 256;
+AttrEntry g_attr[kMaxAttr];
+int g_attr_count = 0;
+
+struct OccEntry {
+    const void *func;
+    int device;
+    size_t smem;
+    int blocks;
+};
+constexpr int kMaxOcc = 512;
+OccEntry g_occ[kMaxOcc];
+int g_occ_count = 0;
+
+int device_state(DeviceState **out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return PA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState &st = g_dev[dev];
+    if (!st.ready) {
+        int sms = 0, optin = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return PA_ERR_CUDA;
+        if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+            cudaSuccess)
+            return PA_ERR_CUDA;
+        void *addr = nullptr;
+        if (cudaGetSymbolAddress(&addr, g_device_error) != cudaSuccess)
+            return PA_ERR_CUDA;
+        st.num_sms = sms;
+        st.smem_optin = (size_t)optin;
+        st.err = static_cast<uint32_t *>(addr);
+        st.ready = true;
+    }
+    *out = &st;
+    return PA_OK;
+}
+
+// Raise the kernel's dynamic shared memory limit once per (device, size).
+int ensure_smem(const void *func, int dev, size_t smem)
+{
+    std::lock_guard<std::mutex> lock(g_mutex);
+    for (int i = 0; i < g_attr_count; ++i)
+        if (g_attr[i].func == func && g_attr[i].device == dev) {
+            if (g_attr[i].smem >= smem)
+                return PA_OK;
+            if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+                cudaSuccess)
+                return PA_ERR_CUDA;
+            g_attr[i].smem = smem;
+            return PA_OK;
+        }
+    if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
+        return PA_ERR_CUDA;
+    if (g_attr_count < kMaxAttr)
+        g_attr[g_attr_count++] = AttrEntry{func, dev, smem};
+    return PA_OK;
+}
+
+int occupancy(const void *func, int dev, int threads, size_t smem, int *blocks)
+{
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        for (int i = 0; i < g_occ_count; ++i)
+            if (g_occ[i].func == func && g_occ[i].device == dev && g_occ[i].smem == smem) {
+                *blocks = g_occ[i].blocks;
+                return PA_OK;
+            }
+    }
+    int nb = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, func, threads, smem) != cudaSuccess)
+        return PA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (g_occ_count < kMaxOcc)
+        g_occ[g_occ_count++] = OccEntry{func, dev, smem, nb};
+    *blocks = nb;
+    return PA_OK;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+int check_common(int num_kv_heads, int head_dim, int block_size, int num_blocks, int dtype)
+{
+    if (dtype != PA_DTYPE_F16 && dtype != PA_DTYPE_BF16)
+        return PA_ERR_UNSUPPORTED;
+    if (block_size != kBlockSize)
+        return PA_ERR_UNSUPPORTED;
+    if (head_dim != 64 && head_dim != 128)
+        return PA_ERR_UNSUPPORTED;
+    if (num_kv_heads <= 0 || num_blocks <= 0)
+        return PA_ERR_INVALID_ARG;
+    return PA_OK;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? PA_OK : PA_ERR_CUDA; }
+
+struct WorkspaceLayout {
+    size_t m_off, l_off, o_off, prefix_off, total;
+    long long rows;
+};
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Workspace of one decode: partial rows (m, l, o) and, for balanced mode, the
+// per-sequence tile prefix.  rows = num_seqs * num_heads * P_max (fixed) or
+// 2 * grid * group (balanced: at most two cut runs per thread block).
+WorkspaceLayout workspace_layout(int mode, int num_seqs, int num_heads, int group, int head_dim,
+                                 int p_max, int grid)
+{
+    WorkspaceLayout w{};
+    if (mode == kModeWhole)
+        return w;
+    w.rows = mode == kModeFixed ? (long long)num_seqs * num_heads * p_max : 2LL * grid * group;
+    w.m_off = 0;
+    w.l_off = round_up(w.m_off + sizeof(float) * w.rows, 256);
+    w.o_off = round_up(w.l_off + sizeof(float) * w.rows, 256);
+    w.prefix_off = round_up(w.o_off + sizeof(float) * w.rows * head_dim, 256);
+    w.total = w.prefix_off;
+    if (mode == kModeBalanced)
+        w.total = round_up(w.prefix_off + sizeof(int32_t) * (num_seqs + 1), 256);
+    return w;
+}
+
+int decode_mode(int partition_size, int *mode, int *part_tiles)
+{
+    if (partition_size == -1) {
+        *mode = kModeWhole;
+        *part_tiles = 1 << 30;
+    } else if (partition_size == 0) {
+        *mode = kModeBalanced;
+        *part_tiles = 0;
+    } else if (partition_size > 0 && partition_size % kBlockSize == 0) {
+        *mode = kModeFixed;
+        *part_tiles = partition_size / kBlockSize;
+    } else {
+        return PA_ERR_INVALID_ARG;
+    }
+    return PA_OK;
+}
+
+}  // namespace
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" {
+
+int pa_version(void) { return PAGEDATTN_VERSION; }
+
+const char *pa_status_string(int status)
+{
+    switch (status) {
+    case PA_OK:
+        return "ok";
+    case PA_ERR_INVALID_ARG:
+        return "invalid argument";
+    case PA_ERR_UNSUPPORTED:
+        return "unsupported configuration";
+    case PA_ERR_WORKSPACE:
+        return "workspace missing or too small";
+    case PA_ERR_CUDA:
+        return "CUDA error";
+    case PA_ERR_DEVICE:
+        return "a kernel recorded an error";
+    default:
+        return "unknown status";
+    }
+}
+
+size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                int max_blocks_per_seq, int partition_size)
+{
+    int mode, pt;
+    if (num_seqs <= 0 || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads ||
+        max_blocks_per_seq <= 0 || decode_mode(partition_size, &mode, &pt) != PA_OK)
+        return 0;
+    int grid = 0;
+    if (mode == kModeBalanced) {
+        DeviceState *ds;
+        if (device_state(&ds) != PA_OK)
+            return 0;
+        grid = ds->num_sms * kMaxBlocksPerSM;
+    }
+    const int p_max = mode == kModeFixed ? (max_blocks_per_seq + pt - 1) / pt : 1;
+    return workspace_layout(mode, num_seqs, num_heads, num_heads / num_kv_heads, head_dim, p_max,
+                            grid)
+        .total;
+}
+
+int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
+              const int32_t *block_tables, const int32_t *seq_lens, int num_seqs, int num_heads,
+              int num_kv_heads, int head_dim, int block_size, int max_blocks_per_seq,
+              int num_blocks, float scale, int dtype, int partition_size, void *workspace,
+              size_t workspace_bytes, void *stream)
+{
+    int rc = check_common(num_kv_heads, head_dim, block_size, num_blocks, dtype);
+    if (rc != PA_OK)
+        return rc;
+    if (num_seqs < 0 || num_heads <= 0 || max_blocks_per_seq <= 0 || !isfinite(scale))
+        return PA_ERR_INVALID_ARG;
+    if (num_heads % num_kv_heads)
+        return PA_ERR_INVALID_ARG;
+    const int group = num_heads / num_kv_heads;
+    if (group > 8 || num_seqs > kMaxSeqs)
+        return PA_ERR_UNSUPPORTED;
+    if (num_seqs == 0)
+        return PA_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(block_tables, 4) || !aligned(seq_lens, 4))
+        return PA_ERR_INVALID_ARG;
+    // flat tile indices are 32-bit
+    if ((long long)num_seqs * max_blocks_per_seq * num_kv_heads >= (1LL << 31) ||
+        (long long)max_blocks_per_seq * kBlockSize >= (1LL << 30))
+        return PA_ERR_UNSUPPORTED;
+    int mode, pt;
+    rc = decode_mode(partition_size, &mode, &pt);
+    if (rc != PA_OK)
+        return rc;
+
+    KernelSet ks{};
+    const bool found = dtype == PA_DTYPE_F16 ? decode_kernels_f16(head_dim, group, &ks)
+                                             : decode_kernels_bf16(head_dim, group, &ks);
+    if (!found)
+        return PA_ERR_UNSUPPORTED;
+    DeviceState *ds;
+    rc = device_state(&ds);
+    if (rc != PA_OK)
+        return rc;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const size_t smem = decode_smem_bytes(ks, num_seqs);
+    if (smem > ds->smem_optin)
+        return PA_ERR_UNSUPPORTED;
+    rc = ensure_smem(ks.decode, dev, smem);
+    if (rc != PA_OK)
+        return rc;
+    int per_sm = 0;
+    rc = occupancy(ks.decode, dev, ks.warps * 32, smem, &per_sm);
+    if (rc != PA_OK)
+        return rc;
+    if (per_sm < 1)
+        return PA_ERR_UNSUPPORTED;
+    if (per_sm > kMaxBlocksPerSM)
+        per_sm = kMaxBlocksPerSM;
+    const int grid = ds->num_sms * per_sm;
+    const int p_max = mode == kModeFixed ? (max_blocks_per_seq + pt - 1) / pt : 1;
+    const WorkspaceLayout wl = workspace_layout(mode, num_seqs, num_heads, group, head_dim, p_max,
+                                                mode == kModeBalanced ? ds->num_sms * kMaxBlocksPerSM
+                                                                      : grid);
+    if (wl.total > 0 && (!workspace || workspace_bytes < wl.total || !aligned(workspace, 256)))
+        return PA_ERR_WORKSPACE;
+
+    DecodeParams p{};
+    p.out = out;
+    p.q = q;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.block_tables = block_tables;
+    p.seq_lens = seq_lens;
+    char *ws = static_cast<char *>(workspace);
+    if (wl.total > 0) {
+        p.ws_m = reinterpret_cast<float *>(ws + wl.m_off);
+        p.ws_l = reinterpret_cast<float *>(ws + wl.l_off);
+        p.ws_o = reinterpret_cast<float *>(ws + wl.o_off);
+        p.ws_prefix = mode == kModeBalanced ? reinterpret_cast<int32_t *>(ws + wl.prefix_off)
+                                            : nullptr;
+    }
+    p.err = ds->err;
+    p.num_seqs = num_seqs;
+    p.num_heads = num_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.max_blocks = max_blocks_per_seq;
+    p.num_blocks = num_blocks;
+    p.mode = mode;
+    p.part_tiles = pt;
+    p.p_max = p_max;
+    p.min_tiles = kMinTiles;
+    p.grid = grid;
+    p.scale_log2 = scale * 1.4426950408889634f;
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    void *args[] = {&p};
+    cudaError_t e = cudaLaunchKernel(ks.decode, dim3(grid), dim3(ks.warps * 32), args, smem, st);
+    if (e != cudaSuccess)
+        return PA_ERR_CUDA;
+    const bool needs_merge = mode == kModeBalanced || (mode == kModeFixed && p_max > 1);
+    if (needs_merge) {
+        e = cudaLaunchKernel(ks.merge, dim3(num_seqs * num_kv_heads), dim3(128), args, 0, st);
+        if (e != cudaSuccess)
+            return PA_ERR_CUDA;
+    }
+    return PA_OK;
+}
+
+int pa_reshape_and_cache(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                         const int64_t *slot_mapping, int num_tokens, int num_kv_heads,
+                         int head_dim, int block_size, int num_blocks, int dtype, void *stream)
+{
+    int rc = check_common(num_kv_heads, head_dim, block_size, num_blocks, dtype);
+    if (rc != PA_OK)
+        return rc;
+    if (num_tokens < 0)
+        return PA_ERR_INVALID_ARG;
+    if (num_tokens == 0)
+        return PA_OK;
+    if (!k_new || !v_new || !k_cache || !v_cache || !slot_mapping)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 16) ||
+        !aligned(v_cache, 16) || !aligned(slot_mapping, 8))
+        return PA_ERR_INVALID_ARG;
+    DeviceState *ds;
+    rc = device_state(&ds);
+    if (rc != PA_OK)
+        return rc;
+    return cuda_status(launch_reshape_and_cache(k_new, v_new, k_cache, v_cache, slot_mapping,
+                                                num_tokens, num_kv_heads, head_dim, num_blocks,
+                                                ds->err, ds->num_sms,
+                                                static_cast<cudaStream_t>(stream)));
+}
+
+int pa_copy_blocks(void *k_cache, void *v_cache, const int64_t *block_mapping, int num_pairs,
+                   int num_kv_heads, int head_dim, int block_size, int num_blocks, int dtype,
+                   void *stream)
+{
+    int rc = check_common(num_kv_heads, head_dim, block_size, num_blocks, dtype);
+    if (rc != PA_OK)
+        return rc;
+    if (num_pairs < 0)
+        return PA_ERR_INVALID_ARG;
+    if (num_pairs == 0)
+        return PA_OK;
+    if (!k_cache || !v_cache || !block_mapping)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(block_mapping, 8))
+        return PA_ERR_INVALID_ARG;
+    DeviceState *ds;
+    rc = device_state(&ds);
+    if (rc != PA_OK)
+        return rc;
+    return cuda_status(launch_copy_blocks(k_cache, v_cache, block_mapping, num_pairs, num_kv_heads,
+                                          head_dim, num_blocks, ds->err,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+int pa_gather_kv(void *k_out, void *v_out, const void *k_cache, const void *v_cache,
+                 const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,
+                 int num_kv_heads, int head_dim, int block_size, int max_blocks_per_seq,
+                 int num_blocks, int dtype, void *stream)
+{
+    int rc = check_common(num_kv_heads, head_dim, block_size, num_blocks, dtype);
+    if (rc != PA_OK)
+        return rc;
+    if (num_seqs < 0 || max_blocks_per_seq <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0)
+        return PA_OK;
+    if (!k_out || !v_out || !k_cache || !v_cache || !block_tables || !seq_lens)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned(k_out, 16) || !aligned(v_out, 16) || !aligned(k_cache, 16) ||
+        !aligned(v_cache, 16) || !aligned(block_tables, 4) || !aligned(seq_lens, 4))
+        return PA_ERR_INVALID_ARG;
+    DeviceState *ds;
+    rc = device_state(&ds);
+    if (rc != PA_OK)
+        return rc;
+    return cuda_status(launch_gather_kv(k_out, v_out, k_cache, v_cache, block_tables, seq_lens,
+                                        num_seqs, num_kv_heads, head_dim, max_blocks_per_seq,
+                                        num_blocks, ds->err, ds->num_sms,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
+int pa_validate_tables(const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,
+                       int max_blocks_per_seq, int num_blocks, int block_size,
+                       uint32_t *bad_count, void *stream)
+{
+    if (block_size != kBlockSize)
+        return PA_ERR_UNSUPPORTED;
+    if (num_seqs < 0 || max_blocks_per_seq <= 0 || num_blocks <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0)
+        return PA_OK;
+    if (!block_tables || !seq_lens || !bad_count || !aligned(block_tables, 4) ||
+        !aligned(seq_lens, 4) || !aligned(bad_count, 4))
+        return PA_ERR_INVALID_ARG;
+    DeviceState *ds;
+    int rc = device_state(&ds);
+    if (rc != PA_OK)
+        return rc;
+    return cuda_status(launch_validate_tables(block_tables, seq_lens, num_seqs, max_blocks_per_seq,
+                                              num_blocks, bad_count, ds->num_sms,
+                                              static_cast<cudaStream_t>(stream)));
+}
+
+int pa_get_device_error(void *stream, uint32_t *bits, int clear)
+{
+    if (!bits)
+        return PA_ERR_INVALID_ARG;
+    DeviceState *ds;
+    int rc = device_state(&ds);
+    if (rc != PA_OK)
+        return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint32_t host = 0;
+    if (cudaMemcpyAsync(&host, ds->err, sizeof host, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return PA_ERR_CUDA;
+    if (clear && cudaMemsetAsync(ds->err, 0, sizeof(uint32_t), st) != cudaSuccess)
+        return PA_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess)
+        return PA_ERR_CUDA;
+    *bits = host;
+    return host ? PA_ERR_DEVICE : PA_OK;
+}
+
+}  // extern "C"

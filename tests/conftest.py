@@ -25,3 +25,25 @@ def pytest_collection_modifyitems(config, items):
     for it in items:
         if "gpu" in it.keywords:
             it.add_marker(skip)
+
+
+@pytest.fixture(scope="session")
+def pa():
+    """The CUDA library's binding, built in-tree first (no fallback if that fails)."""
+    from paged_kv_cache_260_gb300 import _build
+    _build.build()
+    import paged_kv_cache_260_gb300 as m
+    m.load()
+    return m
+
+
+@pytest.fixture(autouse=True)
+def _device_errors_clear(request):
+    """GPU tests start with the library's device error bits cleared."""
+    if "gpu" in request.keywords:
+        import torch
+        if torch.cuda.is_available():
+            import paged_kv_cache_260_gb300 as m
+            if m._lib is not None:
+                m.get_device_error(clear=True)
+    yield

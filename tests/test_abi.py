@@ -1,0 +1,102 @@
+"""The C-ABI library builds, loads and exports every entry point its header
+declares; host-side argument checks return their status codes without
+touching a GPU (all these calls fail validation before any CUDA call)."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_kv_cache_260_gb300 import _build
+    import paged_kv_cache_260_gb300 as pa
+    _build.build()
+    return pa.load()
+
+
+def declared_symbols():
+    syms = set()
+    inc = os.path.join(ROOT, "include")
+    for name in os.listdir(inc):
+        if name.endswith(".h"):
+            text = open(os.path.join(inc, name)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            syms |= set(re.findall(r"\b(pa_[a-z0-9_]+)\s*\(", text))
+    return syms
+
+
+def test_header_declares_the_boundary():
+    syms = declared_symbols()
+    for s in ("pa_decode", "pa_reshape_and_cache", "pa_copy_blocks", "pa_decode_workspace_size",
+              "pa_gather_kv", "pa_validate_tables", "pa_get_device_error", "pa_status_string",
+              "pa_version"):
+        assert s in syms
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for s in declared_symbols():
+        assert hasattr(lib, s), s
+
+
+def test_version_and_status_strings(lib):
+    assert lib.pa_version() == 1
+    assert lib.pa_status_string(0) == b"ok"
+    assert lib.pa_status_string(3) == b"workspace missing or too small"
+
+
+def _decode(lib, **kw):
+    a = dict(out=None, q=None, k=None, v=None, tables=None, lens=None, num_seqs=4, num_heads=8,
+             num_kv_heads=2, head_dim=128, block_size=16, max_blocks=8, num_blocks=64, scale=0.1,
+             dtype=0, partition_size=0, ws=None, ws_bytes=0, stream=None)
+    a.update(kw)
+    return lib.pa_decode(a["out"], a["q"], a["k"], a["v"], a["tables"], a["lens"], a["num_seqs"],
+                         a["num_heads"], a["num_kv_heads"], a["head_dim"], a["block_size"],
+                         a["max_blocks"], a["num_blocks"], C.c_float(a["scale"]), a["dtype"],
+                         a["partition_size"], a["ws"], a["ws_bytes"], a["stream"])
+
+
+def test_decode_rejects_bad_scalars(lib):
+    assert _decode(lib, head_dim=96) == 2              # PA_ERR_UNSUPPORTED
+    assert _decode(lib, block_size=32) == 2
+    assert _decode(lib, dtype=7) == 2
+    assert _decode(lib, num_heads=7) == 1              # not a multiple of kv heads
+    assert _decode(lib, num_heads=20) == 2             # group 10 > 8
+    assert _decode(lib, scale=float("nan")) == 1
+    assert _decode(lib, num_seqs=-1) == 1
+    assert _decode(lib, num_seqs=0) == 0               # nothing to do
+    assert _decode(lib) == 1                           # null pointers
+    fake = C.c_void_p(0x1000)
+    assert _decode(lib, out=fake, q=C.c_void_p(0x1008), k=fake, v=fake, tables=fake,
+                   lens=fake) == 1                     # misaligned q
+
+
+def test_cache_entry_points_reject_bad_scalars(lib):
+    assert lib.pa_reshape_and_cache(None, None, None, None, None, 4, 8, 96, 16, 64, 0, None) == 2
+    assert lib.pa_reshape_and_cache(None, None, None, None, None, -1, 8, 64, 16, 64, 0, None) == 1
+    assert lib.pa_reshape_and_cache(None, None, None, None, None, 0, 8, 64, 16, 64, 0, None) == 0
+    assert lib.pa_reshape_and_cache(None, None, None, None, None, 4, 8, 64, 16, 64, 0, None) == 1
+    assert lib.pa_copy_blocks(None, None, None, 3, 8, 128, 8, 64, 0, None) == 2
+    assert lib.pa_copy_blocks(None, None, None, 3, 8, 128, 16, 64, 0, None) == 1
+    assert lib.pa_copy_blocks(None, None, None, 0, 8, 128, 16, 64, 1, None) == 0
+    assert lib.pa_gather_kv(None, None, None, None, None, None, 2, 8, 128, 16, 4, 64, 0, None) == 1
+    assert lib.pa_validate_tables(None, None, 2, 4, 64, 16, None, None) == 1
+    assert lib.pa_validate_tables(None, None, 2, 4, 64, 8, None, None) == 2
+
+
+def test_fixed_partition_workspace_size(lib):
+    # m and l: S*Hq*P floats each, o: S*Hq*P*D floats, each array 256-byte aligned
+    S, Hq, Hkv, D, mb, P = 4, 32, 8, 128, 8192, 512
+    pmax = (mb * 16 + P - 1) // P
+    rows = S * Hq * pmax
+
+    def up(x):
+        return (x + 255) // 256 * 256
+
+    want = up(up(up(4 * rows) + 4 * rows) + 4 * rows * D)
+    assert lib.pa_decode_workspace_size(S, Hq, Hkv, D, mb, P) == want
+    assert lib.pa_decode_workspace_size(S, Hq, Hkv, D, mb, -1) == 0
+    assert lib.pa_decode_workspace_size(S, Hq, Hkv, D, mb, 24) == 0     # not a multiple of 16

@@ -1,0 +1,234 @@
+"""GPU parity of paged decode attention against the fp64 oracle.
+
+Every case runs the whole decode step through the C ABI on seeded inputs in
+which slots holding no live token are NaN (so any over-read or wrong-table
+read shows), and compares element by element within the stated tolerance:
+max |err| <= 4e-3 for fp16 outputs, 1.6e-2 for bf16.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from gpu_util import TOL, DevWorkload, dev_bits, host_bits, max_err, to_f64
+
+pytestmark = pytest.mark.gpu
+
+MODES = [-1, 0, 16, 64, 512]          # no split, balanced split, fixed partitions
+
+
+def check(pa, w, partition_size=0, ws=None):
+    dw = DevWorkload(w)
+    dw.step(pa, partition_size=partition_size, workspace=ws)
+    ref, k_ref, v_ref = oracle.step(w)
+    err = max_err(dw.out, ref)
+    assert err <= TOL[w.dtype], f"max|err| {err}"
+    assert pa.get_device_error() == 0
+    return dw, ref
+
+
+LENS = [0, 1, 2, 15, 16, 17, 31, 33, 100, 257, 700, 1029]
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("Hq,Hkv,D,dtype", [
+    (8, 8, 64, "f16"), (8, 8, 128, "bf16"), (8, 4, 128, "f16"), (12, 4, 64, "bf16"),
+    (16, 4, 128, "bf16"), (10, 2, 128, "f16"), (12, 2, 64, "f16"), (14, 2, 128, "bf16"),
+    (16, 2, 128, "f16"), (8, 1, 64, "bf16")])
+def test_decode_ragged(pa, mode, Hq, Hkv, D, dtype):
+    w = synth.build("ragged", len(LENS), Hq, Hkv, D, dtype, LENS, seed=100 + Hq + D, append=True,
+                    poison=True)
+    check(pa, w, mode)
+
+
+@pytest.mark.parametrize("name", ["tiny", "mha7b", "gqa8b", "parsamp"])
+def test_configs_reduced(pa, name):
+    if name == "tiny":
+        w = synth.tiny(poison=True)
+    elif name == "mha7b":
+        w = synth.mha7b(poison=True, num_seqs=8)
+    elif name == "gqa8b":
+        w = synth.gqa8b(poison=True, num_seqs=32)
+    else:
+        w = synth.parsamp(poison=True, num_prompts=2, samples=8)
+    for mode in (0, -1, 512):
+        check(pa, w, mode)
+
+
+def test_long_reduced_split_k(pa):
+    w = synth.long(poison=True, lens=(4096, 8192, 12288 + 5, 16384 - 7))
+    check(pa, w, 512)
+    check(pa, w, 0)
+
+
+def test_seq_len_one_returns_v_exactly(pa):
+    w = synth.build("one", 6, 16, 4, 128, "bf16", [1] * 6, seed=3)
+    dw = DevWorkload(w)
+    pa.decode(dw.out, dw.q, dw.k, dw.v, dw.tables, dw.lens, w.scale)
+    out = host_bits(dw.out)
+    for s in range(6):
+        for h in range(16):
+            assert np.array_equal(out[s, h], w.v_cache[w.block_tables[s, 0], h // 4, 0])
+
+
+def test_identical_keys_give_mean_of_v(pa):
+    w = synth.build("same", 4, 8, 2, 128, "f16", [5, 40, 333, 1000], seed=4)
+    w.k_cache = w.k_cache.copy()
+    w.k_cache[:] = w.k_cache[0, :, 0:1, :]
+    dw = DevWorkload(w)
+    pa.decode(dw.out, dw.q, dw.k, dw.v, dw.tables, dw.lens, w.scale)
+    got = to_f64(dw.out)
+    for s, L in enumerate(w.seq_lens):
+        _, vv = oracle.gather_kv(w.k_cache, w.v_cache, w.block_tables, s, int(L))
+        mean = oracle.decode_bits(vv, "f16").mean(axis=1)
+        for h in range(8):
+            assert np.abs(got[s, h] - mean[h // 4]).max() <= TOL["f16"]
+
+
+def test_block_permutation_is_bit_exact(pa):
+    w = synth.build("perm", 5, 16, 4, 128, "bf16", [3, 64, 300, 999, 17], seed=8, pool_factor=2.0)
+    dw = DevWorkload(w)
+    pa.decode(dw.out, dw.q, dw.k, dw.v, dw.tables, dw.lens, w.scale)
+    base = dw.out.clone()
+    perm = np.random.default_rng(1).permutation(w.num_blocks)
+    k2 = np.empty_like(w.k_cache)
+    v2 = np.empty_like(w.v_cache)
+    k2[perm] = w.k_cache
+    v2[perm] = w.v_cache
+    t2 = np.where(w.block_tables >= 0, perm[np.maximum(w.block_tables, 0)], -1).astype(np.int32)
+    out2 = torch.empty_like(dw.q)
+    pa.decode(out2, dw.q, dev_bits(k2, "bf16"), dev_bits(v2, "bf16"),
+              torch.from_numpy(t2).cuda(), dw.lens, w.scale)
+    assert torch.equal(out2, base)
+
+
+def test_cow_remap_is_bit_exact(pa):
+    w = synth.parsamp(num_prompts=2, samples=8, prompt_len=64, max_suffix=40)
+    dw = DevWorkload(w)
+    pa.reshape_and_cache(dw.k_new, dw.v_new, dw.k, dw.v, dw.slots)
+    before = torch.empty_like(dw.q)
+    pa.decode(before, dw.q, dw.k, dw.v, torch.from_numpy(w.tables_before_cow).cuda(), dw.lens,
+              w.scale)
+    pa.copy_blocks(dw.k, dw.v, dw.pairs)
+    pa.decode(dw.out, dw.q, dw.k, dw.v, dw.tables, dw.lens, w.scale)
+    assert torch.equal(before, dw.out)
+
+
+def test_cow_unaligned_prefix_no_crosstalk(pa):
+    kw = dict(num_prompts=2, samples=4, prompt_len=40, suffix_lens=[0] * 8, num_heads=8,
+              num_kv_heads=2, head_dim=128, poison=True)
+    w = synth.parsamp(**kw)
+    dw, ref = check(pa, w, 0)
+    w2 = synth.parsamp(**kw)
+    w2.k_new = w2.k_new.copy()
+    w2.k_new[5] = synth.to_bits(np.full(w2.k_new[5].shape, 2.0, np.float32), "f16")
+    dw2, ref2 = check(pa, w2, 0)
+    diff = (dw.out != dw2.out).flatten(1).any(1).cpu().numpy()
+    assert diff.tolist() == [s == 5 for s in range(8)]
+
+
+def test_fixed_partials_match_oracle(pa):
+    P = 64
+    w = synth.build("parts", 5, 16, 4, 128, "f16", [17, 64, 65, 300, 1000], seed=12, poison=True)
+    dw = DevWorkload(w)
+    ws = pa.workspace_for(dw.q, dw.k, dw.tables, P)
+    pa.decode(dw.out, dw.q, dw.k, dw.v, dw.tables, dw.lens, w.scale, partition_size=P,
+              workspace=ws)
+    torch.cuda.synchronize()
+    S, Hq, D = w.q.shape
+    pmax = -(-w.max_blocks_per_seq * 16 // P)
+    rows = S * Hq * pmax
+
+    def up(x):
+        return (x + 255) // 256 * 256
+
+    raw = ws.cpu().numpy()
+    l_off = up(4 * rows)
+    o_off = up(l_off + 4 * rows)
+    gm = raw[:4 * rows].view(np.float32).reshape(S, Hq, pmax)
+    gl = raw[l_off:l_off + 4 * rows].view(np.float32).reshape(S, Hq, pmax)
+    go = raw[o_off:o_off + 4 * rows * D].view(np.float32).reshape(S, Hq, pmax, D)
+    m, l, o = oracle.partials(w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.scale,
+                              "f16", P, max_partitions=pmax)
+    for s, L in enumerate(w.seq_lens):
+        n = -(-int(L) // P)
+        if n <= 1:
+            continue                      # a single partition is written as the output itself
+        np.testing.assert_allclose(gm[s, :, :n], m[s, :, :n], rtol=1e-5, atol=1e-5)
+        np.testing.assert_allclose(gl[s, :, :n], l[s, :, :n], rtol=1e-4, atol=1e-5)
+        np.testing.assert_allclose(go[s, :, :n], o[s, :, :n], rtol=0, atol=2e-4)
+
+
+def test_single_partition_equals_no_split(pa):
+    w = synth.build("one_part", 6, 32, 8, 128, "bf16", [5, 16, 100, 511, 512, 300], seed=13)
+    dw = DevWorkload(w)
+    pa.decode(dw.out, dw.q, dw.k, dw.v, dw.tables, dw.lens, w.scale, partition_size=-1)
+    a = dw.out.clone()
+    pa.decode(dw.out, dw.q, dw.k, dw.v, dw.tables, dw.lens, w.scale, partition_size=512)
+    assert torch.equal(a, dw.out)
+
+
+def test_repeatable(pa):
+    w = synth.gqa8b(num_seqs=24)
+    dw = DevWorkload(w)
+    pa.decode(dw.out, dw.q, dw.k, dw.v, dw.tables, dw.lens, w.scale)
+    a = dw.out.clone()
+    pa.decode(dw.out, dw.q, dw.k, dw.v, dw.tables, dw.lens, w.scale)
+    assert torch.equal(a, dw.out)
+
+
+def test_all_empty_and_zero_scale(pa):
+    w = synth.build("empty", 3, 8, 2, 64, "f16", [0, 0, 0], seed=1, pool_blocks=4, max_blocks=2)
+    dw = DevWorkload(w)
+    dw.out.fill_(1.0)
+    pa.decode(dw.out, dw.q, dw.k, dw.v, dw.tables, dw.lens, w.scale)
+    assert torch.count_nonzero(dw.out) == 0
+    w = synth.build("scale0", 3, 8, 2, 64, "f16", [7, 70, 700], seed=2, scale=0.0)
+    check(pa, w, 0)
+
+
+def test_many_short_sequences(pa):
+    rng = np.random.default_rng(5)
+    lens = rng.integers(0, 40, size=3000)
+    w = synth.build("many", 3000, 8, 1, 64, "bf16", lens, seed=6, poison=True)
+    check(pa, w, 0)
+    check(pa, w, -1)
+
+
+def test_bad_table_entry_is_flagged_not_faulting(pa):
+    w = synth.build("badtab", 3, 8, 2, 64, "f16", [20, 40, 60], seed=9)
+    w.block_tables = w.block_tables.copy()
+    w.block_tables[1, 1] = w.num_blocks + 100
+    dw = DevWorkload(w)
+    pa.decode(dw.out, dw.q, dw.k, dw.v, dw.tables, dw.lens, w.scale)
+    assert pa.get_device_error() & pa.DEVERR["TABLE_RANGE"]
+
+
+def test_bad_seq_len_is_flagged(pa):
+    w = synth.build("badlen", 3, 8, 2, 64, "f16", [20, 40, 60], seed=9)
+    dw = DevWorkload(w)
+    dw.lens[1] = 10 ** 6
+    pa.decode(dw.out, dw.q, dw.k, dw.v, dw.tables, dw.lens, w.scale)
+    assert pa.get_device_error() & pa.DEVERR["SEQLEN_RANGE"]
+
+
+def test_workspace_too_small(pa):
+    w = synth.build("ws", 3, 8, 2, 64, "f16", [20, 400, 60], seed=9)
+    dw = DevWorkload(w)
+    small = torch.empty(256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(pa.PagedAttnError) as e:
+        pa.decode(dw.out, dw.q, dw.k, dw.v, dw.tables, dw.lens, w.scale, partition_size=64,
+                  workspace=small)
+    assert e.value.status == 3
+
+
+def test_other_stream(pa):
+    w = synth.gqa8b(num_seqs=8, poison=True)
+    dw = DevWorkload(w)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        dw.step(pa)
+    s.synchronize()
+    ref, _, _ = oracle.step(w)
+    assert max_err(dw.out, ref) <= TOL["bf16"]
