@@ -278,8 +278,9 @@ class Step:
     def capture(self, steps_per_graph: int):
         """Capture `steps_per_graph` steps, with events around each decode."""
         import torch
-        self.ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                   for _ in range(steps_per_graph)]
+        # external events become event-record nodes of the graph, so each
+        # replay timestamps every decode
+        self.ev = [(timing_event(), timing_event()) for _ in range(steps_per_graph)]
         s = torch.cuda.Stream(self.dev)
         s.wait_stream(torch.cuda.current_stream(self.dev))
         with torch.cuda.stream(s):
