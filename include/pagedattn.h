@@ -126,6 +126,37 @@ int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache
               void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * pa_decode without a workspace argument, for callers that cannot allocate
+ * device memory: an engine that gives (nearly) all free HBM to its KV block
+ * pool at start-up and forbids allocations afterwards, a plugin whose host
+ * framework hands it only inputs and outputs, or code running where
+ * cudaMalloc is not allowed.  The pages describe no such entry point; it has
+ * no counterpart there.
+ *
+ * Same arguments, result and split as pa_decode with partition_size = 0
+ * (balanced split).  The split-K scratch is a fixed device array of
+ * PA_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that loads the
+ * library holds until the process exits; this call allocates nothing.
+ *   - Sizes whose scratch would exceed PA_NOALLOC_SCRATCH_BYTES (see
+ *     pa_decode_workspace_size(..., partition_size = 0)) return
+ *     PA_ERR_WORKSPACE.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture on the device.
+ *   - All calls on a device share the one array and it keeps what the last
+ *     call left in it: calls that can overlap on the GPU (different streams,
+ *     no ordering between them) race and corrupt each other's results.  Order
+ *     them on one stream.
+ */
+#define PA_NOALLOC_SCRATCH_BYTES (4u << 20)
+
+int pa_decode_noalloc(void *out, const void *q, const void *k_cache, const void *v_cache,
+                      const int32_t *block_tables, const int32_t *seq_lens,
+                      int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                      int block_size, int max_blocks_per_seq, int num_blocks,
+                      float scale, int dtype, void *stream);
+
+/*
  * Write each new token's K and V into its pool slot: for token i with
  * slot = slot_mapping[i] >= 0, for every kv head h,
  *     k_cache[slot / 16][h][slot % 16][:] = k_new[i][h][:]   (same for V).

@@ -17,6 +17,7 @@ import threading
 
 __all__ = [
     "PagedAttnError", "load", "version", "decode", "decode_workspace_size", "workspace_for",
+    "decode_noalloc",
     "reshape_and_cache", "copy_blocks", "gather_kv", "validate_tables", "get_device_error",
     "PA_DTYPE_F16", "PA_DTYPE_BF16", "DEVERR", "STATUS",
 ]
@@ -61,6 +62,8 @@ def load(path: str = LIB_PATH):
         L.pa_decode_workspace_size.argtypes = [i, i, i, i, i, i]
         L.pa_decode.restype = i
         L.pa_decode.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, i, vp, sz, vp]
+        L.pa_decode_noalloc.restype = i
+        L.pa_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, vp]
         L.pa_reshape_and_cache.restype = i
         L.pa_reshape_and_cache.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, vp]
         L.pa_copy_blocks.restype = i
@@ -160,6 +163,26 @@ def decode(out, q, k_cache, v_cache, block_tables, seq_lens, scale, partition_si
                           float(scale), _dtype_code(q), int(partition_size), _ptr(workspace),
                           wbytes, _stream(stream))
     _check("pa_decode", rc)
+    return out
+
+
+def decode_noalloc(out, q, k_cache, v_cache, block_tables, seq_lens, scale, stream=None):
+    """pa_decode_noalloc: decode with the library's own fixed scratch (balanced split).
+
+    For callers that cannot allocate a workspace.  Calls share one scratch
+    array per device, so calls that may overlap on the GPU must be ordered on
+    one stream; the first call on a device must come before any stream capture.
+    """
+    n, hq, d = q.shape
+    nb, hkv, bs, d2 = k_cache.shape
+    _require(out.shape == q.shape and d2 == d and v_cache.shape == k_cache.shape, "shapes")
+    _require(block_tables.dim() == 2 and block_tables.shape[0] == n and seq_lens.shape == (n,),
+             "table shapes")
+    rc = load().pa_decode_noalloc(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                  _ptr(block_tables), _ptr(seq_lens), n, hq, hkv, d, bs,
+                                  block_tables.shape[1], nb, float(scale), _dtype_code(q),
+                                  _stream(stream))
+    _check("pa_decode_noalloc", rc)
     return out
 
 
