@@ -1,6 +1,8 @@
 // pa_api.cu -- the C ABI declared in include/pagedattn.h: host-side argument
 // checks, per-device state and kernel dispatch.  Nothing here allocates
 // device memory or synchronises, except pa_get_device_error().
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <math.h>
 #include <mutex>
 #include <stdint.h>
@@ -113,6 +115,44 @@ int occupancy(const void *func, int dev, int threads, size_t smem, int *blocks)
         g_occ[g_occ_count++] = OccEntry{func, dev, smem, nb};
     *blocks = nb;
     return PA_OK;
+}
+
+// cuTensorMapEncodeTiled, reached through the runtime so the library needs no
+// direct link against the driver library.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+// The pool seen as a 2-D array [num_blocks * num_kv_heads * 16 rows][head_dim]
+// of 16-bit elements, read in boxes of 16 rows x 64 columns (128 bytes) with
+// the 128-byte swizzle.  One box row is one token's 64 channels.
+int make_pool_map(CUtensorMap *tm, const void *pool, int dtype, int head_dim, long long rows)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc)
+        return PA_ERR_CUDA;
+    const cuuint64_t gdim[2] = {(cuuint64_t)head_dim, (cuuint64_t)rows};
+    const cuuint64_t gstride[1] = {(cuuint64_t)head_dim * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)kBlockSize};
+    const cuuint32_t estride[2] = {1, 1};
+    const CUresult r = enc(tm,
+                           dtype == PA_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                  : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                           2, const_cast<void *>(pool), gdim, gstride, box, estride,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
 }
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -248,9 +288,10 @@ int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache
     if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
         !aligned(block_tables, 4) || !aligned(seq_lens, 4))
         return PA_ERR_INVALID_ARG;
-    // flat tile indices are 32-bit
+    // flat tile indices and tensor-map row coordinates are 32-bit
+    const long long pool_rows = (long long)num_blocks * num_kv_heads * kBlockSize;
     if ((long long)num_seqs * max_blocks_per_seq * num_kv_heads >= (1LL << 31) ||
-        (long long)max_blocks_per_seq * kBlockSize >= (1LL << 30))
+        (long long)max_blocks_per_seq * kBlockSize >= (1LL << 30) || pool_rows >= (1LL << 31))
         return PA_ERR_UNSUPPORTED;
     int mode, pt;
     rc = decode_mode(partition_size, &mode, &pt);
@@ -318,14 +359,22 @@ int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache
     p.grid = grid;
     p.scale_log2 = scale * 1.4426950408889634f;
 
+    CUtensorMap tmk, tmv;
+    rc = make_pool_map(&tmk, k_cache, dtype, head_dim, pool_rows);
+    if (rc == PA_OK)
+        rc = make_pool_map(&tmv, v_cache, dtype, head_dim, pool_rows);
+    if (rc != PA_OK)
+        return rc;
+
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    void *args[] = {&p};
+    void *args[] = {&p, &tmk, &tmv};
     cudaError_t e = cudaLaunchKernel(ks.decode, dim3(grid), dim3(ks.warps * 32), args, smem, st);
     if (e != cudaSuccess)
         return PA_ERR_CUDA;
     const bool needs_merge = mode == kModeBalanced || (mode == kModeFixed && p_max > 1);
     if (needs_merge) {
-        e = cudaLaunchKernel(ks.merge, dim3(num_seqs * num_kv_heads), dim3(128), args, 0, st);
+        void *margs[] = {&p};
+        e = cudaLaunchKernel(ks.merge, dim3(num_seqs * num_kv_heads), dim3(128), margs, 0, st);
         if (e != cudaSuccess)
             return PA_ERR_CUDA;
     }

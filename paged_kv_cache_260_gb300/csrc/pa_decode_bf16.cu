@@ -1,5 +1,5 @@
 // pa_decode_bf16.cu -- bf16 instantiations of the decode and merge kernels.
-#include "pa_decode.cuh"
+#include "pa_decode_mma.cuh"
 
 namespace pa {
 bool decode_kernels_bf16(int head_dim, int group, KernelSet *ks)

@@ -1,5 +1,5 @@
 // pa_decode_f16.cu -- fp16 instantiations of the decode and merge kernels.
-#include "pa_decode.cuh"
+#include "pa_decode_mma.cuh"
 
 namespace pa {
 bool decode_kernels_f16(int head_dim, int group, KernelSet *ks)
