@@ -137,7 +137,7 @@ def decode_source_hash() -> str:
     """Hash of the decode kernel sources: ncu counters apply only to this build."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_cache_260_gb300", "csrc")
-    for name in ("pa_decode.cuh", "pa_device.cuh", "pa_internal.h"):
+    for name in ("pa_decode_mma.cuh", "pa_schedule.cuh", "pa_device.cuh", "pa_internal.h"):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -253,12 +253,13 @@ class Step:
         self.ev = None
 
     def _count_launches(self):
-        n = 1                                           # decode kernel
+        n = 1                                           # decode
         n += int(self.pairs is not None)                # copy_blocks
         n += int(self.slots is not None)                # reshape_and_cache
-        maxlen = self.tables.shape[1] * 16
-        if self.ps == 0 or (self.ps > 0 and maxlen > self.ps):
-            n += 1                                      # log-sum-exp merge
+        if self.ps >= 0:
+            n += 1                                      # merge of cut runs / partitions
+        if self.ps > 0 and self.tables.shape[1] * 16 > self.ps:
+            n += 1                                      # merge of partitions per run
         return n
 
     def run(self, ev_pair=None):
@@ -491,7 +492,7 @@ def run_ours(args):
         },
         "e2e": {"value": total_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "roofline": {"bound": "hbm", "kernel": "pa_decode (decode kernel + split-K merge)",
+        "roofline": {"bound": "hbm", "kernel": "pa_decode: decode_mma_kernel + merge kernel(s)",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs, copy burst)"
                      if peak_src == "measured" else "fallback 6.8 TB/s",

@@ -98,25 +98,30 @@ size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads,
  *
  * Split-K along the sequence (FlashDecoding, ICML tutorial notes, section
  * "内核优化"), chosen by partition_size:
- *   -1  no split: one thread block reduces each (sequence, kv head) whole;
- *    0  balanced split: the grid is sized to the GPU and every thread block
- *       gets the same number of 16-token tiles; (sequence, kv head) runs cut
- *       by a tile-range boundary are finished by a log-sum-exp merge;
+ *   -1  no split: one warp reduces each (sequence, kv head) run whole;
+ *    0  balanced split: the grid is sized to the GPU and every warp gets the
+ *       same number of 16-token tiles; runs cut by a tile-range boundary are
+ *       finished by a log-sum-exp merge;
  *   >0  fixed partitions of partition_size tokens (a multiple of 16); each
  *       partition's partial result is merged with the log-sum-exp rule
  *           M = max_p m_p,  w_p = l_p exp(m_p - M),  o = sum_p w_p o_p / sum_p w_p.
- *       The partials are left in the workspace, fp32, as three arrays each
- *       starting at a 256-byte boundary:
+ *       The partials are left at the start of the workspace, fp32, as three
+ *       arrays each starting at a 256-byte boundary:
  *           m [num_seqs][num_heads][P_max]  max of the partition's scaled scores
  *           l [num_seqs][num_heads][P_max]  sum_t exp(score_t - m)
  *           o [num_seqs][num_heads][P_max][head_dim]  normalised partial output
  *       P_max = ceil(max_blocks_per_seq * 16 / partition_size); entries of
  *       partitions past a sequence's end, and of sequences that fit one
- *       partition, are not written.
+ *       partition, are not written.  Scratch of the split follows them.
+ *
+ * A split decode is the decode kernel plus one merge kernel (fixed mode with
+ * more than one partition: two).  They are programmatic dependent launches:
+ * each may be scheduled while the kernel before it on the stream drains, and
+ * touches no global memory until that kernel has completed.
  *
  * workspace: device buffer of at least pa_decode_workspace_size(...) bytes,
- * caller-owned, contents need no initialisation.  Calls that share a
- * workspace must be ordered on one stream.
+ * 256-byte aligned, caller-owned; its contents need no initialisation.  Calls
+ * that share a workspace must be ordered on one stream.
  */
 int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
               const int32_t *block_tables, const int32_t *seq_lens,
@@ -148,7 +153,7 @@ int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache
  *     no ordering between them) race and corrupt each other's results.  Order
  *     them on one stream.
  */
-#define PA_NOALLOC_SCRATCH_BYTES (4u << 20)
+#define PA_NOALLOC_SCRATCH_BYTES (16u << 20)
 
 int pa_decode_noalloc(void *out, const void *q, const void *k_cache, const void *v_cache,
                       const int32_t *block_tables, const int32_t *seq_lens,

@@ -9,6 +9,7 @@
 
 #include "pa_cache.h"
 #include "pa_internal.h"
+#include "pa_schedule.cuh"
 #include "pagedattn.h"
 
 namespace pa {
@@ -155,6 +156,22 @@ int make_pool_map(CUtensorMap *tm, const void *pool, int dtype, int head_dim, lo
     return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
 }
 
+int launch_dependent(const void *func, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                     void **args)
+{
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelExC(&cfg, func, args) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 int check_common(int num_kv_heads, int head_dim, int block_size, int num_blocks, int dtype)
@@ -173,29 +190,41 @@ int check_common(int num_kv_heads, int head_dim, int block_size, int num_blocks,
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? PA_OK : PA_ERR_CUDA; }
 
 struct WorkspaceLayout {
-    size_t m_off, l_off, o_off, prefix_off, total;
-    long long rows;
+    size_t m_off, l_off, o_off, sm_off, sl_off, so_off, desc_off, total;
 };
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Workspace of one decode: partial rows (m, l, o) and, for balanced mode, the
-// per-sequence tile prefix.  rows = num_seqs * num_heads * P_max (fixed) or
-// 2 * grid * group (balanced: at most two cut runs per thread block).
-WorkspaceLayout workspace_layout(int mode, int num_seqs, int num_heads, int group, int head_dim,
-                                 int p_max, int grid)
+// Workspace of one decode, each array starting at a 256-byte boundary:
+//   fixed mode only: m, l, o of every partition, [num_seqs][num_heads][P_max]
+//   (x head_dim for o) -- the documented layout;
+//   both split modes: m, l, o of two slots per worker and query head of the
+//   group (a worker's first and last pieces are the only ones that can be
+//   cut), then one cut descriptor per worker.
+WorkspaceLayout workspace_layout(int mode, int num_seqs, int num_heads, int num_kv_heads,
+                                 int head_dim, int p_max, int workers)
 {
     WorkspaceLayout w{};
     if (mode == kModeWhole)
         return w;
-    w.rows = mode == kModeFixed ? (long long)num_seqs * num_heads * p_max : 2LL * grid * group;
-    w.m_off = 0;
-    w.l_off = round_up(w.m_off + sizeof(float) * w.rows, 256);
-    w.o_off = round_up(w.l_off + sizeof(float) * w.rows, 256);
-    w.prefix_off = round_up(w.o_off + sizeof(float) * w.rows * head_dim, 256);
-    w.total = w.prefix_off;
-    if (mode == kModeBalanced)
-        w.total = round_up(w.prefix_off + sizeof(int32_t) * (num_seqs + 1), 256);
+    const int group = num_heads / num_kv_heads;
+    const size_t prow = mode == kModeFixed ? (size_t)num_seqs * num_heads * p_max : 0;
+    const size_t srow = 2 * (size_t)workers * group;
+    size_t at = 0;
+    w.m_off = at;
+    at = round_up(at + sizeof(float) * prow, 256);
+    w.l_off = at;
+    at = round_up(at + sizeof(float) * prow, 256);
+    w.o_off = at;
+    at = round_up(at + sizeof(float) * prow * head_dim, 256);
+    w.sm_off = at;
+    at = round_up(at + sizeof(float) * srow, 256);
+    w.sl_off = at;
+    at = round_up(at + sizeof(float) * srow, 256);
+    w.so_off = at;
+    at = round_up(at + sizeof(float) * srow * head_dim, 256);
+    w.desc_off = at;
+    w.total = round_up(at + sizeof(CutDesc) * workers, 256);
     return w;
 }
 
@@ -252,16 +281,15 @@ size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, i
     if (num_seqs <= 0 || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads ||
         max_blocks_per_seq <= 0 || decode_mode(partition_size, &mode, &pt) != PA_OK)
         return 0;
-    int grid = 0;
-    if (mode == kModeBalanced) {
+    int workers = 0;
+    if (mode != kModeWhole) {
         DeviceState *ds;
         if (device_state(&ds) != PA_OK)
             return 0;
-        grid = ds->num_sms * kMaxBlocksPerSM;
+        workers = ds->num_sms * kMaxWarpsPerSM;
     }
     const int p_max = mode == kModeFixed ? (max_blocks_per_seq + pt - 1) / pt : 1;
-    return workspace_layout(mode, num_seqs, num_heads, num_heads / num_kv_heads, head_dim, p_max,
-                            grid)
+    return workspace_layout(mode, num_seqs, num_heads, num_kv_heads, head_dim, p_max, workers)
         .total;
 }
 
@@ -309,25 +337,34 @@ int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache
         return rc;
     int dev = 0;
     cudaGetDevice(&dev);
-    const size_t smem = decode_smem_bytes(ks, num_seqs);
+    int var = 0;
+    size_t smem = decode_smem_bytes(ks.smem_fixed[0], num_seqs);
+    if (smem > ds->smem_optin) {
+        var = 1;
+        smem = decode_smem_bytes(ks.smem_fixed[1], num_seqs);
+    }
     if (smem > ds->smem_optin)
         return PA_ERR_UNSUPPORTED;
-    rc = ensure_smem(ks.decode, dev, smem);
+    const void *decode_fn = ks.decode[var];
+    const int warps = ks.warps[var];
+    rc = ensure_smem(decode_fn, dev, smem);
     if (rc != PA_OK)
         return rc;
     int per_sm = 0;
-    rc = occupancy(ks.decode, dev, ks.warps * 32, smem, &per_sm);
+    rc = occupancy(decode_fn, dev, warps * 32, smem, &per_sm);
     if (rc != PA_OK)
         return rc;
     if (per_sm < 1)
         return PA_ERR_UNSUPPORTED;
-    if (per_sm > kMaxBlocksPerSM)
-        per_sm = kMaxBlocksPerSM;
+    if (per_sm * warps > kMaxWarpsPerSM)
+        per_sm = kMaxWarpsPerSM / warps;
     const int grid = ds->num_sms * per_sm;
+    const int workers = grid * warps;
     const int p_max = mode == kModeFixed ? (max_blocks_per_seq + pt - 1) / pt : 1;
-    const WorkspaceLayout wl = workspace_layout(mode, num_seqs, num_heads, group, head_dim, p_max,
-                                                mode == kModeBalanced ? ds->num_sms * kMaxBlocksPerSM
-                                                                      : grid);
+    // sized for the most workers any call on this device can use, so the
+    // size does not depend on the launch configuration chosen here
+    const WorkspaceLayout wl = workspace_layout(mode, num_seqs, num_heads, num_kv_heads, head_dim,
+                                                p_max, ds->num_sms * kMaxWarpsPerSM);
     if (wl.total > 0 && (!workspace || workspace_bytes < wl.total || !aligned(workspace, 256)))
         return PA_ERR_WORKSPACE;
 
@@ -343,8 +380,10 @@ int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache
         p.ws_m = reinterpret_cast<float *>(ws + wl.m_off);
         p.ws_l = reinterpret_cast<float *>(ws + wl.l_off);
         p.ws_o = reinterpret_cast<float *>(ws + wl.o_off);
-        p.ws_prefix = mode == kModeBalanced ? reinterpret_cast<int32_t *>(ws + wl.prefix_off)
-                                            : nullptr;
+        p.ws_sm = reinterpret_cast<float *>(ws + wl.sm_off);
+        p.ws_sl = reinterpret_cast<float *>(ws + wl.sl_off);
+        p.ws_so = reinterpret_cast<float *>(ws + wl.so_off);
+        p.ws_desc = reinterpret_cast<CutDesc *>(ws + wl.desc_off);
     }
     p.err = ds->err;
     p.num_seqs = num_seqs;
@@ -356,7 +395,7 @@ int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache
     p.part_tiles = pt;
     p.p_max = p_max;
     p.min_tiles = kMinTiles;
-    p.grid = grid;
+    p.workers = workers;
     p.scale_log2 = scale * 1.4426950408889634f;
 
     CUtensorMap tmk, tmv;
@@ -366,19 +405,20 @@ int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache
     if (rc != PA_OK)
         return rc;
 
+    // Every kernel here is a programmatic dependent launch: its blocks may be
+    // scheduled while the preceding kernel on the stream drains, and they
+    // touch no global memory before that kernel has completed.
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     void *args[] = {&p, &tmk, &tmv};
-    cudaError_t e = cudaLaunchKernel(ks.decode, dim3(grid), dim3(ks.warps * 32), args, smem, st);
-    if (e != cudaSuccess)
-        return PA_ERR_CUDA;
-    const bool needs_merge = mode == kModeBalanced || (mode == kModeFixed && p_max > 1);
-    if (needs_merge) {
-        void *margs[] = {&p};
-        e = cudaLaunchKernel(ks.merge, dim3(num_seqs * num_kv_heads), dim3(128), margs, 0, st);
-        if (e != cudaSuccess)
-            return PA_ERR_CUDA;
-    }
-    return PA_OK;
+    rc = launch_dependent(decode_fn, dim3(grid), dim3(warps * 32), smem, st, args);
+    if (rc != PA_OK || mode == kModeWhole)
+        return rc;
+    void *margs[] = {&p};
+    rc = launch_dependent(ks.merge_cut, dim3(workers), dim3(256), 0, st, margs);
+    if (rc != PA_OK || mode != kModeFixed || p_max < 2)
+        return rc;
+    return launch_dependent(ks.merge_part, dim3(num_seqs * num_heads), dim3(head_dim), 0, st,
+                            margs);
 }
 
 int pa_reshape_and_cache(const void *k_new, const void *v_new, void *k_cache, void *v_cache,

@@ -17,6 +17,7 @@ reshape_and_cache_kernel(const uint4 *__restrict__ k_new, const uint4 *__restric
                          const int64_t *__restrict__ slot_mapping, int num_tokens,
                          int num_kv_heads, int row_vecs, long long num_slots, uint32_t *err)
 {
+    grid_dependents_launch();   // a dependent decode may be scheduled now; it waits for us
     const long long per_token = (long long)num_kv_heads * row_vecs;   // vectors of K per token
     const long long total = 2LL * num_tokens * per_token;            // K and V
     for (long long x = blockIdx.x * (long long)blockDim.x + threadIdx.x; x < total;
@@ -52,6 +53,7 @@ __global__ void __launch_bounds__(256)
 copy_blocks_kernel(uint4 *k_cache, uint4 *v_cache, const int64_t *__restrict__ block_mapping,
                    int num_pairs, long long block_vecs, long long num_blocks, uint32_t *err)
 {
+    grid_dependents_launch();
     const int pair = blockIdx.y >> 1;
     const bool is_v = blockIdx.y & 1;
     const int64_t src = __ldg(block_mapping + 2 * pair);

@@ -18,9 +18,11 @@
 //    in 64-column boxes with the 128-byte swizzle, so the fragment loads
 //    below hit 8 distinct bank groups; they complete on an mbarrier.
 //  * A persistent grid walks the flat (sequence, kv head, tile) list
-//    (pa_schedule.cuh).  Each warp owns a ring of copy stages and takes every
-//    W-th tile of its block's current run; warps combine their softmax states
-//    in shared memory at the end of a run.
+//    (pa_schedule.cuh).  Every warp is an independent worker with its own
+//    contiguous, equal share of tiles and its own ring of copy stages; warps
+//    never synchronise with each other.  A run that lies in one worker's share
+//    is written straight from registers; the pieces of a cut run go to
+//    per-worker slots and a separate merge kernel combines them.
 //  * One warp serves the whole query group of a kv head (G <= 8), so each K/V
 //    byte leaves HBM once per decode.  Per tile, on the tensor cores:
 //        S[16 tokens x 8 heads] = K[16 x D] . Q^T[D x 8]       (K = A operand)
@@ -56,12 +58,9 @@ template <int D, int W, int S>
 struct MmaLayout {
     using Sh = MmaShape<D>;
     static constexpr size_t stages = (size_t)W * S * Sh::STAGE;
-    static constexpr size_t cm = (size_t)W * 8 * 4;
-    static constexpr size_t cl = cm;
-    static constexpr size_t cacc = (size_t)W * 8 * D * 4;
     static constexpr size_t bars = (size_t)W * S * 8;
     // +1024: the dynamic shared memory base is aligned up to the swizzle atom
-    static constexpr size_t fixed = 1024 + stages + cm + cl + cacc + bars;
+    static constexpr size_t fixed = 1024 + stages + bars;
 };
 
 // Byte offset of the 16-byte chunk `chunk` (0..7) of row `row` inside a
@@ -69,6 +68,21 @@ struct MmaLayout {
 __device__ __forceinline__ uint32_t swz(int row, int chunk)
 {
     return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
+}
+
+// Row of the partial-result arrays (m, l, o) for fixed-mode partition `part`
+// of run (s, h), head g: the documented [num_seqs][num_heads][P_max] layout.
+__device__ __forceinline__ size_t part_row(const DecodeParams &p, int G, int s, int h, int part,
+                                           int g)
+{
+    return ((size_t)s * p.num_heads + h * G + g) * p.p_max + part;
+}
+
+// Row of the slot arrays for worker slot `slot` (2 * worker, +1 for the
+// worker's last piece), head g.
+__device__ __forceinline__ size_t slot_row(int G, int slot, int g)
+{
+    return (size_t)slot * G + g;
 }
 
 template <typename T, int D, int W, int S>
@@ -86,29 +100,28 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
     unsigned char *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
-    unsigned char *stage_base = smem;
-    float *cm = reinterpret_cast<float *>(smem + Lay::stages);
-    float *cl = cm + W * 8;
-    float *cacc = cl + W * 8;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(cacc + W * 8 * D);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Lay::stages);
     int32_t *pre = reinterpret_cast<int32_t *>(bars + W * S);
     int32_t *lens = pre + p.num_seqs + 1;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int n = p.num_seqs, Hkv = p.num_kv_heads, Hq = p.num_heads;
     const int G = Hq / Hkv;
+    const int worker = blockIdx.x * W + warp;
 
     if (lane == 0) {
         for (int st = 0; st < S; ++st)
             mbar_init(smem_addr(&bars[warp * S + st]), 1);
         mbar_init_fence();
     }
-    build_prefix<W>(p, pre, lens);
+    // the merge kernels that follow may be scheduled now; they wait for us
+    grid_dependents_launch();
+    // no global memory is touched before the preceding kernel has completed
+    grid_dependency_wait();
+    build_prefix<W * 32>(p, pre, lens);
     __syncthreads();
 
-    if (p.mode == kModeBalanced && blockIdx.x == 0)
-        for (int s = tid; s <= n; s += W * 32)
-            p.ws_prefix[s] = pre[s];
+    // sequences without tokens get zeros (no piece ever covers them)
     for (int s = blockIdx.x; s < n; s += gridDim.x) {
         if (lens[s] == 0) {
             T *o = reinterpret_cast<T *>(p.out) + (size_t)s * Hq * D;
@@ -119,15 +132,15 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
 
     const uint64_t pol = l2_evict_first_policy();
     const uint32_t bar0 = smem_addr(&bars[warp * S]);
-    unsigned char *wst = stage_base + (size_t)warp * S * Sh::STAGE;
+    unsigned char *wst = smem + (size_t)warp * S * Sh::STAGE;
     const uint32_t wst_addr = smem_addr(wst);
     const int qb_bytes = G * D * 2;
 
     // ---- producer: this warp's tiles, S ahead of the consumer (lane 0 issues) ----
     Walker prod;
-    prod.init(pre, lens, n, Hkv, p.mode, p.part_tiles, p.min_tiles, gridDim.x, blockIdx.x);
+    prod.init(pre, lens, n, Hkv, p.mode, p.part_tiles, p.min_tiles, p.workers, worker);
     Walker cons = prod;
-    int ptile = prod.valid ? prod.tb + warp : 0;
+    int ptile = prod.valid ? prod.tb : 0;
     bool pfirst = true, pdone = !prod.valid;
     auto advance = [&]() {
         while (!pdone && ptile >= prod.te) {
@@ -135,7 +148,7 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
             if (!prod.valid)
                 pdone = true;
             else {
-                ptile = prod.tb + warp;
+                ptile = prod.tb;
                 pfirst = true;
             }
         }
@@ -169,7 +182,7 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
                           qb_bytes, bar);
         }
         pfirst = false;
-        ptile += W;
+        ++ptile;
         advance();
         if (!pdone && lane == 0)
             pphys = __ldg(p.block_tables + (size_t)prod.s * p.max_blocks + ptile);
@@ -193,6 +206,7 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
     int it = 0;
     bool aborted = false;
     int abort_it = 0;
+    CutDesc desc{0, 0, 0, 0, 0, 0, 0, 0};
 
     while (cons.valid) {
         m0 = m1 = -INFINITY;
@@ -205,7 +219,7 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
         const int L = lens[cons.s];
         bool need_q = true;
 
-        for (int tile = cons.tb + warp; tile < cons.te; tile += W) {
+        for (int tile = cons.tb; tile < cons.te; ++tile) {
             const int st = it % S;
             if (!aborted && !mbar_wait_bounded(bar0 + st * 8, (uint32_t)((it / S) & 1))) {
                 aborted = true;
@@ -217,11 +231,11 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
             const uint32_t vst = kst + Sh::TILE;
             if (need_q) {
                 const unsigned char *qs = wst + (size_t)st * Sh::STAGE + 2 * Sh::TILE;
+                const uint32_t *qrow = reinterpret_cast<const uint32_t *>(qs + (size_t)r * D * 2);
 #pragma unroll
                 for (int ks = 0; ks < KS; ++ks) {
-                    const uint32_t *row = reinterpret_cast<const uint32_t *>(qs + (size_t)r * D * 2);
-                    qf[ks][0] = r < G ? row[(16 * ks + 2 * qd) / 2] : 0u;
-                    qf[ks][1] = r < G ? row[(16 * ks + 8 + 2 * qd) / 2] : 0u;
+                    qf[ks][0] = r < G ? qrow[(16 * ks + 2 * qd) / 2] : 0u;
+                    qf[ks][1] = r < G ? qrow[(16 * ks + 8 + 2 * qd) / 2] : 0u;
                 }
                 need_q = false;
             }
@@ -276,7 +290,7 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
             const uint32_t pb0 = movmatrix_trans(M::pack(p0, p1));
             const uint32_t pb1 = movmatrix_trans(M::pack(p2, p3));
 
-            // O^T += V^T . P^T
+            // O^T += V^T . P^T ; value rows past the end are zeroed (0 * NaN is NaN)
             uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
             if (masked) {
                 mlo = (2 * qd < nvalid ? 0x0000ffffu : 0u) | (2 * qd + 1 < nvalid ? 0xffff0000u : 0u);
@@ -300,72 +314,79 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
             ++it;
         }
 
-        // ---- end of piece: combine the warps' states ----
+        // ---- end of piece: write this warp's result ----
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {
             l0 += __shfl_xor_sync(FULL, l0, off);
             l1 += __shfl_xor_sync(FULL, l1, off);
         }
-        if (r == 0) {
-            if (h0 < G) {
-                cm[warp * 8 + h0] = m0;
-                cl[warp * 8 + h0] = l0;
-            }
-            if (h1 < G) {
-                cm[warp * 8 + h1] = m1;
-                cl[warp * 8 + h1] = l1;
-            }
-        }
+        const float inv0 = 1.f / l0, inv1 = 1.f / l1;
+        const int s = cons.s, h = cons.h;
+        if (cons.whole_run()) {
+            T *out = reinterpret_cast<T *>(p.out) + ((size_t)s * Hq + h * G) * D;
 #pragma unroll
-        for (int mt = 0; mt < KS; ++mt) {
-            const int d0 = 16 * mt + r;
-            if (h0 < G) {
-                cacc[(warp * 8 + h0) * D + d0] = o[mt][0];
-                cacc[(warp * 8 + h0) * D + d0 + 8] = o[mt][2];
-            }
-            if (h1 < G) {
-                cacc[(warp * 8 + h1) * D + d0] = o[mt][1];
-                cacc[(warp * 8 + h1) * D + d0 + 8] = o[mt][3];
-            }
-        }
-        __syncthreads();
-        {
-            const bool whole = cons.whole();
-            for (int e = tid; e < G * D; e += W * 32) {
-                const int g = e / D, d = e % D;
-                float Mx = -INFINITY;
-#pragma unroll
-                for (int w = 0; w < W; ++w)
-                    Mx = fmaxf(Mx, cm[w * 8 + g]);
-                float Ls = 0.f, O = 0.f;
-#pragma unroll
-                for (int w = 0; w < W; ++w) {
-                    const float mw = cm[w * 8 + g];
-                    const float f = mw == -INFINITY ? 0.f : exp2f(mw - Mx);
-                    Ls += f * cl[w * 8 + g];
-                    O += f * cacc[(w * 8 + g) * D + d];
+            for (int mt = 0; mt < KS; ++mt) {
+                const int d0 = 16 * mt + r;
+                if (h0 < G) {
+                    out[h0 * D + d0] = E::from_f(o[mt][0] * inv0);
+                    out[h0 * D + d0 + 8] = E::from_f(o[mt][2] * inv0);
                 }
-                const float res = O / Ls;
-                if (whole) {
-                    T *out = reinterpret_cast<T *>(p.out);
-                    out[((size_t)cons.s * Hq + cons.h * G + g) * D + d] = E::from_f(res);
-                } else {
-                    size_t row;
-                    if (p.mode == kModeBalanced)
-                        row = (size_t)(2 * blockIdx.x + (cons.first ? 0 : 1)) * G + g;
-                    else
-                        row = ((size_t)cons.s * Hq + cons.h * G + g) * p.p_max + cons.part;
-                    p.ws_o[row * D + d] = res;
-                    if (d == 0) {
-                        p.ws_m[row] = Mx * kLn2;
-                        p.ws_l[row] = Ls;
-                    }
+                if (h1 < G) {
+                    out[h1 * D + d0] = E::from_f(o[mt][1] * inv1);
+                    out[h1 * D + d0 + 8] = E::from_f(o[mt][3] * inv1);
                 }
             }
+        } else {
+            // a partition (fixed mode) goes to its documented row; a cut piece
+            // to this worker's first or last slot
+            const bool wp = cons.whole_part();
+            const int slot = 2 * worker + (cons.first ? 0 : 1);
+            float *pm = wp ? p.ws_m : p.ws_sm;
+            float *pl = wp ? p.ws_l : p.ws_sl;
+            float *po = wp ? p.ws_o : p.ws_so;
+            const size_t row0 = wp ? part_row(p, G, s, h, cons.part, h0) : slot_row(G, slot, h0);
+            const size_t row1 = wp ? part_row(p, G, s, h, cons.part, h1) : slot_row(G, slot, h1);
+#pragma unroll
+            for (int mt = 0; mt < KS; ++mt) {
+                const int d0 = 16 * mt + r;
+                if (h0 < G) {
+                    po[row0 * D + d0] = o[mt][0] * inv0;
+                    po[row0 * D + d0 + 8] = o[mt][2] * inv0;
+                }
+                if (h1 < G) {
+                    po[row1 * D + d0] = o[mt][1] * inv1;
+                    po[row1 * D + d0 + 8] = o[mt][3] * inv1;
+                }
+            }
+            if (r == 0) {
+                if (h0 < G) {
+                    pm[row0] = m0 * kLn2;
+                    pl[row0] = l0;
+                }
+                if (h1 < G) {
+                    pm[row1] = m1 * kLn2;
+                    pl[row1] = l1;
+                }
+            }
+            // the unit (run, or partition in fixed mode) this piece belongs to
+            const int u0 = cons.F + (p.mode == kModeFixed ? cons.part * cons.pt : 0);
+            const int nu = p.mode == kModeFixed ? min(cons.pt, cons.nt - cons.part * cons.pt) : cons.nt;
+            if (!wp && u0 >= cons.A && u0 + nu > cons.B) {
+                desc.s = s;
+                desc.h = h;
+                desc.part = cons.part;
+                desc.u0 = u0;
+                desc.nu = nu;
+                desc.R = cons.R;
+                desc.np = p.mode == kModeFixed ? (cons.nt + cons.pt - 1) / cons.pt : 1;
+                desc.valid = 1;
+            }
         }
-        __syncthreads();
         cons.next();
     }
+    // every worker leaves a descriptor, valid or not, so none is stale
+    if (p.ws_desc && lane == 0)
+        p.ws_desc[worker] = desc;
 
     // a wait that gave up leaves copies in flight: let them land (bounded)
     if (aborted) {
@@ -375,122 +396,191 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
 }
 
 // ---------------------------------------------------------------------------
-// Log-sum-exp merge of split runs (the rule the split-K partials obey):
-//     M = max_p m_p,  w_p = l_p exp(m_p - M),  out = sum_p w_p o_p / sum_p w_p.
-// One thread block per (sequence, kv head); runs that were not cut return.
+// Log-sum-exp merge of partial results (m_p, l_p, o_p):
+//     M = max_p m_p,  w_p = l_p exp(m_p - M),  out = sum_p w_p o_p / sum_p w_p
+// (split-K along the sequence, FlashDecoding, ICML tutorial notes, section
+// "内核优化").  merge_cut_kernel combines the pieces of each cut unit: one
+// thread block per worker, whose descriptor names the unit starting in its
+// range; warp g takes query head g of the group, each lane D/32 channels,
+// folding the pieces in one pass with a running maximum.  The result is the
+// output (a run) or, in fixed mode, the partition's documented row.
 // ---------------------------------------------------------------------------
 template <typename T, int D>
-__global__ void __launch_bounds__(128) merge_kernel(const DecodeParams p)
+__global__ void __launch_bounds__(256) merge_cut_kernel(const DecodeParams p)
 {
-    using E = Elem<T>;
-    constexpr int CH = 64;            // pieces whose weights are staged at a time
-    __shared__ float sM[8], sW[8];
-    __shared__ float wts[CH][8];
+    constexpr int V = D / 32;
+    constexpr int CH = 8;
+    grid_dependents_launch();
+    grid_dependency_wait();
+    const CutDesc *dp = p.ws_desc + blockIdx.x;
+    const int valid = __ldcg(&dp->valid);
     const int Hkv = p.num_kv_heads, Hq = p.num_heads, G = Hq / Hkv;
-    const int s = blockIdx.x / Hkv, h = blockIdx.x % Hkv;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (!valid || g >= G)
+        return;
+    const int s = __ldcg(&dp->s), h = __ldcg(&dp->h), part = __ldcg(&dp->part);
+    const int u0 = __ldcg(&dp->u0), nu = __ldcg(&dp->nu), R = __ldcg(&dp->R), np = __ldcg(&dp->np);
+    const int c0 = blockIdx.x, c1 = (u0 + nu - 1) / R;
+    const int npieces = c1 - c0 + 1;
 
-    int npieces, c0 = 0, F = 0, R = 1;
-    if (p.mode == kModeBalanced) {
-        const int32_t *pre = p.ws_prefix;
-        const int nt = pre[s + 1] - pre[s];
-        if (nt == 0)
-            return;
-        const int total = Hkv * pre[p.num_seqs];
-        R = max((total + p.grid - 1) / p.grid, p.min_tiles);
-        F = Hkv * pre[s] + h * nt;
-        c0 = F / R;
-        const int c1 = (F + nt - 1) / R;
-        if (c0 == c1)
-            return;
-        npieces = c1 - c0 + 1;
-    } else {
-        int L = __ldg(p.seq_lens + s);
-        L = max(0, min(L, p.max_blocks * kBlockSize));
-        const int nt = (L + kBlockSize - 1) / kBlockSize;
-        npieces = (nt + p.part_tiles - 1) / p.part_tiles;
-        if (npieces <= 1)
-            return;
-    }
-    // partial row of piece pi, head g (same numbering the decode wrote)
-    auto row = [&](int pi, int g) -> size_t {
-        if (p.mode == kModeBalanced) {
-            const int c = c0 + pi;
-            const int slot = (c == c0 && F != c0 * R) ? 2 * c + 1 : 2 * c;
-            return (size_t)slot * G + g;
-        }
-        return ((size_t)s * Hq + h * G + g) * p.p_max + pi;
-    };
-
-    for (int g = warp; g < G; g += 4) {
-        float Mx = -INFINITY;
-        for (int pi = lane; pi < npieces; pi += 32)
-            Mx = fmaxf(Mx, p.ws_m[row(pi, g)]);
+    float Mx = -INFINITY, Ws = 0.f, acc[V];
 #pragma unroll
-        for (int off = 16; off; off >>= 1)
-            Mx = fmaxf(Mx, __shfl_xor_sync(0xffffffffu, Mx, off));
-        float Wt = 0.f;
-        for (int pi = lane; pi < npieces; pi += 32) {
-            const size_t rw = row(pi, g);
-            Wt += p.ws_l[rw] * exp2f((p.ws_m[rw] - Mx) * kLog2e);
-        }
-#pragma unroll
-        for (int off = 16; off; off >>= 1)
-            Wt += __shfl_xor_sync(0xffffffffu, Wt, off);
-        if (lane == 0) {
-            sM[g] = Mx;
-            sW[g] = Wt;
-        }
-    }
-    __syncthreads();
-
-    constexpr int PER = (8 * D + 127) / 128;
-    float O[PER];
-#pragma unroll
-    for (int k = 0; k < PER; ++k)
-        O[k] = 0.f;
+    for (int v = 0; v < V; ++v)
+        acc[v] = 0.f;
     for (int base = 0; base < npieces; base += CH) {
-        const int cnt = min(CH, npieces - base);
-        for (int e = tid; e < cnt * G; e += 128) {
-            const int pi = e / G, g = e % G;
-            const size_t rw = row(base + pi, g);
-            wts[pi][g] = p.ws_l[rw] * exp2f((p.ws_m[rw] - sM[g]) * kLog2e);
-        }
-        __syncthreads();
+        float mv[CH], lv[CH], ov[CH][V];
 #pragma unroll
-        for (int k = 0; k < PER; ++k) {
-            const int e = tid + k * 128;
-            if (e < G * D) {
-                const int g = e / D, d = e % D;
-                float acc = O[k];
-                for (int pi = 0; pi < cnt; ++pi)
-                    acc += wts[pi][g] * p.ws_o[row(base + pi, g) * D + d];
-                O[k] = acc;
+        for (int i = 0; i < CH; ++i) {
+            if (base + i < npieces) {
+                const int c = c0 + base + i;
+                const int slot = (c == c0 && u0 != c0 * R) ? 2 * c + 1 : 2 * c;
+                const size_t row = slot_row(G, slot, g);
+                mv[i] = __ldcg(p.ws_sm + row);
+                lv[i] = __ldcg(p.ws_sl + row);
+                const float *src = p.ws_so + row * D + lane * V;
+                if constexpr (V == 4) {
+                    const float4 x = __ldcg(reinterpret_cast<const float4 *>(src));
+                    ov[i][0] = x.x, ov[i][1] = x.y, ov[i][2] = x.z, ov[i][3] = x.w;
+                } else {
+                    const float2 x = __ldcg(reinterpret_cast<const float2 *>(src));
+                    ov[i][0] = x.x, ov[i][1] = x.y;
+                }
             }
         }
-        __syncthreads();
-    }
-    T *out = reinterpret_cast<T *>(p.out);
 #pragma unroll
-    for (int k = 0; k < PER; ++k) {
-        const int e = tid + k * 128;
-        if (e < G * D) {
-            const int g = e / D, d = e % D;
-            out[((size_t)s * Hq + h * G + g) * D + d] = E::from_f(O[k] / sW[g]);
+        for (int i = 0; i < CH; ++i) {
+            if (base + i < npieces) {
+                const float nM = fmaxf(Mx, mv[i]);
+                const float a = Mx == -INFINITY ? 0.f : exp2f((Mx - nM) * kLog2e);
+                const float b = lv[i] * exp2f((mv[i] - nM) * kLog2e);
+                Ws = Ws * a + b;
+#pragma unroll
+                for (int v = 0; v < V; ++v)
+                    acc[v] = acc[v] * a + b * ov[i][v];
+                Mx = nM;
+            }
         }
     }
+    const float inv = 1.f / Ws;
+    if (p.mode == kModeFixed && np >= 2) {
+        const size_t row = part_row(p, G, s, h, part, g);
+        float *dst = p.ws_o + row * D + lane * V;
+#pragma unroll
+        for (int v = 0; v < V; ++v)
+            dst[v] = acc[v] * inv;
+        if (lane == 0) {
+            p.ws_m[row] = Mx;
+            p.ws_l[row] = Ws;
+        }
+    } else {
+        using M = Mma<T>;
+        T *dst = reinterpret_cast<T *>(p.out) + ((size_t)s * Hq + h * G + g) * D + lane * V;
+        uint32_t *d32 = reinterpret_cast<uint32_t *>(dst);
+#pragma unroll
+        for (int v = 0; v < V; v += 2)
+            d32[v / 2] = M::pack(acc[v] * inv, acc[v + 1] * inv);
+    }
+}
+
+// Fixed mode: merge the partitions of every run with two or more of them.
+// One thread block per (sequence, kv head, query head of the group), one
+// thread per channel; partition weights are staged in shared memory and the
+// channel sums keep eight partition rows in flight per thread.
+template <typename T, int D>
+__global__ void __launch_bounds__(D) merge_part_kernel(const DecodeParams p)
+{
+    using E = Elem<T>;
+    constexpr int NW = D / 32;
+    __shared__ float wts[D];
+    __shared__ float red[NW];
+    __shared__ float sM, sW;
+    grid_dependency_wait();
+    const int Hkv = p.num_kv_heads, Hq = p.num_heads, G = Hq / Hkv;
+    const int g = blockIdx.x % G, run = blockIdx.x / G;
+    const int s = run / Hkv, h = run % Hkv;
+    const int d = threadIdx.x, lane = d & 31, warp = d >> 5;
+    int L = __ldg(p.seq_lens + s);
+    L = max(0, min(L, p.max_blocks * kBlockSize));
+    const int nt = (L + kBlockSize - 1) / kBlockSize;
+    const int np = (nt + p.part_tiles - 1) / p.part_tiles;
+    if (np <= 1)
+        return;
+    const size_t row0 = part_row(p, G, s, h, 0, g);   // partitions of (s, h, g) are consecutive rows
+
+    float Mx = -INFINITY;
+    for (int pi = d; pi < np; pi += D)
+        Mx = fmaxf(Mx, __ldcg(p.ws_m + row0 + pi));
+#pragma unroll
+    for (int off = 16; off; off >>= 1)
+        Mx = fmaxf(Mx, __shfl_xor_sync(0xffffffffu, Mx, off));
+    if (lane == 0)
+        red[warp] = Mx;
+    __syncthreads();
+    if (d == 0) {
+        float v = red[0];
+        for (int w = 1; w < NW; ++w)
+            v = fmaxf(v, red[w]);
+        sM = v;
+    }
+    __syncthreads();
+    Mx = sM;
+    float Wt = 0.f;
+    for (int pi = d; pi < np; pi += D)
+        Wt += __ldcg(p.ws_l + row0 + pi) * exp2f((__ldcg(p.ws_m + row0 + pi) - Mx) * kLog2e);
+#pragma unroll
+    for (int off = 16; off; off >>= 1)
+        Wt += __shfl_xor_sync(0xffffffffu, Wt, off);
+    __syncthreads();
+    if (lane == 0)
+        red[warp] = Wt;
+    __syncthreads();
+    if (d == 0) {
+        float v = 0.f;
+        for (int w = 0; w < NW; ++w)
+            v += red[w];
+        sW = v;
+    }
+    float acc = 0.f;
+    for (int base = 0; base < np; base += D) {
+        const int cnt = min(D, np - base);
+        __syncthreads();
+        if (d < cnt)
+            wts[d] = __ldcg(p.ws_l + row0 + base + d) *
+                     exp2f((__ldcg(p.ws_m + row0 + base + d) - Mx) * kLog2e);
+        __syncthreads();
+        const float *col = p.ws_o + (row0 + base) * D + d;
+        int pi = 0;
+        for (; pi + 8 <= cnt; pi += 8) {
+            float v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                v[u] = __ldcg(col + (size_t)(pi + u) * D);
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                acc += wts[pi + u] * v[u];
+        }
+        for (; pi < cnt; ++pi)
+            acc += wts[pi] * __ldcg(col + (size_t)pi * D);
+    }
+    __syncthreads();
+    T *out = reinterpret_cast<T *>(p.out);
+    out[((size_t)s * Hq + h * G + g) * D + d] = E::from_f(acc / sW);
 }
 
 template <typename T, int D>
 inline void fill_kernel_set(KernelSet *ks)
 {
-    constexpr int W = 4;
+    // wide: one thread block per SM of WW independent warps; compact: 4 warps
     constexpr int S = 2;
-    ks->decode = reinterpret_cast<const void *>(&decode_mma_kernel<T, D, W, S>);
-    ks->merge = reinterpret_cast<const void *>(&merge_kernel<T, D>);
-    ks->warps = W;
-    ks->stages = S;
-    ks->smem_fixed = MmaLayout<D, W, S>::fixed;
+    constexpr int WW = D == 128 ? 10 : 12;
+    ks->decode[0] = reinterpret_cast<const void *>(&decode_mma_kernel<T, D, WW, S>);
+    ks->warps[0] = WW;
+    ks->smem_fixed[0] = MmaLayout<D, WW, S>::fixed;
+    ks->decode[1] = reinterpret_cast<const void *>(&decode_mma_kernel<T, D, 4, S>);
+    ks->warps[1] = 4;
+    ks->smem_fixed[1] = MmaLayout<D, 4, S>::fixed;
+    ks->merge_cut = reinterpret_cast<const void *>(&merge_cut_kernel<T, D>);
+    ks->merge_part = reinterpret_cast<const void *>(&merge_part_kernel<T, D>);
 }
 
 template <typename T>

@@ -59,8 +59,8 @@ extern "C" int pa_decode_noalloc(void *out, const void *q, const void *k_cache,
 {
     if (num_seqs == 0)
         return PA_OK;
-    // The balanced split's scratch never needs clearing: the kernels write
-    // every partial row and prefix entry before reading it.
+    // The balanced split's scratch never needs clearing: every call writes
+    // each worker's cut descriptor and every partial row before reading it.
     const size_t need = pa_decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim,
                                                  max_blocks_per_seq, 0);
     if (need > pa::kNoAllocScratchBytes)

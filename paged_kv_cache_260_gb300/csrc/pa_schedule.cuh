@@ -1,18 +1,20 @@
-// pa_schedule.cuh -- how a decode's work is cut and handed to thread blocks.
+// pa_schedule.cuh -- how a decode's work is cut and handed to warps.
 //
 // The work is a flat list of (sequence, kv head, 16-token tile) units ordered
-// by sequence, then kv head, then tile.  A persistent grid walks it:
-//  * balanced mode: thread block b owns the tile range [b*R, (b+1)*R), R the
-//    tiles divided evenly over the grid, so every block reads the same bytes
-//    whatever the length mix; a (sequence, kv head) run cut by a range
-//    boundary leaves partial results that the log-sum-exp merge combines
-//    (split-K along the sequence, FlashDecoding in the ICML tutorial notes,
-//    section "内核优化");
-//  * fixed mode: the units are partitions of part_tiles tiles of one run,
-//    handed out in balanced contiguous ranges of partitions;
-//  * whole mode: the units are whole runs (no split).
-// Every thread of a block evaluates the walker identically, so the pieces it
-// yields are block-uniform.
+// by sequence, then kv head, then tile; the tiles of one (sequence, kv head)
+// form a "run".  Every warp of the persistent grid is an independent worker
+// that walks its own part of the list, so warps never wait for each other:
+//  * balanced mode: worker k owns the tile range [k*R, (k+1)*R), R the tiles
+//    divided evenly over all workers, so every worker reads the same bytes
+//    whatever the length mix.  A run cut by a range boundary leaves partial
+//    results that a log-sum-exp merge combines (split-K along the sequence,
+//    FlashDecoding in the ICML tutorial notes, section "内核优化").
+//  * fixed mode: the same ranges, with runs also cut at partition boundaries
+//    (part_tiles tiles); each partition's partial result is the split-K unit,
+//    merged per run afterwards.
+//  * whole mode: worker k owns whole runs (no split), an even share by count.
+// A "piece" is the part of one run (and, in fixed mode, of one partition) that
+// lies in one worker's range: tiles [tb, te) of run (s, h).
 #pragma once
 
 #include "pa_device.cuh"
@@ -20,31 +22,32 @@
 
 namespace pa {
 
-// ---------------------------------------------------------------------------
-// Work walker: enumerates the runs ("pieces") one thread block processes.  A
-// piece is a range [tb, te) of tiles of the (sequence s, kv head h) run.
-// Every thread of the block evaluates it identically.
-// ---------------------------------------------------------------------------
 struct Walker {
     // constants
-    const int32_t *pre;   // unit prefix [n + 1] (tiles, partitions or 0/1 per sequence)
+    const int32_t *pre;   // prefix over sequences of tiles (whole mode: of non-empty runs' sequences)
     const int32_t *lens;  // clamped lengths [n]
     int n, hkv, mode, pt;
+    int R;                // tiles per worker (balanced / fixed)
     // state
     int s, h, tb, te, nt;
-    int cur;      // balanced: first flat tile of (s, h); fixed/whole: flat item index
-    int end;      // balanced: end of the block's tile range; fixed/whole: end item
-    int part;     // fixed: partition index within (s, h)
-    int np;       // fixed/whole: partitions of sequence s
+    int F;                // flat index of tile 0 of run (s, h)
+    int A, B;             // this worker's flat tile range, or run-index range (whole mode)
+    int cur;              // whole mode: current run index
+    int part;             // fixed mode: partition of the current piece
     bool valid;
-    bool first;   // first piece of this thread block
+    bool first;           // first piece of this worker
 
+    __device__ __forceinline__ int tiles_of(int seq) const
+    {
+        return (lens[seq] + kBlockSize - 1) / kBlockSize;
+    }
+
+    // largest s with hkv * pre[s] <= x (sequences without units are skipped)
     __device__ __forceinline__ int find_seq(int x) const
     {
-        // largest s with hkv * pre[s] <= x (sequences without units are skipped)
         int lo = 0, hi = n - 1;
         while (lo < hi) {
-            int mid = (lo + hi + 1) >> 1;
+            const int mid = (lo + hi + 1) >> 1;
             if (hkv * pre[mid] <= x)
                 lo = mid;
             else
@@ -53,22 +56,19 @@ struct Walker {
         return lo;
     }
 
-    __device__ __forceinline__ int tiles_of(int seq) const { return (lens[seq] + kBlockSize - 1) / kBlockSize; }
-
-    __device__ __forceinline__ void set_fixed_piece()
+    // piece end inside run (s, h) starting at tile tb
+    __device__ __forceinline__ void close_piece()
     {
-        nt = tiles_of(s);
+        te = min(nt, B - F);
         if (mode == kModeFixed) {
-            tb = part * pt;
-            te = min(nt, tb + pt);
-        } else {
-            tb = 0;
-            te = nt;
+            part = tb / pt;
+            te = min(te, (part + 1) * pt);
         }
     }
 
-    __device__ __forceinline__ void init(const int32_t *pre_, const int32_t *lens_, int n_, int hkv_,
-                                         int mode_, int pt_, int min_tiles, int grid, int bid)
+    __device__ __forceinline__ void init(const int32_t *pre_, const int32_t *lens_, int n_,
+                                         int hkv_, int mode_, int pt_, int min_tiles, int workers,
+                                         int k)
     {
         pre = pre_;
         lens = lens_;
@@ -77,37 +77,36 @@ struct Walker {
         mode = mode_;
         pt = pt_;
         first = true;
-        const int total = hkv * pre[n];
-        if (mode == kModeBalanced) {
-            int R = (total + grid - 1) / grid;
-            R = max(R, min_tiles);
-            const long long a = (long long)bid * R;
-            valid = a < total;
+        part = 0;
+        const int total = hkv * pre[n];          // tiles, or non-empty runs in whole mode
+        if (mode == kModeWhole) {
+            A = (int)((long long)k * total / workers);
+            B = (int)((long long)(k + 1) * total / workers);
+            valid = A < B;
             if (!valid)
                 return;
-            const int A = (int)a;
-            end = min(total, A + R);
+            cur = A;
             s = find_seq(A);
-            nt = pre[s + 1] - pre[s];
-            const int rel = A - hkv * pre[s];
-            h = rel / nt;
-            cur = hkv * pre[s] + h * nt;
-            tb = A - cur;
-            te = min(nt, end - cur);
-        } else {
-            const int i0 = (int)((long long)bid * total / grid);
-            end = (int)((long long)(bid + 1) * total / grid);
-            valid = i0 < end;
-            if (!valid)
-                return;
-            cur = i0;
-            s = find_seq(i0);
-            np = pre[s + 1] - pre[s];
-            const int rel = i0 - hkv * pre[s];
-            h = rel / np;
-            part = rel % np;
-            set_fixed_piece();
+            h = A - hkv * pre[s];
+            nt = tiles_of(s);
+            F = 0;
+            tb = 0;
+            te = nt;
+            return;
         }
+        R = max((total + workers - 1) / workers, min_tiles);
+        const long long a = (long long)k * R;
+        valid = a < total;
+        if (!valid)
+            return;
+        A = (int)a;
+        B = min(total, A + R);
+        s = find_seq(A);
+        nt = pre[s + 1] - pre[s];
+        h = (A - hkv * pre[s]) / nt;
+        F = hkv * pre[s] + h * nt;
+        tb = A - F;
+        close_piece();
     }
 
     __device__ __forceinline__ void next_seq()
@@ -120,62 +119,64 @@ struct Walker {
     __device__ __forceinline__ void next()
     {
         first = false;
-        if (mode == kModeBalanced) {
-            cur += nt;
-            if (cur >= end) {
+        if (mode == kModeWhole) {
+            if (++cur >= B) {
                 valid = false;
                 return;
             }
             if (++h == hkv) {
                 h = 0;
                 next_seq();
+                nt = tiles_of(s);
+            }
+            tb = 0;
+            te = nt;
+            return;
+        }
+        if (F + te >= B) {
+            valid = false;
+            return;
+        }
+        if (te < nt) {           // fixed mode: next partition of the same run
+            tb = te;
+        } else {                 // next run
+            F += nt;
+            if (++h == hkv) {
+                h = 0;
+                next_seq();
                 nt = pre[s + 1] - pre[s];
             }
             tb = 0;
-            te = min(nt, end - cur);
-        } else {
-            if (++cur >= end) {
-                valid = false;
-                return;
-            }
-            if (++part == np) {
-                part = 0;
-                if (++h == hkv) {
-                    h = 0;
-                    next_seq();
-                    np = pre[s + 1] - pre[s];
-                }
-            }
-            set_fixed_piece();
         }
+        close_piece();
     }
 
-    __device__ __forceinline__ bool whole() const
+    // the piece is the whole run
+    __device__ __forceinline__ bool whole_run() const { return tb == 0 && te == nt; }
+
+    // fixed mode: the piece is a whole partition
+    __device__ __forceinline__ bool whole_part() const
     {
-        return mode == kModeBalanced ? (tb == 0 && te == nt) : (mode == kModeWhole || np == 1);
+        return mode == kModeFixed && tb == part * pt && te == min(nt, (part + 1) * pt);
     }
 };
 
-// Units a sequence of (clamped) length L contributes to the flat work list.
-__device__ __forceinline__ int seq_units(int L, int mode, int pt)
+// Units a sequence of (clamped) length L contributes to the flat list.
+__device__ __forceinline__ int seq_units(int L, int mode)
 {
     const int nt = (L + kBlockSize - 1) / kBlockSize;
-    if (mode == kModeBalanced)
-        return nt;
-    if (mode == kModeFixed)
-        return (nt + pt - 1) / pt;
-    return nt > 0 ? 1 : 0;
+    return mode == kModeWhole ? (nt > 0 ? 1 : 0) : nt;
 }
 
 // Clamp the lengths into shared memory and build the exclusive unit prefix.
-template <int W>
+template <int NT>
 __device__ __forceinline__ void build_prefix(const DecodeParams &p, int32_t *pre, int32_t *lens)
 {
-    __shared__ int warp_sum[W];
+    constexpr int NW = NT / 32;
+    __shared__ int warp_sum[NW];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int n = p.num_seqs;
-    const int nthr = W * 32;
-    const int per = (n + nthr - 1) / nthr;
+    const int per = (n + NT - 1) / NT;
     const int lo = min(n, tid * per), hi = min(n, lo + per);
     const int maxlen = p.max_blocks * kBlockSize;
     int sum = 0;
@@ -187,7 +188,7 @@ __device__ __forceinline__ void build_prefix(const DecodeParams &p, int32_t *pre
             L = L < 0 ? 0 : maxlen;
         }
         lens[s] = L;
-        sum += seq_units(L, p.mode, p.part_tiles);
+        sum += seq_units(L, p.mode);
     }
     if (bad && blockIdx.x == 0)
         record_error(p.err, PA_DEVERR_SEQLEN_RANGE);
@@ -207,10 +208,17 @@ __device__ __forceinline__ void build_prefix(const DecodeParams &p, int32_t *pre
     int run = before + incl - sum;
     for (int s = lo; s < hi; ++s) {
         pre[s] = run;
-        run += seq_units(lens[s], p.mode, p.part_tiles);
+        run += seq_units(lens[s], p.mode);
     }
-    if (tid == nthr - 1)
+    if (tid == NT - 1)
         pre[n] = before + incl;
 }
+
+// A cut unit (a run in balanced mode, a partition in fixed mode) as recorded
+// by the worker in whose range it starts, for the merge.
+struct CutDesc {
+    int s, h, part, u0;   // sequence, kv head, partition, flat index of the unit's first tile
+    int nu, R, np, valid; // tiles of the unit, tiles per worker, partitions of the run, flag
+};
 
 }  // namespace pa

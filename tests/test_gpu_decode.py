@@ -157,16 +157,23 @@ def test_fixed_partials_match_oracle(pa):
             continue                      # a single partition is written as the output itself
         np.testing.assert_allclose(gm[s, :, :n], m[s, :, :n], rtol=1e-5, atol=1e-5)
         np.testing.assert_allclose(gl[s, :, :n], l[s, :, :n], rtol=1e-4, atol=1e-5)
-        np.testing.assert_allclose(go[s, :, :n], o[s, :, :n], rtol=0, atol=2e-4)
+        # the weights enter the second product rounded to fp16 (relative error
+        # <= 2^-11), so a normalised partial output moves by <= 2^-11 max|v|
+        _, vv = oracle.gather_kv(w.k_cache, w.v_cache, w.block_tables, s, int(L))
+        vmax = float(np.abs(oracle.decode_bits(vv, "f16")).max())
+        np.testing.assert_allclose(go[s, :, :n], o[s, :, :n], rtol=0, atol=2.0 ** -11 * vmax + 1e-5)
 
 
 def test_single_partition_equals_no_split(pa):
+    # with partitions longer than every sequence the split only cuts runs to
+    # balance the warps; the merge is exact in real arithmetic, so the result
+    # agrees with the unsplit decode up to rounding
     w = synth.build("one_part", 6, 32, 8, 128, "bf16", [5, 16, 100, 511, 512, 300], seed=13)
     dw = DevWorkload(w)
     pa.decode(dw.out, dw.q, dw.k, dw.v, dw.tables, dw.lens, w.scale, partition_size=-1)
     a = dw.out.clone()
     pa.decode(dw.out, dw.q, dw.k, dw.v, dw.tables, dw.lens, w.scale, partition_size=512)
-    assert torch.equal(a, dw.out)
+    assert float((a.float() - dw.out.float()).abs().max()) <= TOL["bf16"]
 
 
 def test_repeatable(pa):
