@@ -483,22 +483,23 @@ __global__ void __launch_bounds__(256) merge_cut_kernel(const DecodeParams p)
 }
 
 // Fixed mode: merge the partitions of every run with two or more of them.
-// One thread block per (sequence, kv head, query head of the group), one
-// thread per channel; partition weights are staged in shared memory and the
-// channel sums keep eight partition rows in flight per thread.
+// One thread block of eight warps per (sequence, kv head, query head of the
+// group): warp w folds partitions w, w+8, ... with each lane holding D/32
+// channels and four partition rows in flight; the eight partial sums are
+// added in shared memory.
 template <typename T, int D>
-__global__ void __launch_bounds__(D) merge_part_kernel(const DecodeParams p)
+__global__ void __launch_bounds__(256) merge_part_kernel(const DecodeParams p)
 {
     using E = Elem<T>;
-    constexpr int NW = D / 32;
-    __shared__ float wts[D];
-    __shared__ float red[NW];
-    __shared__ float sM, sW;
+    constexpr int V = D / 32;
+    constexpr int U = 4;
+    __shared__ float red_m[8], red_w[8];
+    __shared__ float part_acc[8][D];
     grid_dependency_wait();
     const int Hkv = p.num_kv_heads, Hq = p.num_heads, G = Hq / Hkv;
     const int g = blockIdx.x % G, run = blockIdx.x / G;
     const int s = run / Hkv, h = run % Hkv;
-    const int d = threadIdx.x, lane = d & 31, warp = d >> 5;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     int L = __ldg(p.seq_lens + s);
     L = max(0, min(L, p.max_blocks * kBlockSize));
     const int nt = (L + kBlockSize - 1) / kBlockSize;
@@ -507,64 +508,72 @@ __global__ void __launch_bounds__(D) merge_part_kernel(const DecodeParams p)
         return;
     const size_t row0 = part_row(p, G, s, h, 0, g);   // partitions of (s, h, g) are consecutive rows
 
+    // M = max_p m_p, W = sum_p l_p exp(m_p - M)
     float Mx = -INFINITY;
-    for (int pi = d; pi < np; pi += D)
+    for (int pi = tid; pi < np; pi += 256)
         Mx = fmaxf(Mx, __ldcg(p.ws_m + row0 + pi));
 #pragma unroll
     for (int off = 16; off; off >>= 1)
         Mx = fmaxf(Mx, __shfl_xor_sync(0xffffffffu, Mx, off));
     if (lane == 0)
-        red[warp] = Mx;
+        red_m[warp] = Mx;
     __syncthreads();
-    if (d == 0) {
-        float v = red[0];
-        for (int w = 1; w < NW; ++w)
-            v = fmaxf(v, red[w]);
-        sM = v;
-    }
-    __syncthreads();
-    Mx = sM;
-    float Wt = 0.f;
-    for (int pi = d; pi < np; pi += D)
-        Wt += __ldcg(p.ws_l + row0 + pi) * exp2f((__ldcg(p.ws_m + row0 + pi) - Mx) * kLog2e);
+    Mx = red_m[0];
 #pragma unroll
-    for (int off = 16; off; off >>= 1)
-        Wt += __shfl_xor_sync(0xffffffffu, Wt, off);
-    __syncthreads();
-    if (lane == 0)
-        red[warp] = Wt;
-    __syncthreads();
-    if (d == 0) {
-        float v = 0.f;
-        for (int w = 0; w < NW; ++w)
-            v += red[w];
-        sW = v;
-    }
-    float acc = 0.f;
-    for (int base = 0; base < np; base += D) {
-        const int cnt = min(D, np - base);
-        __syncthreads();
-        if (d < cnt)
-            wts[d] = __ldcg(p.ws_l + row0 + base + d) *
-                     exp2f((__ldcg(p.ws_m + row0 + base + d) - Mx) * kLog2e);
-        __syncthreads();
-        const float *col = p.ws_o + (row0 + base) * D + d;
-        int pi = 0;
-        for (; pi + 8 <= cnt; pi += 8) {
-            float v[8];
+    for (int w = 1; w < 8; ++w)
+        Mx = fmaxf(Mx, red_m[w]);
+
+    float acc[V], Wt = 0.f;
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
-                v[u] = __ldcg(col + (size_t)(pi + u) * D);
+    for (int v = 0; v < V; ++v)
+        acc[v] = 0.f;
+    for (int base = warp; base < np; base += 8 * U) {
+        float wv[U], ov[U][V];
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
-                acc += wts[pi + u] * v[u];
+        for (int u = 0; u < U; ++u) {
+            const int pi = base + 8 * u;
+            if (pi < np) {
+                const size_t row = row0 + pi;
+                wv[u] = __ldcg(p.ws_l + row) * exp2f((__ldcg(p.ws_m + row) - Mx) * kLog2e);
+                const float *src = p.ws_o + row * D + lane * V;
+                if constexpr (V == 4) {
+                    const float4 x = __ldcg(reinterpret_cast<const float4 *>(src));
+                    ov[u][0] = x.x, ov[u][1] = x.y, ov[u][2] = x.z, ov[u][3] = x.w;
+                } else {
+                    const float2 x = __ldcg(reinterpret_cast<const float2 *>(src));
+                    ov[u][0] = x.x, ov[u][1] = x.y;
+                }
+            } else {
+                wv[u] = 0.f;
+#pragma unroll
+                for (int v = 0; v < V; ++v)
+                    ov[u][v] = 0.f;
+            }
         }
-        for (; pi < cnt; ++pi)
-            acc += wts[pi] * __ldcg(col + (size_t)pi * D);
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            Wt += wv[u];
+#pragma unroll
+            for (int v = 0; v < V; ++v)
+                acc[v] += wv[u] * ov[u][v];
+        }
     }
+#pragma unroll
+    for (int v = 0; v < V; ++v)
+        part_acc[warp][lane * V + v] = acc[v];
+    if (lane == 0)
+        red_w[warp] = Wt;
     __syncthreads();
-    T *out = reinterpret_cast<T *>(p.out);
-    out[((size_t)s * Hq + h * G + g) * D + d] = E::from_f(acc / sW);
+    if (tid < D) {
+        float o = 0.f, W = 0.f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+            o += part_acc[w][tid];
+            W += red_w[w];
+        }
+        T *out = reinterpret_cast<T *>(p.out);
+        out[((size_t)s * Hq + h * G + g) * D + tid] = E::from_f(o / W);
+    }
 }
 
 template <typename T, int D>
