@@ -414,10 +414,12 @@ int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache
     if (rc != PA_OK || mode == kModeWhole)
         return rc;
     void *margs[] = {&p};
-    rc = launch_dependent(ks.merge_cut, dim3(workers), dim3(256), 0, st, margs);
+    // one warp per query head of the group: small blocks, so all of them can
+    // be resident beside the decode while it drains
+    rc = launch_dependent(ks.merge_cut, dim3(workers), dim3(32 * group), 0, st, margs);
     if (rc != PA_OK || mode != kModeFixed || p_max < 2)
         return rc;
-    return launch_dependent(ks.merge_part, dim3(num_seqs * num_heads), dim3(256), 0, st, margs);
+    return launch_dependent(ks.merge_part, dim3(num_seqs * num_heads), dim3(512), 0, st, margs);
 }
 
 int pa_reshape_and_cache(const void *k_new, const void *v_new, void *k_cache, void *v_cache,

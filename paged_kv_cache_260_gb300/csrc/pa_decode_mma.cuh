@@ -483,18 +483,19 @@ __global__ void __launch_bounds__(256) merge_cut_kernel(const DecodeParams p)
 }
 
 // Fixed mode: merge the partitions of every run with two or more of them.
-// One thread block of eight warps per (sequence, kv head, query head of the
-// group): warp w folds partitions w, w+8, ... with each lane holding D/32
-// channels and four partition rows in flight; the eight partial sums are
-// added in shared memory.
+// One thread block of sixteen warps per (sequence, kv head, query head of the
+// group): warp w folds partitions w, w+16, ... with each lane holding D/32
+// channels and eight partition rows in flight; the partial sums are added in
+// shared memory.
 template <typename T, int D>
-__global__ void __launch_bounds__(256) merge_part_kernel(const DecodeParams p)
+__global__ void __launch_bounds__(512) merge_part_kernel(const DecodeParams p)
 {
     using E = Elem<T>;
     constexpr int V = D / 32;
-    constexpr int U = 4;
-    __shared__ float red_m[8], red_w[8];
-    __shared__ float part_acc[8][D];
+    constexpr int U = 8;
+    constexpr int NW = 16;
+    __shared__ float red_m[NW], red_w[NW];
+    __shared__ float part_acc[NW][D];
     grid_dependency_wait();
     const int Hkv = p.num_kv_heads, Hq = p.num_heads, G = Hq / Hkv;
     const int g = blockIdx.x % G, run = blockIdx.x / G;
@@ -510,7 +511,7 @@ __global__ void __launch_bounds__(256) merge_part_kernel(const DecodeParams p)
 
     // M = max_p m_p, W = sum_p l_p exp(m_p - M)
     float Mx = -INFINITY;
-    for (int pi = tid; pi < np; pi += 256)
+    for (int pi = tid; pi < np; pi += NW * 32)
         Mx = fmaxf(Mx, __ldcg(p.ws_m + row0 + pi));
 #pragma unroll
     for (int off = 16; off; off >>= 1)
@@ -520,18 +521,18 @@ __global__ void __launch_bounds__(256) merge_part_kernel(const DecodeParams p)
     __syncthreads();
     Mx = red_m[0];
 #pragma unroll
-    for (int w = 1; w < 8; ++w)
+    for (int w = 1; w < NW; ++w)
         Mx = fmaxf(Mx, red_m[w]);
 
     float acc[V], Wt = 0.f;
 #pragma unroll
     for (int v = 0; v < V; ++v)
         acc[v] = 0.f;
-    for (int base = warp; base < np; base += 8 * U) {
+    for (int base = warp; base < np; base += NW * U) {
         float wv[U], ov[U][V];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const int pi = base + 8 * u;
+            const int pi = base + NW * u;
             if (pi < np) {
                 const size_t row = row0 + pi;
                 wv[u] = __ldcg(p.ws_l + row) * exp2f((__ldcg(p.ws_m + row) - Mx) * kLog2e);
@@ -567,7 +568,7 @@ __global__ void __launch_bounds__(256) merge_part_kernel(const DecodeParams p)
     if (tid < D) {
         float o = 0.f, W = 0.f;
 #pragma unroll
-        for (int w = 0; w < 8; ++w) {
+        for (int w = 0; w < NW; ++w) {
             o += part_acc[w][tid];
             W += red_w[w];
         }
