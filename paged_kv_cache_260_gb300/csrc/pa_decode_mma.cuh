@@ -116,7 +116,10 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
     }
     // the merge kernels that follow may be scheduled now; they wait for us
     grid_dependents_launch();
-    // no global memory is touched before the preceding kernel has completed
+    for (int i = tid * 32; i < n; i += W * 32 * 32)
+        prefetch_l2(p.seq_lens + i);
+    // no global memory is read or written before the preceding kernel has
+    // completed (the prefetch above only warms L2)
     grid_dependency_wait();
     build_prefix<W * 32>(p, pre, lens);
     __syncthreads();

@@ -225,4 +225,12 @@ __device__ __forceinline__ void grid_dependents_launch()
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Pull a line into L2 ahead of use.  Safe before grid_dependency_wait(): L2
+// is the point of coherence, so a later write by the preceding grid is still
+// seen by every load that follows the wait.
+__device__ __forceinline__ void prefetch_l2(const void *ptr)
+{
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
+}
+
 }  // namespace pa
