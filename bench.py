@@ -253,9 +253,8 @@ class Step:
         self.ev = None
 
     def _count_launches(self):
-        n = 1                                           # decode
+        n = 1                                           # decode (append fused in)
         n += int(self.pairs is not None)                # copy_blocks
-        n += int(self.slots is not None)                # reshape_and_cache
         if self.ps >= 0:
             n += 1                                      # merge of cut runs / partitions
         if self.ps > 0 and self.tables.shape[1] * 16 > self.ps:
@@ -267,12 +266,16 @@ class Step:
         pa = self.pa
         if self.pairs is not None:
             pa.copy_blocks(self.k, self.v, self.pairs)
-        if self.slots is not None:
-            pa.reshape_and_cache(self.k_new, self.v_new, self.k, self.v, self.slots)
         if ev_pair is not None:
             ev_pair[0].record()
-        pa.decode(self.out, self.q, self.k, self.v, self.tables, self.lens, self.w.scale,
-                  partition_size=self.ps, workspace=self.ws)
+        if self.slots is not None:
+            # reshape_and_cache of the newest token fused into the decode launch
+            pa.decode_append(self.out, self.q, self.k, self.v, self.tables, self.lens, self.k_new,
+                             self.v_new, self.slots, self.w.scale, partition_size=self.ps,
+                             workspace=self.ws)
+        else:
+            pa.decode(self.out, self.q, self.k, self.v, self.tables, self.lens, self.w.scale,
+                      partition_size=self.ps, workspace=self.ws)
         if ev_pair is not None:
             ev_pair[1].record()
 
@@ -502,8 +505,9 @@ def run_ours(args):
             "head_dim": w.head_dim, "block_size": 16, "partition_size": ps,
             "kv_bytes_per_step": kv_bytes,
             "unique_kv_bytes_per_step": unique_bytes,
-            "step": "copy_blocks + reshape_and_cache + decode (+ merge)"[
-                0 if w.block_mapping is not None else 14:],
+            "step": ("copy_blocks + " if w.block_mapping is not None else "")
+                    + ("decode with reshape_and_cache fused (pa_decode_append)"
+                       if w.slot_mapping is not None else "decode") + " + merge",
             "l2": ("inputs larger than L2 (KV read per step %.0f MB vs 129 MB L2)" % (unique_bytes / 1e6)
                    if l2_ok else "L2 flushed (258 MB write) before every step; steps timed alone"),
             "timing": ("CUDA graph of %d steps replayed %d times, CUDA events" % (spg, args.steps // spg)
@@ -512,7 +516,7 @@ def run_ours(args):
         },
         "e2e": {"value": total_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "roofline": {"bound": "hbm", "kernel": "pa_decode: decode_mma_kernel + merge kernel(s)",
+        "roofline": {"bound": "hbm", "kernel": "decode_mma_kernel + merge kernel(s) (one pa_decode / pa_decode_append call)",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs, copy burst)"
                      if peak_src == "measured" else "fallback 6.8 TB/s",

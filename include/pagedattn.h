@@ -61,6 +61,7 @@ enum pa_dtype { PA_DTYPE_F16 = 0, PA_DTYPE_BF16 = 1 };
 #define PA_DEVERR_TABLE_RANGE  0x4u  /* decode/gather: table entry outside [0, num_blocks) */
 #define PA_DEVERR_SEQLEN_RANGE 0x8u  /* seq_len < 0 or > max_blocks_per_seq*block_size */
 #define PA_DEVERR_TIMEOUT      0x10u /* a bounded wait on a copy expired */
+#define PA_DEVERR_APPEND_SLOT  0x20u /* decode_append: slot is not the last position's */
 
 /* PAGEDATTN_VERSION of the loaded library. */
 int pa_version(void);
@@ -129,6 +130,32 @@ int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache
               int block_size, int max_blocks_per_seq, int num_blocks,
               float scale, int dtype, int partition_size,
               void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * One decode step with the new tokens appended on the way: the result equals
+ *     pa_reshape_and_cache(k_new, v_new, k_cache, v_cache, slot_mapping,
+ *                          num_seqs, ...)
+ * followed by pa_decode(...), in one launch (plus the merge).  Token s is the
+ * newest token of sequence s: slot_mapping[s] must be the slot of position
+ * seq_lens[s] - 1 (through block_tables), or negative when sequence s gets
+ * no token.  The warp that owns that position's tile takes the row from
+ * k_new / v_new directly and writes it to the pool, so no other read of the
+ * slot happens in the call.  A slot that is not the last position's is not
+ * written and sets PA_DEVERR_APPEND_SLOT.  The block that receives a token
+ * must not be read by another sequence in the same call (copy-on-write
+ * guarantees this: a shared block is copied before it is written).
+ *
+ *   k_new, v_new  [num_seqs][num_kv_heads][head_dim]  dtype
+ *   slot_mapping  [num_seqs] int64
+ * Other arguments as pa_decode; k_cache, v_cache are written.
+ */
+int pa_decode_append(void *out, const void *q, void *k_cache, void *v_cache,
+                     const int32_t *block_tables, const int32_t *seq_lens,
+                     const void *k_new, const void *v_new, const int64_t *slot_mapping,
+                     int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                     int block_size, int max_blocks_per_seq, int num_blocks,
+                     float scale, int dtype, int partition_size,
+                     void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * pa_decode without a workspace argument, for callers that cannot allocate

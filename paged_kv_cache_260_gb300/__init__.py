@@ -17,7 +17,7 @@ import threading
 
 __all__ = [
     "PagedAttnError", "load", "version", "decode", "decode_workspace_size", "workspace_for",
-    "decode_noalloc",
+    "decode_noalloc", "decode_append",
     "reshape_and_cache", "copy_blocks", "gather_kv", "validate_tables", "get_device_error",
     "PA_DTYPE_F16", "PA_DTYPE_BF16", "DEVERR", "STATUS",
 ]
@@ -28,7 +28,7 @@ BLOCK_SIZE = 16
 STATUS = {0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED", 3: "PA_ERR_WORKSPACE",
           4: "PA_ERR_CUDA", 5: "PA_ERR_DEVICE"}
 DEVERR = {"SLOT_RANGE": 0x1, "BLOCK_RANGE": 0x2, "TABLE_RANGE": 0x4, "SEQLEN_RANGE": 0x8,
-          "TIMEOUT": 0x10}
+          "TIMEOUT": 0x10, "APPEND_SLOT": 0x20}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libpagedattn.so")
@@ -62,6 +62,9 @@ def load(path: str = LIB_PATH):
         L.pa_decode_workspace_size.argtypes = [i, i, i, i, i, i]
         L.pa_decode.restype = i
         L.pa_decode.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, i, vp, sz, vp]
+        L.pa_decode_append.restype = i
+        L.pa_decode_append.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i,
+                                       f, i, i, vp, sz, vp]
         L.pa_decode_noalloc.restype = i
         L.pa_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, vp]
         L.pa_reshape_and_cache.restype = i
@@ -163,6 +166,29 @@ def decode(out, q, k_cache, v_cache, block_tables, seq_lens, scale, partition_si
                           float(scale), _dtype_code(q), int(partition_size), _ptr(workspace),
                           wbytes, _stream(stream))
     _check("pa_decode", rc)
+    return out
+
+
+def decode_append(out, q, k_cache, v_cache, block_tables, seq_lens, k_new, v_new, slot_mapping,
+                  scale, partition_size=0, workspace=None, stream=None):
+    """pa_decode_append: reshape_and_cache of each sequence's newest token, then decode,
+    in one launch.  slot_mapping[s] is the slot of position seq_lens[s] - 1 (or < 0)."""
+    n, hq, d = q.shape
+    nb, hkv, bs, d2 = k_cache.shape
+    _require(out.shape == q.shape and d2 == d and v_cache.shape == k_cache.shape, "shapes")
+    _require(block_tables.dim() == 2 and block_tables.shape[0] == n and seq_lens.shape == (n,),
+             "table shapes")
+    _require(k_new.shape == (n, hkv, d) and v_new.shape == k_new.shape and
+             slot_mapping.shape == (n,), "new-token shapes")
+    if workspace is None:
+        workspace = workspace_for(q, k_cache, block_tables, partition_size)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load().pa_decode_append(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                 _ptr(block_tables), _ptr(seq_lens), _ptr(k_new), _ptr(v_new),
+                                 _ptr(slot_mapping), n, hq, hkv, d, bs, block_tables.shape[1], nb,
+                                 float(scale), _dtype_code(q), int(partition_size),
+                                 _ptr(workspace), wbytes, _stream(stream))
+    _check("pa_decode_append", rc)
     return out
 
 

@@ -293,11 +293,12 @@ size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, i
         .total;
 }
 
-int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
-              const int32_t *block_tables, const int32_t *seq_lens, int num_seqs, int num_heads,
-              int num_kv_heads, int head_dim, int block_size, int max_blocks_per_seq,
-              int num_blocks, float scale, int dtype, int partition_size, void *workspace,
-              size_t workspace_bytes, void *stream)
+static int decode_impl(void *out, const void *q, const void *k_cache, const void *v_cache,
+                       const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,
+                       int num_heads, int num_kv_heads, int head_dim, int block_size,
+                       int max_blocks_per_seq, int num_blocks, float scale, int dtype,
+                       int partition_size, void *workspace, size_t workspace_bytes, void *stream,
+                       const void *k_new, const void *v_new, const int64_t *slot_mapping)
 {
     int rc = check_common(num_kv_heads, head_dim, block_size, num_blocks, dtype);
     if (rc != PA_OK)
@@ -375,6 +376,9 @@ int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache
     p.v_cache = v_cache;
     p.block_tables = block_tables;
     p.seq_lens = seq_lens;
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.slot_mapping = slot_mapping;
     char *ws = static_cast<char *>(workspace);
     if (wl.total > 0) {
         p.ws_m = reinterpret_cast<float *>(ws + wl.m_off);
@@ -420,6 +424,34 @@ int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache
     if (rc != PA_OK || mode != kModeFixed || p_max < 2)
         return rc;
     return launch_dependent(ks.merge_part, dim3(num_seqs * num_heads), dim3(512), 0, st, margs);
+}
+
+int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
+              const int32_t *block_tables, const int32_t *seq_lens, int num_seqs, int num_heads,
+              int num_kv_heads, int head_dim, int block_size, int max_blocks_per_seq,
+              int num_blocks, float scale, int dtype, int partition_size, void *workspace,
+              size_t workspace_bytes, void *stream)
+{
+    return decode_impl(out, q, k_cache, v_cache, block_tables, seq_lens, num_seqs, num_heads,
+                       num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks, scale,
+                       dtype, partition_size, workspace, workspace_bytes, stream, nullptr, nullptr,
+                       nullptr);
+}
+
+int pa_decode_append(void *out, const void *q, void *k_cache, void *v_cache,
+                     const int32_t *block_tables, const int32_t *seq_lens, const void *k_new,
+                     const void *v_new, const int64_t *slot_mapping, int num_seqs, int num_heads,
+                     int num_kv_heads, int head_dim, int block_size, int max_blocks_per_seq,
+                     int num_blocks, float scale, int dtype, int partition_size, void *workspace,
+                     size_t workspace_bytes, void *stream)
+{
+    if (num_seqs > 0 && (!k_new || !v_new || !slot_mapping || !aligned(k_new, 16) ||
+                         !aligned(v_new, 16) || !aligned(slot_mapping, 8)))
+        return PA_ERR_INVALID_ARG;
+    return decode_impl(out, q, k_cache, v_cache, block_tables, seq_lens, num_seqs, num_heads,
+                       num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks, scale,
+                       dtype, partition_size, workspace, workspace_bytes, stream, k_new, v_new,
+                       slot_mapping);
 }
 
 int pa_reshape_and_cache(const void *k_new, const void *v_new, void *k_cache, void *v_cache,

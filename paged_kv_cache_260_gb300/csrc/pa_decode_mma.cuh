@@ -222,6 +222,33 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
         const int L = lens[cons.s];
         bool need_q = true;
 
+        // Fused append: the new token sits at position L-1, in the run's last
+        // tile, which only this warp reads.  Its K/V row is taken from
+        // k_new / v_new into the stage after the tile lands (the pool slot
+        // still holds a stale row) and written to the pool for later steps.
+        constexpr int NCH = D / 8;                // 16-byte chunks per row
+        const int last_tile = (L - 1) / kBlockSize;
+        bool app = false;
+        int app_phys = 0;
+        uint4 app_row = make_uint4(0u, 0u, 0u, 0u);
+        if (p.k_new != nullptr && L > 0 && cons.te == cons.nt) {
+            const int64_t slot = __ldg(p.slot_mapping + cons.s);
+            if (slot >= 0) {
+                app_phys = __ldg(p.block_tables + (size_t)cons.s * p.max_blocks + last_tile);
+                if ((unsigned)app_phys < (unsigned)p.num_blocks &&
+                    slot == (int64_t)app_phys * kBlockSize + (L - 1) % kBlockSize) {
+                    app = true;
+                    if (lane < 2 * NCH) {
+                        const T *src = reinterpret_cast<const T *>(lane < NCH ? p.k_new : p.v_new) +
+                                       ((size_t)cons.s * Hkv + cons.h) * D + (lane % NCH) * 8;
+                        app_row = __ldg(reinterpret_cast<const uint4 *>(src));
+                    }
+                } else if (lane == 0) {
+                    record_error(p.err, PA_DEVERR_APPEND_SLOT);
+                }
+            }
+        }
+
         for (int tile = cons.tb; tile < cons.te; ++tile) {
             const int st = it % S;
             if (!aborted && !mbar_wait_bounded(bar0 + st * 8, (uint32_t)((it / S) & 1))) {
@@ -243,6 +270,21 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
                 need_q = false;
             }
             const int nvalid = min(kBlockSize, L - tile * kBlockSize);
+            if (app && tile == last_tile) {
+                const int row = (L - 1) % kBlockSize;
+                if (lane < 2 * NCH) {
+                    const int c = lane % NCH;   // chunk of 8 channels
+                    unsigned char *dst = wst + (size_t)st * Sh::STAGE + (lane < NCH ? 0 : Sh::TILE) +
+                                         (c >> 3) * Sh::BOX + swz(row, c & 7);
+                    *reinterpret_cast<uint4 *>(dst) = app_row;
+                    T *pool = reinterpret_cast<T *>(const_cast<void *>(lane < NCH ? p.k_cache : p.v_cache));
+                    const size_t prow = ((size_t)app_phys * Hkv + cons.h) * kBlockSize + row;
+                    *reinterpret_cast<uint4 *>(pool + prow * D + c * 8) = app_row;
+                    // the next copy into this stage must not overtake these writes
+                    fence_proxy_async_shared();
+                }
+                __syncwarp();
+            }
 
             // S = K . Q^T  (two accumulators to shorten the dependency chain)
             float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};

@@ -233,4 +233,11 @@ __device__ __forceinline__ void prefetch_l2(const void *ptr)
     asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
 }
 
+// Order this thread's generic-proxy writes to shared memory before later
+// async-proxy (TMA) accesses of the same bytes.
+__device__ __forceinline__ void fence_proxy_async_shared()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 }  // namespace pa

@@ -24,6 +24,9 @@ struct DecodeParams {
     const void *v_cache;
     const int32_t *block_tables;
     const int32_t *seq_lens;
+    const void *k_new;             // append: token s's K/V [num_seqs][Hkv][D], or null
+    const void *v_new;
+    const int64_t *slot_mapping;   // append: slot of position seq_lens[s] - 1, <0 = none
     float *ws_m;           // fixed mode, per partition: max of scaled scores (natural-log units)
     float *ws_l;           //   sum of exp(score - m)
     float *ws_o;           //   normalised partial output

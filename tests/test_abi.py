@@ -74,6 +74,15 @@ def test_decode_rejects_bad_scalars(lib):
                    lens=fake) == 1                     # misaligned q
 
 
+def test_decode_append_requires_the_new_tokens(lib):
+    fake = C.c_void_p(0x1000)
+    args = [fake] * 6 + [None, None, None, 4, 8, 2, 128, 16, 8, 64, C.c_float(0.1), 0, 0, None,
+                         0, None]
+    assert lib.pa_decode_append(*args) == 1          # k_new, v_new, slot_mapping missing
+    args[6:9] = [fake, C.c_void_p(0x1008), fake]
+    assert lib.pa_decode_append(*args) == 1          # misaligned v_new
+
+
 def test_cache_entry_points_reject_bad_scalars(lib):
     assert lib.pa_reshape_and_cache(None, None, None, None, None, 4, 8, 96, 16, 64, 0, None) == 2
     assert lib.pa_reshape_and_cache(None, None, None, None, None, -1, 8, 64, 16, 64, 0, None) == 1

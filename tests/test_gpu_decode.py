@@ -239,3 +239,54 @@ def test_other_stream(pa):
     s.synchronize()
     ref, _, _ = oracle.step(w)
     assert max_err(dw.out, ref) <= TOL["bf16"]
+
+
+# ---------------------------------------------------------------------------
+# pa_decode_append: reshape_and_cache + decode in one launch
+# ---------------------------------------------------------------------------
+def _append_cases():
+    return {
+        "tiny": synth.tiny(poison=True),
+        "gqa8b": synth.gqa8b(num_seqs=24, poison=True),
+        "ragged": synth.build("ragged", len(LENS), 16, 4, 128, "bf16", LENS, seed=55, append=True,
+                              poison=True),
+        "parsamp": synth.parsamp(num_prompts=2, samples=4, prompt_len=40, suffix_lens=[0] * 8,
+                                 num_heads=8, num_kv_heads=2, head_dim=64, poison=True),
+    }
+
+
+@pytest.mark.parametrize("mode", [-1, 0, 64])
+@pytest.mark.parametrize("name", ["tiny", "gqa8b", "ragged", "parsamp"])
+def test_decode_append_equals_separate_steps(pa, name, mode):
+    w = _append_cases()[name]
+    a = DevWorkload(w)
+    a.step(pa, partition_size=mode)                      # copy, reshape, decode
+    b = DevWorkload(w)
+    if b.pairs is not None:
+        pa.copy_blocks(b.k, b.v, b.pairs)
+    pa.decode_append(b.out, b.q, b.k, b.v, b.tables, b.lens, b.k_new, b.v_new, b.slots, w.scale,
+                     partition_size=mode)
+    assert torch.equal(a.out, b.out)
+    # pools hold NaN in unused slots: compare raw 16-bit patterns
+    assert torch.equal(a.k.view(torch.int16), b.k.view(torch.int16))
+    assert torch.equal(a.v.view(torch.int16), b.v.view(torch.int16))
+    assert pa.get_device_error() == 0
+    ref, k_ref, v_ref = oracle.step(w)
+    assert max_err(b.out, ref) <= TOL[w.dtype]
+    assert np.array_equal(host_bits(b.k), k_ref) and np.array_equal(host_bits(b.v), v_ref)
+
+
+def test_decode_append_rejects_a_slot_not_at_the_end(pa):
+    w = synth.tiny()
+    dw = DevWorkload(w)
+    k0 = dw.k.clone()
+    slots = dw.slots.clone()
+    s = int(np.argmax(w.seq_lens))                       # a sequence with several tokens
+    L = int(w.seq_lens[s])
+    pos = L - 2                                          # not the newest position
+    slots[s] = int(w.block_tables[s, pos // 16]) * 16 + pos % 16
+    pa.decode_append(dw.out, dw.q, dw.k, dw.v, dw.tables, dw.lens, dw.k_new, dw.v_new, slots,
+                     w.scale)
+    assert pa.get_device_error() & pa.DEVERR["APPEND_SLOT"]
+    blk, off = slots[s].item() // 16, slots[s].item() % 16
+    assert torch.equal(dw.k[blk, :, off], k0[blk, :, off])   # that token was not written

@@ -42,3 +42,15 @@ def test_full_size_step(pa, name):
             assert np.array_equal(host_bits(dw.v), v_ref)
         del dw
         torch.cuda.empty_cache()
+    if w.slot_mapping is not None:
+        # the launch configuration the benchmark times: the append fused into the decode
+        dw = DevWorkload(w)
+        if dw.pairs is not None:
+            pa.copy_blocks(dw.k, dw.v, dw.pairs)
+        pa.decode_append(dw.out, dw.q, dw.k, dw.v, dw.tables, dw.lens, dw.k_new, dw.v_new,
+                         dw.slots, w.scale, partition_size=MODES[name][0])
+        err = max_err(dw.out, ref)
+        assert err <= TOL[w.dtype], f"{name} fused append: max|err| {err}"
+        assert pa.get_device_error() == 0
+        assert np.array_equal(host_bits(dw.k), k_ref)
+        assert np.array_equal(host_bits(dw.v), v_ref)
