@@ -529,6 +529,80 @@ def run_ours(args):
     print(json.dumps(line), flush=True)
 
 
+def run_swap(args):
+    """Swap half the GQA batch's blocks out to a page-locked host pool and back
+    (pa_swap_blocks), timed with CUDA events; the denominator is the plain
+    pinned-memory copy rate of the same bytes measured in the same run."""
+    import torch
+    from paged_kv_cache_260_gb300 import _build
+    _build.build()
+    import paged_kv_cache_260_gb300 as pa
+    pa.load()
+    device = torch.device("cuda:0")
+    torch.cuda.set_device(device)
+    w = make_workload("gqa8b")
+    st = Step(w, device, 0)
+    seqs = range(0, w.num_seqs, 2)
+    blocks = np.concatenate([w.block_tables[s, :(int(w.seq_lens[s]) + 15) // 16] for s in seqs])
+    nb = len(blocks)
+    host_k = torch.empty((nb,) + tuple(st.k.shape[1:]), dtype=st.k.dtype).pin_memory()
+    host_v = torch.empty_like(host_k).pin_memory()
+    out_pairs = torch.from_numpy(np.stack([blocks, np.arange(nb)], 1).astype(np.int64)).to(device)
+    in_pairs = torch.from_numpy(np.stack([np.arange(nb), blocks], 1).astype(np.int64)).to(device)
+    moved = 2 * nb * st.k[0].numel() * st.k.element_size()      # K and V, one direction
+    for _ in range(args.warmup):
+        pa.swap_blocks(host_k, host_v, st.k, st.v, out_pairs)
+        pa.swap_blocks(st.k, st.v, host_k, host_v, in_pairs)
+    torch.cuda.synchronize(device)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    t_out = t_in = 0.0
+    steps = max(1, min(args.steps, 50))
+    for _ in range(steps):
+        ev[0].record()
+        pa.swap_blocks(host_k, host_v, st.k, st.v, out_pairs)
+        ev[1].record()
+        pa.swap_blocks(st.k, st.v, host_k, host_v, in_pairs)
+        ev[2].record()
+        torch.cuda.synchronize(device)
+        t_out += ev[0].elapsed_time(ev[1])
+        t_in += ev[1].elapsed_time(ev[2])
+    assert pa.get_device_error() == 0
+    # plain copies of the same bytes between device and page-locked host memory
+    dev_buf = torch.empty(moved, dtype=torch.uint8, device=device)
+    host_buf = torch.empty(moved, dtype=torch.uint8).pin_memory()
+    for _ in range(3):
+        host_buf.copy_(dev_buf, non_blocking=True)
+        dev_buf.copy_(host_buf, non_blocking=True)
+    torch.cuda.synchronize(device)
+    c_out = c_in = 0.0
+    for _ in range(steps):
+        ev[0].record()
+        host_buf.copy_(dev_buf, non_blocking=True)
+        ev[1].record()
+        dev_buf.copy_(host_buf, non_blocking=True)
+        ev[2].record()
+        torch.cuda.synchronize(device)
+        c_out += ev[0].elapsed_time(ev[1])
+        c_in += ev[1].elapsed_time(ev[2])
+    gbs = lambda t: moved * steps / (t * 1e-3) / 1e9
+    value = 2 * moved * steps / ((t_out + t_in) * 1e-3) / 1e9
+    peak = 2 * moved * steps / ((c_out + c_in) * 1e-3) / 1e9
+    print(json.dumps({
+        "metric": "swap_blocks: GB/s moved between the GPU pool and a page-locked host pool",
+        "value": value, "unit": "GB/s", "n_gpus": 1, "steps": steps, "warmup": args.warmup,
+        "ms_per_step": (t_out + t_in) / steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": f"swap out and back in {nb} blocks ({moved / 1e6:.0f} MB of K+V) "
+                               "of 64 of the 128 GQA-8B sequences, random block ids"},
+        "swap_out_gbs": gbs(t_out), "swap_in_gbs": gbs(t_in),
+        "roofline": {"bound": "host link", "achieved": value, "peak": peak, "unit": "GB/s",
+                     "frac": value / peak,
+                     "peak_source": "pinned-memory cudaMemcpy of the same bytes, same run",
+                     "copy_out_gbs": gbs(c_out), "copy_in_gbs": gbs(c_in)},
+        "gpu_launches": 2 * steps,
+    }), flush=True)
+
+
 def run_reference(args):
     """The oracle as the reference arm: each step is a bounded sample of the
     workload (whole sequences in order) on the host cores."""
@@ -580,7 +654,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=list(DESCRIPTION), default="gqa8b")
+    ap.add_argument("--workload", choices=list(DESCRIPTION) + ["swap"], default="gqa8b")
     ap.add_argument("--partition", type=int, default=None,
                     help="-1 no split, 0 balanced split, >0 fixed partition tokens")
     ap.add_argument("--no-graph", action="store_true")
@@ -590,6 +664,8 @@ def main(argv=None):
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "swap":
+        run_swap(args)
     else:
         run_ours(args)
 

@@ -231,6 +231,29 @@ int pa_copy_blocks(void *k_cache, void *v_cache, const int64_t *block_mapping,
                    int num_blocks, int dtype, void *stream);
 
 /*
+ * Swap blocks between two pools, for preemption: for every pair i,
+ *     dst_k[dst] = src_k[src], dst_v[dst] = src_v[src]
+ * whole blocks, (src, dst) = block_mapping[i][0], block_mapping[i][1].  One
+ * side is the GPU pool, the other a pool of the same layout in page-locked
+ * host memory (cudaHostAlloc / cudaHostRegister): blocks of a preempted
+ * sequence move to host memory and back instead of being recomputed (the
+ * swap row of the OS-paging table and section 系统实现要点 of the vLLM
+ * reading notes).  The copy is one kernel reading and writing both pools
+ * directly; on GB300 host memory is reached over NVLink-C2C.
+ *
+ *   src_num_blocks, dst_num_blocks  pool sizes in blocks
+ *   block_mapping  [num_pairs][2] int64, device or page-locked host memory
+ * Pools must be device memory, managed memory or page-locked host memory;
+ * anything else (pageable host memory) returns PA_ERR_INVALID_ARG.  Pairs
+ * naming a block outside its pool are skipped and set PA_DEVERR_BLOCK_RANGE.
+ * No dst may appear twice (not checked).  Bit-exact.
+ */
+int pa_swap_blocks(void *dst_k, void *dst_v, const void *src_k, const void *src_v,
+                   const int64_t *block_mapping, int num_pairs, int num_kv_heads,
+                   int head_dim, int block_size, int src_num_blocks, int dst_num_blocks,
+                   int dtype, void *stream);
+
+/*
  * Debug/test export: materialise each sequence's K and V contiguously,
  * read through its block table (the same indirection the decode uses):
  *     k_out[s][h][t][:] = k_cache[block_tables[s][t/16]][h][t%16][:],  t < seq_lens[s]

@@ -78,6 +78,9 @@ def lib():
         L.oracle_copy_blocks.argtypes = [_u16p, _u16p, _i64p, C.c_int, C.c_int, C.c_int,
                                          C.c_int, C.c_long]
         L.oracle_copy_blocks.restype = C.c_long
+        L.oracle_swap_blocks.argtypes = [_u16p, _u16p, _u16p, _u16p, _i64p, C.c_int, C.c_int,
+                                         C.c_int, C.c_int, C.c_long, C.c_long]
+        L.oracle_swap_blocks.restype = C.c_long
         _lib = L
     return _lib
 
@@ -239,6 +242,16 @@ def copy_blocks(k_cache, v_cache, block_mapping) -> int:
     nb, Hkv, _, D = k_cache.shape
     return int(lib().oracle_copy_blocks(k_cache, v_cache, bm, bm.shape[0], Hkv, D,
                                         BLOCK_SIZE, nb))
+
+
+def swap_blocks(dst_k, dst_v, src_k, src_v, block_mapping) -> int:
+    """Copy blocks src (of the source pools) -> dst (of the destination pools) in place."""
+    assert dst_k.flags.c_contiguous and dst_v.flags.c_contiguous
+    bm = _c(block_mapping, np.int64).reshape(-1, 2)
+    snb, Hkv, _, D = src_k.shape
+    dnb = dst_k.shape[0]
+    return int(lib().oracle_swap_blocks(dst_k, dst_v, _c(src_k, np.uint16), _c(src_v, np.uint16),
+                                        bm, bm.shape[0], Hkv, D, BLOCK_SIZE, snb, dnb))
 
 
 def step(w, threads=None):

@@ -320,3 +320,33 @@ long oracle_copy_blocks(uint16_t *k_cache, uint16_t *v_cache,
     }
     return bad;
 }
+
+/*
+ * Swap: for each (src, dst) pair copy block src of the source pools into
+ * block dst of the destination pools (every kv head and slot, K and V).  One
+ * pool side is GPU memory, the other host memory: preempted sequences' blocks
+ * move to host memory and back (the swap row of the OS-paging table and
+ * section 系统实现要点 of the vLLM reading notes).  Pairs naming a block
+ * outside its pool are skipped and counted in the return value.
+ */
+long oracle_swap_blocks(uint16_t *dst_k, uint16_t *dst_v, const uint16_t *src_k,
+                        const uint16_t *src_v, const int64_t *block_mapping, int num_pairs,
+                        int num_kv_heads, int head_dim, int block_size, long src_blocks,
+                        long dst_blocks)
+{
+    long bad = 0;
+    long per_block = (long)num_kv_heads * block_size * head_dim;
+    for (int i = 0; i < num_pairs; ++i) {
+        int64_t src = block_mapping[2 * i];
+        int64_t dst = block_mapping[2 * i + 1];
+        if (src < 0 || dst < 0 || src >= src_blocks || dst >= dst_blocks) {
+            ++bad;
+            continue;
+        }
+        for (long e = 0; e < per_block; ++e) {
+            dst_k[dst * per_block + e] = src_k[src * per_block + e];
+            dst_v[dst * per_block + e] = src_v[src * per_block + e];
+        }
+    }
+    return bad;
+}

@@ -18,7 +18,7 @@ import threading
 __all__ = [
     "PagedAttnError", "load", "version", "decode", "decode_workspace_size", "workspace_for",
     "decode_noalloc", "decode_append",
-    "reshape_and_cache", "copy_blocks", "gather_kv", "validate_tables", "get_device_error",
+    "reshape_and_cache", "copy_blocks", "swap_blocks", "gather_kv", "validate_tables", "get_device_error",
     "PA_DTYPE_F16", "PA_DTYPE_BF16", "DEVERR", "STATUS",
 ]
 
@@ -71,6 +71,8 @@ def load(path: str = LIB_PATH):
         L.pa_reshape_and_cache.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, vp]
         L.pa_copy_blocks.restype = i
         L.pa_copy_blocks.argtypes = [vp, vp, vp, i, i, i, i, i, i, vp]
+        L.pa_swap_blocks.restype = i
+        L.pa_swap_blocks.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, vp]
         L.pa_gather_kv.restype = i
         L.pa_gather_kv.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, vp]
         L.pa_validate_tables.restype = i
@@ -232,6 +234,20 @@ def copy_blocks(k_cache, v_cache, block_mapping, stream=None):
                                block_mapping.shape[0], hkv, d, bs, nb, _dtype_code(k_cache),
                                _stream(stream))
     _check("pa_copy_blocks", rc)
+
+
+def swap_blocks(dst_k, dst_v, src_k, src_v, block_mapping, stream=None):
+    """pa_swap_blocks: whole-block copies src -> dst between two pools (one of them
+    typically in page-locked host memory, e.g. ``torch.empty(..).pin_memory()``)."""
+    snb, hkv, bs, d = src_k.shape
+    dnb = dst_k.shape[0]
+    _require(dst_k.shape[1:] == src_k.shape[1:] and dst_v.shape == dst_k.shape and
+             src_v.shape == src_k.shape, "pool shapes")
+    _require(block_mapping.dim() == 2 and block_mapping.shape[1] == 2, "block_mapping shape")
+    rc = load().pa_swap_blocks(_ptr(dst_k), _ptr(dst_v), _ptr(src_k), _ptr(src_v),
+                               _ptr(block_mapping), block_mapping.shape[0], hkv, d, bs, snb, dnb,
+                               _dtype_code(src_k), _stream(stream))
+    _check("pa_swap_blocks", rc)
 
 
 def gather_kv(k_out, v_out, k_cache, v_cache, block_tables, seq_lens, stream=None):

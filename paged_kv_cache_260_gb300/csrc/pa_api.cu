@@ -499,8 +499,54 @@ int pa_copy_blocks(void *k_cache, void *v_cache, const int64_t *block_mapping, i
     rc = device_state(&ds);
     if (rc != PA_OK)
         return rc;
-    return cuda_status(launch_copy_blocks(k_cache, v_cache, block_mapping, num_pairs, num_kv_heads,
-                                          head_dim, num_blocks, ds->err,
+    return cuda_status(launch_copy_blocks(k_cache, v_cache, k_cache, v_cache, block_mapping,
+                                          num_pairs, num_kv_heads, head_dim, num_blocks,
+                                          num_blocks, ds->err, static_cast<cudaStream_t>(stream)));
+}
+
+// Device address of a pool the kernels may read or write: device or managed
+// memory, or host memory that is page-locked and mapped; nullptr otherwise.
+static void *device_view(void *p)
+{
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();   // keep the failed query out of later error checks
+        return nullptr;
+    }
+    if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged ||
+        a.type == cudaMemoryTypeHost)
+        return a.devicePointer;
+    return nullptr;
+}
+
+int pa_swap_blocks(void *dst_k, void *dst_v, const void *src_k, const void *src_v,
+                   const int64_t *block_mapping, int num_pairs, int num_kv_heads, int head_dim,
+                   int block_size, int src_num_blocks, int dst_num_blocks, int dtype, void *stream)
+{
+    int rc = check_common(num_kv_heads, head_dim, block_size, src_num_blocks, dtype);
+    if (rc != PA_OK)
+        return rc;
+    if (num_pairs < 0 || dst_num_blocks <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (num_pairs == 0)
+        return PA_OK;
+    if (!dst_k || !dst_v || !src_k || !src_v || !block_mapping)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned(dst_k, 16) || !aligned(dst_v, 16) || !aligned(src_k, 16) ||
+        !aligned(src_v, 16) || !aligned(block_mapping, 8))
+        return PA_ERR_INVALID_ARG;
+    DeviceState *ds;
+    rc = device_state(&ds);
+    if (rc != PA_OK)
+        return rc;
+    void *dk = device_view(dst_k), *dv = device_view(dst_v);
+    void *sk = device_view(const_cast<void *>(src_k)), *sv = device_view(const_cast<void *>(src_v));
+    void *bm = device_view(const_cast<int64_t *>(block_mapping));
+    if (!dk || !dv || !sk || !sv || !bm)
+        return PA_ERR_INVALID_ARG;     // pageable host memory: not reachable by the kernel
+    return cuda_status(launch_copy_blocks(dk, dv, sk, sv, static_cast<const int64_t *>(bm),
+                                          num_pairs, num_kv_heads, head_dim, src_num_blocks,
+                                          dst_num_blocks, ds->err,
                                           static_cast<cudaStream_t>(stream)));
 }
 

@@ -46,26 +46,28 @@ reshape_and_cache_kernel(const uint4 *__restrict__ k_new, const uint4 *__restric
 }
 
 // ---------------------------------------------------------------------------
-// copy_blocks: whole-block copies for copy-on-write.  blockIdx.y picks the
-// pair and K or V; each thread moves 4 vectors 256 apart (4 loads in flight).
+// Whole-block copies between pools: copy_blocks (copy-on-write, within one
+// pool) and swap_blocks (between the GPU pool and a pool in pinned host
+// memory, reached over the C2C link).  blockIdx.y picks the pair and K or V;
+// each thread moves 4 vectors 256 apart (4 loads in flight).
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256)
-copy_blocks_kernel(uint4 *k_cache, uint4 *v_cache, const int64_t *__restrict__ block_mapping,
-                   int num_pairs, long long block_vecs, long long num_blocks, uint32_t *err)
+copy_blocks_kernel(uint4 *dst_k, uint4 *dst_v, const uint4 *src_k, const uint4 *src_v,
+                   const int64_t *__restrict__ block_mapping, int num_pairs, long long block_vecs,
+                   long long src_blocks, long long dst_blocks, uint32_t *err)
 {
     grid_dependents_launch();
     const int pair = blockIdx.y >> 1;
     const bool is_v = blockIdx.y & 1;
     const int64_t src = __ldg(block_mapping + 2 * pair);
     const int64_t dst = __ldg(block_mapping + 2 * pair + 1);
-    if (src < 0 || dst < 0 || src >= num_blocks || dst >= num_blocks) {
+    if (src < 0 || dst < 0 || src >= src_blocks || dst >= dst_blocks) {
         if (blockIdx.x == 0 && threadIdx.x == 0 && !is_v)
             record_error(err, PA_DEVERR_BLOCK_RANGE);
         return;
     }
-    uint4 *pool = is_v ? v_cache : k_cache;
-    const uint4 *from = pool + src * block_vecs;
-    uint4 *to = pool + dst * block_vecs;
+    const uint4 *from = (is_v ? src_v : src_k) + src * block_vecs;
+    uint4 *to = (is_v ? dst_v : dst_k) + dst * block_vecs;
     constexpr int U = 4;
     for (long long base = (long long)blockIdx.x * 256 * U; base < block_vecs;
          base += (long long)gridDim.x * 256 * U) {
@@ -179,8 +181,9 @@ cudaError_t launch_reshape_and_cache(const void *k_new, const void *v_new, void 
     return cudaGetLastError();
 }
 
-cudaError_t launch_copy_blocks(void *k_cache, void *v_cache, const int64_t *block_mapping,
-                               int num_pairs, int num_kv_heads, int head_dim, int num_blocks,
+cudaError_t launch_copy_blocks(void *dst_k, void *dst_v, const void *src_k, const void *src_v,
+                               const int64_t *block_mapping, int num_pairs, int num_kv_heads,
+                               int head_dim, long long src_blocks, long long dst_blocks,
                                uint32_t *err, cudaStream_t stream)
 {
     const long long block_vecs = (long long)num_kv_heads * kBlockSize * head_dim * 2 / 16;
@@ -188,10 +191,10 @@ cudaError_t launch_copy_blocks(void *k_cache, void *v_cache, const int64_t *bloc
     for (int first = 0; first < num_pairs; first += 30000) {
         const int cnt = num_pairs - first < 30000 ? num_pairs - first : 30000;
         dim3 grid(gx, 2 * cnt);
-        copy_blocks_kernel<<<grid, 256, 0, stream>>>(static_cast<uint4 *>(k_cache),
-                                                     static_cast<uint4 *>(v_cache),
-                                                     block_mapping + 2LL * first, cnt, block_vecs,
-                                                     num_blocks, err);
+        copy_blocks_kernel<<<grid, 256, 0, stream>>>(
+            static_cast<uint4 *>(dst_k), static_cast<uint4 *>(dst_v),
+            static_cast<const uint4 *>(src_k), static_cast<const uint4 *>(src_v),
+            block_mapping + 2LL * first, cnt, block_vecs, src_blocks, dst_blocks, err);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess)
             return e;

@@ -11,8 +11,9 @@ cudaError_t launch_reshape_and_cache(const void *k_new, const void *v_new, void 
                                      int num_kv_heads, int head_dim, int num_blocks,
                                      uint32_t *err, int num_sms, cudaStream_t stream);
 
-cudaError_t launch_copy_blocks(void *k_cache, void *v_cache, const int64_t *block_mapping,
-                               int num_pairs, int num_kv_heads, int head_dim, int num_blocks,
+cudaError_t launch_copy_blocks(void *dst_k, void *dst_v, const void *src_k, const void *src_v,
+                               const int64_t *block_mapping, int num_pairs, int num_kv_heads,
+                               int head_dim, long long src_blocks, long long dst_blocks,
                                uint32_t *err, cudaStream_t stream);
 
 cudaError_t launch_gather_kv(void *k_out, void *v_out, const void *k_cache, const void *v_cache,

@@ -421,3 +421,30 @@ def test_workload_shapes():
     p = synth.parsamp(num_heads=4, num_kv_heads=1, head_dim=64)
     assert p.block_mapping.shape == (112, 2) and p.num_seqs == 128
     assert p.seq_lens.min() >= 1025 and p.seq_lens.max() <= 1024 + 256 + 1
+
+
+def test_swap_out_and_back_restores_blocks():
+    # preemption by swapping (OS-paging table): blocks go to a host pool and come back
+    w = synth.build("swap", 6, 16, 4, 64, "bf16", [40, 100, 300, 17, 64, 5], seed=8,
+                    pool_factor=3.0)
+    rng = np.random.default_rng(2)
+    seq_blocks = w.block_tables[2, :synth.cdiv(int(w.seq_lens[2]), 16)]
+    host_k = np.zeros((len(seq_blocks) + 3,) + w.k_cache.shape[1:], np.uint16)
+    host_v = np.zeros_like(host_k)
+    out_pairs = np.stack([seq_blocks, 3 + np.arange(len(seq_blocks))], 1).astype(np.int64)
+    assert oracle.swap_blocks(host_k, host_v, w.k_cache, w.v_cache, out_pairs) == 0
+    for src, dst in out_pairs:
+        assert np.array_equal(host_k[dst], w.k_cache[src]) and np.array_equal(host_v[dst], w.v_cache[src])
+    assert not host_k[:3].any()                           # untouched host blocks stay as they were
+    # back into other device blocks: decode through the remapped table is unchanged
+    free = np.setdiff1d(np.arange(w.num_blocks), w.block_tables[w.block_tables >= 0])
+    new_ids = rng.choice(free, size=len(seq_blocks), replace=False)
+    k2, v2 = w.k_cache.copy(), w.v_cache.copy()
+    in_pairs = np.stack([3 + np.arange(len(seq_blocks)), new_ids], 1).astype(np.int64)
+    assert oracle.swap_blocks(k2, v2, host_k, host_v, in_pairs) == 0
+    t2 = w.block_tables.copy()
+    t2[2, :len(seq_blocks)] = new_ids
+    base = oracle.decode(w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.scale, w.dtype)
+    again = oracle.decode(w.q, k2, v2, t2, w.seq_lens, w.scale, w.dtype)
+    assert np.array_equal(base, again)
+    assert oracle.swap_blocks(k2, v2, host_k, host_v, np.array([[0, w.num_blocks]])) == 1
