@@ -81,6 +81,10 @@ def lib():
         L.oracle_swap_blocks.argtypes = [_u16p, _u16p, _u16p, _u16p, _i64p, C.c_int, C.c_int,
                                          C.c_int, C.c_int, C.c_long, C.c_long]
         L.oracle_swap_blocks.restype = C.c_long
+        L.oracle_prefill.argtypes = [_f64p, _u16p, _u16p, _u16p, _i32p, _i32p, _i32p, C.c_int,
+                                     C.c_int, C.c_int, C.c_int, C.c_int, C.c_double, C.c_int,
+                                     C.c_int, C.c_int]
+        L.oracle_prefill.restype = None
         _lib = L
     return _lib
 
@@ -242,6 +246,32 @@ def copy_blocks(k_cache, v_cache, block_mapping) -> int:
     nb, Hkv, _, D = k_cache.shape
     return int(lib().oracle_copy_blocks(k_cache, v_cache, bm, bm.shape[0], Hkv, D,
                                         BLOCK_SIZE, nb))
+
+
+def prefill(q, k_cache, v_cache, block_tables, seq_lens, query_start, scale, dtype: str,
+            threads=None) -> np.ndarray:
+    """Chunked-prefill output [total_rows, Hq, D] in fp64 (causal over the pool)."""
+    q = _c(q, np.uint16)
+    k_cache = _c(k_cache, np.uint16)
+    v_cache = _c(v_cache, np.uint16)
+    block_tables = _c(block_tables, np.int32)
+    seq_lens = _c(seq_lens, np.int32)
+    query_start = _c(query_start, np.int32)
+    T, Hq, D = q.shape
+    S = seq_lens.shape[0]
+    out = np.zeros((T, Hq, D), dtype=np.float64)
+    L = lib()
+    dt = DTYPES[dtype]
+
+    def run(s):
+        L.oracle_prefill(out, q, k_cache, v_cache, block_tables, seq_lens, query_start, Hq,
+                         k_cache.shape[1], D, BLOCK_SIZE, block_tables.shape[1], float(scale), dt,
+                         s, s + 1)
+
+    nt = threads or num_threads()
+    with _cf.ThreadPoolExecutor(nt) as ex:
+        list(ex.map(run, range(S)))
+    return out
 
 
 def swap_blocks(dst_k, dst_v, src_k, src_v, block_mapping) -> int:

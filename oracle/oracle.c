@@ -99,16 +99,34 @@ static long pool_index(const int32_t *block_tables, int max_blocks_per_seq,
  * m = -inf, l = 0, o = 0.  The score vector is kept whole, as in dense
  * softmax: no running max, no tiling.
  */
+static void attend_row(double *o, double *m_out, double *l_out, const uint16_t *qh,
+                       const uint16_t *k_cache, const uint16_t *v_cache,
+                       const int32_t *block_tables, int max_blocks_per_seq,
+                       int num_heads, int num_kv_heads, int head_dim, int block_size,
+                       double scale, int dtype, int s, int h, int t0, int t1);
+
 void oracle_attend(double *o, double *m_out, double *l_out,
                    const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
                    const int32_t *block_tables, int max_blocks_per_seq,
                    int num_heads, int num_kv_heads, int head_dim, int block_size,
                    double scale, int dtype, int s, int h, int t0, int t1)
 {
+    attend_row(o, m_out, l_out, q + ((long)s * num_heads + h) * head_dim, k_cache, v_cache,
+               block_tables, max_blocks_per_seq, num_heads, num_kv_heads, head_dim, block_size,
+               scale, dtype, s, h, t0, t1);
+}
+
+/* The attention of one query row qh (query head h of sequence s) over the
+ * sequence's tokens [t0, t1); see oracle_attend. */
+static void attend_row(double *o, double *m_out, double *l_out, const uint16_t *qh,
+                       const uint16_t *k_cache, const uint16_t *v_cache,
+                       const int32_t *block_tables, int max_blocks_per_seq,
+                       int num_heads, int num_kv_heads, int head_dim, int block_size,
+                       double scale, int dtype, int s, int h, int t0, int t1)
+{
     int D = head_dim;
     int G = num_heads / num_kv_heads;
     int kvh = h / G;
-    const uint16_t *qh = q + ((long)s * num_heads + h) * D;
     for (int d = 0; d < D; ++d)
         o[d] = 0.0;
     if (t1 <= t0) {
@@ -349,4 +367,36 @@ long oracle_swap_blocks(uint16_t *dst_k, uint16_t *dst_v, const uint16_t *src_k,
         }
     }
     return bad;
+}
+
+/*
+ * Paged prefill of a chunk of new tokens per sequence (chunked prefill, the
+ * Sarathi-Serve scheme in the notes: a long prompt is processed in chunks,
+ * interleaved with decode steps).  The chunk of sequence s is rows
+ * query_start[s] .. query_start[s+1] of q ([total][num_heads][D]); they are
+ * the last positions of the sequence, whose length seq_lens[s] includes the
+ * chunk, and their K/V are already in the pool.  Row i of the chunk sits at
+ * position p = seq_lens[s] - chunk + i and attends causally to tokens 0..p.
+ * out[row][h][d] (double), for sequences [seq_begin, seq_end).
+ */
+void oracle_prefill(double *out, const uint16_t *q, const uint16_t *k_cache,
+                    const uint16_t *v_cache, const int32_t *block_tables,
+                    const int32_t *seq_lens, const int32_t *query_start, int num_heads,
+                    int num_kv_heads, int head_dim, int block_size, int max_blocks_per_seq,
+                    double scale, int dtype, int seq_begin, int seq_end)
+{
+    for (int s = seq_begin; s < seq_end; ++s) {
+        int chunk = query_start[s + 1] - query_start[s];
+        for (int i = 0; i < chunk; ++i) {
+            long row = query_start[s] + i;
+            int p = seq_lens[s] - chunk + i;
+            for (int h = 0; h < num_heads; ++h) {
+                double m, l;
+                attend_row(out + (row * num_heads + h) * head_dim, &m, &l,
+                           q + (row * num_heads + h) * head_dim, k_cache, v_cache,
+                           block_tables, max_blocks_per_seq, num_heads, num_kv_heads,
+                           head_dim, block_size, scale, dtype, s, h, 0, p + 1);
+            }
+        }
+    }
 }

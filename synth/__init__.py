@@ -130,6 +130,7 @@ class Workload:
     tables_before_cow: Optional[np.ndarray] = None
     live: Optional[np.ndarray] = None
     partition_size: int = 0
+    query_start: Optional[np.ndarray] = None   # prefill: rows of q per sequence [S+1]
     meta: dict = field(default_factory=dict)
 
     @property
@@ -404,12 +405,42 @@ def parsamp(poison=False, seed=1005, num_prompts=16, samples=8, prompt_len=1024,
     return w
 
 
+def build_prefill(name: str, num_heads: int, num_kv_heads: int, head_dim: int, dtype: str,
+                  seq_lens, chunk_lens, seed: int, *, pool_factor: float = 1.25,
+                  poison: bool = False, max_blocks: Optional[int] = None) -> Workload:
+    """A chunked-prefill step: sequence s holds seq_lens[s] tokens whose last
+    chunk_lens[s] are the chunk being prefilled (their K/V already in the
+    pool); q has one row per chunk token, rows of sequence s starting at
+    query_start[s]."""
+    seq_lens = np.asarray(seq_lens, dtype=np.int32)
+    chunk_lens = np.asarray(chunk_lens, dtype=np.int32)
+    assert np.all(chunk_lens <= seq_lens)
+    w = build(name, len(seq_lens), num_heads, num_kv_heads, head_dim, dtype, seq_lens, seed,
+              pool_factor=pool_factor, poison=poison, max_blocks=max_blocks)
+    qs = np.zeros(len(seq_lens) + 1, dtype=np.int32)
+    qs[1:] = np.cumsum(chunk_lens)
+    ss = np.random.SeedSequence([seed, 11])
+    w.q = _normal_bits(ss, int(qs[-1]) * num_heads * head_dim, dtype).reshape(
+        int(qs[-1]), num_heads, head_dim)
+    w.query_start = qs
+    return w
+
+
+def prefill_chunks(seed=1006):
+    """Chunked prefill, GQA-8B-shaped: 8 sequences, 32/8 heads, head_dim 128,
+    bf16; contexts U[512, 4096] ending in a 512-token chunk."""
+    rng = _len_rng(seed)
+    lens = rng.integers(512, 4096, size=8, endpoint=True)
+    return build_prefill("prefill", 32, 8, 128, BF16, lens, np.full(8, 512), seed)
+
+
 WORKLOADS = {
     "tiny": tiny,
     "mha7b": mha7b,
     "gqa8b": gqa8b,
     "long": long,
     "parsamp": parsamp,
+    "prefill": prefill_chunks,
 }
 
 

@@ -448,3 +448,47 @@ def test_swap_out_and_back_restores_blocks():
     again = oracle.decode(w.q, k2, v2, t2, w.seq_lens, w.scale, w.dtype)
     assert np.array_equal(base, again)
     assert oracle.swap_blocks(k2, v2, host_k, host_v, np.array([[0, w.num_blocks]])) == 1
+
+
+# ---------------------------------------------------------------------------
+# chunked prefill (causal attention of a chunk of new tokens over the pool)
+# ---------------------------------------------------------------------------
+def _prefill_case(dtype="f16", Hq=8, Hkv=2, D=32):
+    return synth.build_prefill("pf", Hq, Hkv, D, dtype, [5, 40, 70, 16], [5, 17, 33, 1], seed=31)
+
+
+def test_prefill_rows_are_decodes_of_their_prefixes():
+    w = _prefill_case()
+    out = oracle.prefill(w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.query_start,
+                         w.scale, w.dtype)
+    for s in range(w.num_seqs):
+        c = w.query_start[s + 1] - w.query_start[s]
+        for i in range(c):
+            row = w.query_start[s] + i
+            p = int(w.seq_lens[s]) - c + i
+            one = oracle.decode(w.q[row][None], w.k_cache, w.v_cache, w.block_tables[s][None],
+                                np.array([p + 1], np.int32), w.scale, w.dtype)
+            assert np.array_equal(out[row], one[0])
+
+
+@pytest.mark.parametrize("Hq,Hkv,D,dtype", [(4, 4, 16, "f16"), (8, 2, 64, "bf16")])
+def test_prefill_equals_causal_sdpa(Hq, Hkv, D, dtype):
+    rng = np.random.default_rng(12)
+    lens, chunks = [30, 64, 9], [30, 20, 4]
+    q_, k, v, tables = _contiguous_case(rng, lens, Hq, Hkv, D, dtype)
+    qs = np.concatenate([[0], np.cumsum(chunks)]).astype(np.int32)
+    q = synth.to_bits(rng.standard_normal((qs[-1], Hq, D)).astype(np.float32), dtype)
+    scale = 1.0 / math.sqrt(D)
+    out = oracle.prefill(q, k, v, tables, np.array(lens, np.int32), qs, scale, dtype)
+    kd, vd, qd = (oracle.decode_bits(x, dtype) for x in (k, v, q))
+    for s, (L, c) in enumerate(zip(lens, chunks)):
+        blocks = tables[s, :synth.cdiv(L, 16)]
+        kc = np.concatenate([kd[b] for b in blocks], axis=1)[:, :L]
+        vc = np.concatenate([vd[b] for b in blocks], axis=1)[:, :L]
+        # chunk row i (position L-c+i) may see tokens 0..L-c+i
+        mask = np.arange(L)[None, :] <= (L - c + np.arange(c))[:, None]
+        ref = F.scaled_dot_product_attention(
+            torch.from_numpy(qd[qs[s]:qs[s + 1]]).permute(1, 0, 2)[None],
+            torch.from_numpy(kc)[None], torch.from_numpy(vc)[None],
+            attn_mask=torch.from_numpy(mask), scale=scale, enable_gqa=True)[0].permute(1, 0, 2)
+        np.testing.assert_allclose(out[qs[s]:qs[s + 1]], ref.numpy(), rtol=0, atol=1e-12)
