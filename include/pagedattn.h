@@ -276,6 +276,14 @@ int pa_validate_tables(const int32_t *block_tables, const int32_t *seq_lens,
                        int block_size, uint32_t *bad_count, void *stream);
 
 /*
+ * Test export for the failure path every copy wait shares: a kernel arms an
+ * mbarrier for bytes no copy will deliver and waits with a limit of
+ * limit_us microseconds (1..1e6).  The wait must give up, set
+ * PA_DEVERR_TIMEOUT and let the kernel finish, leaving the context usable.
+ */
+int pa_selftest_bounded_wait(int limit_us, void *stream);
+
+/*
  * Synchronise `stream`, return in *bits the PA_DEVERR_* bits kernels on the
  * current device have recorded since the last clear, and clear them when
  * `clear` is non-zero.  Returns PA_ERR_DEVICE when bits is non-zero.

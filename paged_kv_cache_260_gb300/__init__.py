@@ -77,6 +77,8 @@ def load(path: str = LIB_PATH):
         L.pa_gather_kv.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, vp]
         L.pa_validate_tables.restype = i
         L.pa_validate_tables.argtypes = [vp, vp, i, i, i, i, vp, vp]
+        L.pa_selftest_bounded_wait.restype = i
+        L.pa_selftest_bounded_wait.argtypes = [i, vp]
         L.pa_get_device_error.restype = i
         L.pa_get_device_error.argtypes = [vp, C.POINTER(C.c_uint32), i]
         _lib = L
@@ -267,6 +269,12 @@ def validate_tables(block_tables, seq_lens, num_blocks, bad_count, stream=None):
     rc = load().pa_validate_tables(_ptr(block_tables), _ptr(seq_lens), n, mb, num_blocks,
                                    BLOCK_SIZE, _ptr(bad_count), _stream(stream))
     _check("pa_validate_tables", rc)
+
+
+def selftest_bounded_wait(limit_us=2000, stream=None):
+    """pa_selftest_bounded_wait: a copy wait that must time out and report it."""
+    _check("pa_selftest_bounded_wait", load().pa_selftest_bounded_wait(int(limit_us),
+                                                                       _stream(stream)))
 
 
 def get_device_error(clear=True, stream=None) -> int:

@@ -599,6 +599,18 @@ int pa_validate_tables(const int32_t *block_tables, const int32_t *seq_lens, int
                                               static_cast<cudaStream_t>(stream)));
 }
 
+int pa_selftest_bounded_wait(int limit_us, void *stream)
+{
+    if (limit_us <= 0 || limit_us > 1000000)
+        return PA_ERR_INVALID_ARG;
+    DeviceState *ds;
+    int rc = device_state(&ds);
+    if (rc != PA_OK)
+        return rc;
+    return cuda_status(launch_bounded_wait_selftest((uint64_t)limit_us * 1000, ds->err,
+                                                    static_cast<cudaStream_t>(stream)));
+}
+
 int pa_get_device_error(void *stream, uint32_t *bits, int clear)
 {
     if (!bits)

@@ -156,6 +156,27 @@ validate_tables_kernel(const int32_t *__restrict__ block_tables,
 }
 
 // ---------------------------------------------------------------------------
+// Self-test of the bounded wait: an mbarrier expects bytes that no copy will
+// deliver, so the wait must give up after limit_ns, record
+// PA_DEVERR_TIMEOUT and let the kernel finish.  Nothing is in flight.
+// ---------------------------------------------------------------------------
+__global__ void bounded_wait_selftest_kernel(uint64_t limit_ns, uint32_t *err)
+{
+    __shared__ __align__(8) uint64_t bar;
+    const uint32_t b = smem_addr(&bar);
+    if (threadIdx.x == 0) {
+        mbar_init(b, 1);
+        mbar_init_fence();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0)
+        mbar_arrive_expect_tx(b, 16);      // 16 bytes that never arrive
+    __syncthreads();
+    if (!mbar_wait_bounded(b, 0, limit_ns) && threadIdx.x == 0)
+        record_error(err, PA_DEVERR_TIMEOUT);
+}
+
+// ---------------------------------------------------------------------------
 // launchers
 // ---------------------------------------------------------------------------
 static int grid_for(long long work, int threads, int num_sms)
@@ -223,6 +244,12 @@ cudaError_t launch_validate_tables(const int32_t *block_tables, const int32_t *s
     const long long total = (long long)num_seqs * max_blocks;
     validate_tables_kernel<<<grid_for(total, 256, num_sms), 256, 0, stream>>>(
         block_tables, seq_lens, num_seqs, max_blocks, num_blocks, bad_count);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bounded_wait_selftest(uint64_t limit_ns, uint32_t *err, cudaStream_t stream)
+{
+    bounded_wait_selftest_kernel<<<1, 32, 0, stream>>>(limit_ns, err);
     return cudaGetLastError();
 }
 

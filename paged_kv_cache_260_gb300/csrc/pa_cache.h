@@ -25,4 +25,6 @@ cudaError_t launch_validate_tables(const int32_t *block_tables, const int32_t *s
                                    int num_seqs, int max_blocks, int num_blocks,
                                    uint32_t *bad_count, int num_sms, cudaStream_t stream);
 
+cudaError_t launch_bounded_wait_selftest(uint64_t limit_ns, uint32_t *err, cudaStream_t stream);
+
 }  // namespace pa

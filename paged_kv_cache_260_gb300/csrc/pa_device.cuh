@@ -59,14 +59,15 @@ __device__ __forceinline__ uint64_t global_ns()
 }
 
 // Wait for phase `parity` of the barrier to complete; give up after
-// kWaitLimitNs and return false instead of spinning forever.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
+// limit_ns and return false instead of spinning forever.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  uint64_t limit_ns = kWaitLimitNs)
 {
     if (mbar_try_wait(bar, parity))
         return true;
     const uint64_t t0 = global_ns();
     while (!mbar_try_wait(bar, parity)) {
-        if (global_ns() - t0 > kWaitLimitNs)
+        if (global_ns() - t0 > limit_ns)
             return false;
     }
     return true;

@@ -133,3 +133,17 @@ def test_validate_tables_counts_bad_entries(pa):
                        w.num_blocks, cnt)
     n_read_bad = int(tables[1, -1] == 9999 and (w.seq_lens[1] + 15) // 16 == tables.shape[1])
     assert int(cnt.item()) == 2 + n_read_bad
+
+
+def test_bounded_wait_gives_up_and_reports(pa):
+    # a copy wait that nothing completes: the kernel must time out, flag it,
+    # finish, and leave the context usable
+    assert pa.get_device_error() == 0
+    pa.selftest_bounded_wait(2000)
+    assert pa.get_device_error() == pa.DEVERR["TIMEOUT"]
+    w = synth.tiny(poison=True)
+    dw = DevWorkload(w)
+    dw.step(pa)
+    ref, _, _ = oracle.step(w)
+    assert float(np.abs(dw.out.float().cpu().numpy() - ref).max()) <= 4e-3
+    assert pa.get_device_error() == 0
