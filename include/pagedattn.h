@@ -62,6 +62,7 @@ enum pa_dtype { PA_DTYPE_F16 = 0, PA_DTYPE_BF16 = 1 };
 #define PA_DEVERR_SEQLEN_RANGE 0x8u  /* seq_len < 0 or > max_blocks_per_seq*block_size */
 #define PA_DEVERR_TIMEOUT      0x10u /* a bounded wait on a copy expired */
 #define PA_DEVERR_APPEND_SLOT  0x20u /* decode_append: slot is not the last position's */
+#define PA_DEVERR_QUERY_RANGE  0x40u /* prefill: chunk < 0, > seq_len or > max_query_len */
 
 /* PAGEDATTN_VERSION of the loaded library. */
 int pa_version(void);
@@ -130,6 +131,42 @@ int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache
               int block_size, int max_blocks_per_seq, int num_blocks,
               float scale, int dtype, int partition_size,
               void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Chunked-prefill attention over the paged pool: the newest tokens of each
+ * sequence (a prompt chunk) attend causally to everything before them and to
+ * one another.  Long prompts are cut into chunks that share steps with
+ * decodes (vLLM deep notes, section "调度优化：Continuous / Chunked /
+ * Disaggregated", part Chunked Prefill; forum summary, section
+ * "Sarathi-Serve：Chunked-Prefill技术"); the chunks of a step are packed
+ * back to back into one flat batch of rows, as in continuous batching (the
+ * same section of the deep notes).
+ *
+ * Sequence s has seq_lens[s] = L tokens in the pool, its newest
+ * c = query_start[s+1] - query_start[s] tokens being the chunk (their K/V
+ * are written first, e.g. by pa_reshape_and_cache).  Query row i of the
+ * chunk is at position L - c + i and its output is
+ *     out[query_start[s] + i, h, :] = sum_{t <= L-c+i} softmax_t(scale q.k_t) v_t
+ * with kv head h / (num_heads / num_kv_heads) and k_t, v_t gathered through
+ * the block table as in pa_decode.
+ *
+ *   out, q        [total_q][num_heads][head_dim] dtype, 16-byte aligned;
+ *                 total_q = query_start[num_seqs]
+ *   query_start   [num_seqs + 1] int32, non-decreasing, query_start[0] = 0
+ *   seq_lens      [num_seqs] int32, chunk <= len <= max_blocks_per_seq * 16
+ *   max_query_len host copy of the longest chunk: it sizes the grid
+ *   other arguments as in pa_decode.
+ * Rows are computed on the fifth-generation tensor cores (S = Q.K^T and
+ * O += P.V with fp32 accumulators in tensor memory); P is rounded to dtype
+ * before P.V.  A chunk longer than its sequence or than max_query_len is
+ * skipped and sets PA_DEVERR_QUERY_RANGE; table entries outside the pool set
+ * PA_DEVERR_TABLE_RANGE (block 0 is read instead).  No workspace; one launch.
+ */
+int pa_prefill(void *out, const void *q, const void *k_cache, const void *v_cache,
+               const int32_t *block_tables, const int32_t *seq_lens, const int32_t *query_start,
+               int num_seqs, int max_query_len, int num_heads, int num_kv_heads, int head_dim,
+               int block_size, int max_blocks_per_seq, int num_blocks, float scale, int dtype,
+               void *stream);
 
 /*
  * One decode step with the new tokens appended on the way: the result equals

@@ -28,7 +28,7 @@ BLOCK_SIZE = 16
 STATUS = {0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED", 3: "PA_ERR_WORKSPACE",
           4: "PA_ERR_CUDA", 5: "PA_ERR_DEVICE"}
 DEVERR = {"SLOT_RANGE": 0x1, "BLOCK_RANGE": 0x2, "TABLE_RANGE": 0x4, "SEQLEN_RANGE": 0x8,
-          "TIMEOUT": 0x10, "APPEND_SLOT": 0x20}
+          "TIMEOUT": 0x10, "APPEND_SLOT": 0x20, "QUERY_RANGE": 0x40}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libpagedattn.so")
@@ -77,6 +77,8 @@ def load(path: str = LIB_PATH):
         L.pa_gather_kv.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, vp]
         L.pa_validate_tables.restype = i
         L.pa_validate_tables.argtypes = [vp, vp, i, i, i, i, vp, vp]
+        L.pa_prefill.restype = i
+        L.pa_prefill.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i, vp]
         L.pa_selftest_bounded_wait.restype = i
         L.pa_selftest_bounded_wait.argtypes = [i, vp]
         L.pa_get_device_error.restype = i
@@ -193,6 +195,30 @@ def decode_append(out, q, k_cache, v_cache, block_tables, seq_lens, k_new, v_new
                                  float(scale), _dtype_code(q), int(partition_size),
                                  _ptr(workspace), wbytes, _stream(stream))
     _check("pa_decode_append", rc)
+    return out
+
+
+def prefill(out, q, k_cache, v_cache, block_tables, seq_lens, query_start, max_query_len, scale,
+            stream=None):
+    """pa_prefill: causal attention of each sequence's newest chunk over the paged pool.
+
+    q, out [total_q, num_heads, head_dim], the chunks packed back to back;
+    query_start int32 [num_seqs + 1]; seq_lens int32 [num_seqs] counts the
+    chunk; max_query_len (host int) is the longest chunk.
+    """
+    t, hq, d = q.shape
+    nb, hkv, bs, d2 = k_cache.shape
+    n = seq_lens.shape[0]
+    _require(out.shape == q.shape and d2 == d and v_cache.shape == k_cache.shape, "shapes")
+    _require(block_tables.dim() == 2 and block_tables.shape[0] == n and
+             query_start.shape == (n + 1,), "table shapes")
+    for x in (out, q, k_cache, v_cache, block_tables, seq_lens, query_start):
+        _require(x.is_cuda and x.is_contiguous(), "tensors must be contiguous CUDA tensors")
+    rc = load().pa_prefill(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                           _ptr(seq_lens), _ptr(query_start), n, int(max_query_len), hq, hkv, d,
+                           bs, block_tables.shape[1], nb, float(scale), _dtype_code(q),
+                           _stream(stream))
+    _check("pa_prefill", rc)
     return out
 
 

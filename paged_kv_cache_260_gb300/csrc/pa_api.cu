@@ -454,6 +454,74 @@ int pa_decode_append(void *out, const void *q, void *k_cache, void *v_cache,
                        slot_mapping);
 }
 
+int pa_prefill(void *out, const void *q, const void *k_cache, const void *v_cache,
+               const int32_t *block_tables, const int32_t *seq_lens, const int32_t *query_start,
+               int num_seqs, int max_query_len, int num_heads, int num_kv_heads, int head_dim,
+               int block_size, int max_blocks_per_seq, int num_blocks, float scale, int dtype,
+               void *stream)
+{
+    int rc = check_common(num_kv_heads, head_dim, block_size, num_blocks, dtype);
+    if (rc != PA_OK)
+        return rc;
+    if (num_seqs < 0 || max_query_len < 0 || num_heads <= 0 || max_blocks_per_seq <= 0 ||
+        !isfinite(scale) || num_heads % num_kv_heads)
+        return PA_ERR_INVALID_ARG;
+    const int group = num_heads / num_kv_heads;
+    if (group > kPrefillRows)
+        return PA_ERR_UNSUPPORTED;
+    if (num_seqs == 0 || max_query_len == 0)
+        return PA_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens || !query_start)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(block_tables, 4) || !aligned(seq_lens, 4) || !aligned(query_start, 4))
+        return PA_ERR_INVALID_ARG;
+    const long long pool_rows = (long long)num_blocks * num_kv_heads * kBlockSize;
+    const int tokens_per_block = kPrefillRows / group;
+    const long long q_ranks = (max_query_len + tokens_per_block - 1) / tokens_per_block;
+    const long long grid = q_ranks * num_seqs * num_kv_heads;
+    if ((long long)max_blocks_per_seq * kBlockSize >= (1LL << 30) || pool_rows >= (1LL << 31) ||
+        grid >= (1LL << 31))
+        return PA_ERR_UNSUPPORTED;
+    PrefillKernel kk{};
+    if (!prefill_kernel(dtype, head_dim, &kk))
+        return PA_ERR_UNSUPPORTED;
+    DeviceState *ds;
+    rc = device_state(&ds);
+    if (rc != PA_OK)
+        return rc;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (kk.smem > ds->smem_optin)
+        return PA_ERR_UNSUPPORTED;
+    rc = ensure_smem(kk.fn, dev, kk.smem);
+    if (rc != PA_OK)
+        return rc;
+    CUtensorMap tmk, tmv;
+    rc = make_pool_map(&tmk, k_cache, dtype, head_dim, pool_rows);
+    if (rc == PA_OK)
+        rc = make_pool_map(&tmv, v_cache, dtype, head_dim, pool_rows);
+    if (rc != PA_OK)
+        return rc;
+    PrefillParams p{};
+    p.out = out;
+    p.q = q;
+    p.block_tables = block_tables;
+    p.seq_lens = seq_lens;
+    p.query_start = query_start;
+    p.err = ds->err;
+    p.num_seqs = num_seqs;
+    p.num_heads = num_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.max_blocks = max_blocks_per_seq;
+    p.num_blocks = num_blocks;
+    p.q_ranks = (int)q_ranks;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    void *args[] = {&p, &tmk, &tmv};
+    return cuda_status(cudaLaunchKernel(kk.fn, dim3((unsigned)grid), dim3(kk.threads), args,
+                                        kk.smem, static_cast<cudaStream_t>(stream)));
+}
+
 int pa_reshape_and_cache(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
                          const int64_t *slot_mapping, int num_tokens, int num_kv_heads,
                          int head_dim, int block_size, int num_blocks, int dtype, void *stream)

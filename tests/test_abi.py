@@ -31,7 +31,8 @@ def declared_symbols():
 
 def test_header_declares_the_boundary():
     syms = declared_symbols()
-    for s in ("pa_decode", "pa_reshape_and_cache", "pa_copy_blocks", "pa_decode_workspace_size",
+    for s in ("pa_decode", "pa_prefill", "pa_reshape_and_cache", "pa_copy_blocks",
+              "pa_decode_workspace_size",
               "pa_gather_kv", "pa_validate_tables", "pa_get_device_error", "pa_status_string",
               "pa_version"):
         assert s in syms
@@ -111,3 +112,24 @@ def test_fixed_partition_workspace_size(lib):
     assert got == 0 or got > documented          # 0: no device to size the slots for
     assert lib.pa_decode_workspace_size(S, Hq, Hkv, D, mb, -1) == 0
     assert lib.pa_decode_workspace_size(S, Hq, Hkv, D, mb, 24) == 0     # not a multiple of 16
+
+
+def test_prefill_rejects_bad_scalars(lib):
+    fake = C.c_void_p(0x1000)
+
+    def call(**kw):
+        a = dict(ptrs=[None] * 7, num_seqs=2, max_q=32, hq=8, hkv=2, d=128, bs=16, maxb=8,
+                 nb=64, scale=0.1, dtype=1)
+        a.update(kw)
+        return lib.pa_prefill(*a["ptrs"], a["num_seqs"], a["max_q"], a["hq"], a["hkv"], a["d"],
+                              a["bs"], a["maxb"], a["nb"], C.c_float(a["scale"]), a["dtype"], None)
+
+    assert call(d=96) == 2
+    assert call(bs=32) == 2
+    assert call(hq=7) == 1
+    assert call(hq=258, hkv=1) == 2                  # group over 128 rows
+    assert call(scale=float("inf")) == 1
+    assert call(max_q=-1) == 1
+    assert call(num_seqs=0) == 0 and call(max_q=0) == 0
+    assert call() == 1                               # null pointers
+    assert call(ptrs=[fake, C.c_void_p(0x1008)] + [fake] * 5) == 1   # misaligned q

@@ -1,0 +1,147 @@
+"""GPU parity of pa_prefill (tcgen05 chunked-prefill attention) against the
+fp64 oracle: ragged chunks over ragged contexts, every supported head size,
+both dtypes, GQA groups that do and do not divide the 128-row tile, pools
+poisoned with NaN outside live tokens, empty chunks, whole-prompt chunks, and
+the error paths.  At the full prefill workload, sampled rows are checked
+against the oracle's decode of the row's prefix (equal to its prefill row,
+which the oracle tests pin)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from gpu_util import TOL, TORCH_DTYPE, dev_bits, max_err
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(pa, w, max_query_len=None, tables=None):
+    q = dev_bits(w.q, w.dtype)
+    k, v = dev_bits(w.k_cache, w.dtype), dev_bits(w.v_cache, w.dtype)
+    out = torch.full_like(q, float("nan"))
+    qs = torch.from_numpy(w.query_start).cuda()
+    t = torch.from_numpy(w.block_tables if tables is None else tables).cuda()
+    mq = int(np.diff(w.query_start).max()) if max_query_len is None else max_query_len
+    pa.prefill(out, q, k, v, t, torch.from_numpy(w.seq_lens).cuda(), qs, mq, w.scale)
+    return out
+
+
+def _ref(w):
+    return oracle.prefill(w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.query_start,
+                          w.scale, w.dtype)
+
+
+CASES = [
+    # Hq, Hkv, D, dtype, seq_lens, chunk_lens
+    (8, 2, 128, "bf16", [300, 70, 129, 1000, 64, 17], [300, 33, 1, 200, 64, 5]),
+    (8, 8, 64, "f16", [40, 257, 511, 96], [40, 150, 77, 96]),
+    (32, 4, 128, "f16", [700, 65, 33], [140, 65, 20]),
+    (16, 16, 128, "bf16", [130, 1], [130, 1]),
+    (12, 4, 64, "bf16", [250, 90, 400], [250, 43, 61]),      # G = 3: 42 tokens, 2 idle rows
+    (32, 2, 128, "bf16", [500, 200], [97, 200]),             # G = 16: 8 tokens per block
+]
+
+
+@pytest.mark.parametrize("case", range(len(CASES)))
+def test_prefill_matches_oracle(pa, case):
+    hq, hkv, d, dt, lens, chunks = CASES[case]
+    w = synth.build_prefill("pf", hq, hkv, d, dt, lens, chunks, seed=40 + case, poison=True)
+    out = _run(pa, w)
+    assert pa.get_device_error() == 0
+    assert max_err(out, _ref(w)) <= TOL[dt]
+
+
+def test_prefill_empty_chunks_and_untouched_rows(pa):
+    w = synth.build_prefill("pf", 8, 2, 128, "f16", [50, 80, 30, 200], [0, 80, 0, 64], seed=9,
+                            poison=True)
+    out = _run(pa, w)
+    assert pa.get_device_error() == 0
+    assert out.shape[0] == 144
+    assert max_err(out, _ref(w)) <= TOL["f16"]
+
+
+def test_prefill_chunk_longer_than_max_query_len_is_reported(pa):
+    w = synth.build_prefill("pf", 8, 2, 64, "bf16", [300, 100], [300, 40], seed=5)
+    _run(pa, w, max_query_len=100)       # 300 rows do not fit 100
+    assert pa.get_device_error() & pa.DEVERR["QUERY_RANGE"]
+    w2 = synth.build_prefill("pf", 8, 2, 64, "bf16", [30, 100], [30, 40], seed=5)
+    w2.seq_lens[0] = 20                  # chunk of 30 longer than its sequence
+    out = _run(pa, w2)
+    assert pa.get_device_error() == pa.DEVERR["QUERY_RANGE"]
+    ref = _ref_rows(w2, 1)
+    assert max_err(out[30:], ref) <= TOL["bf16"]
+
+
+def _ref_rows(w, s):
+    qs = w.query_start
+    return oracle.prefill(w.q[qs[s]:qs[s + 1]], w.k_cache, w.v_cache, w.block_tables[s:s + 1],
+                          w.seq_lens[s:s + 1], np.array([0, qs[s + 1] - qs[s]], np.int32),
+                          w.scale, w.dtype)
+
+
+def test_prefill_bad_table_entry_is_reported(pa):
+    w = synth.build_prefill("pf", 8, 2, 128, "f16", [100, 60], [30, 60], seed=6)
+    tables = w.block_tables.copy()
+    tables[0, 2] = w.num_blocks + 5
+    _run(pa, w, tables=tables)
+    assert pa.get_device_error() == pa.DEVERR["TABLE_RANGE"]
+
+
+def test_prefill_full_workload_sampled_rows(pa):
+    # the 8 x 512-token chunk workload; 3 rows of every sequence and all heads
+    # checked against the oracle's decode of the row's prefix
+    w = synth.prefill_chunks()
+    out = _run(pa, w)
+    assert pa.get_device_error() == 0
+    got = out.float().cpu().numpy().astype(np.float64)
+    assert np.isfinite(got).all()
+    rng = np.random.default_rng(3)
+    for s in range(w.num_seqs):
+        c = int(w.query_start[s + 1] - w.query_start[s])
+        for i in sorted(set([0, c - 1, int(rng.integers(c))])):
+            row = int(w.query_start[s]) + i
+            p = int(w.seq_lens[s]) - c + i
+            ref = oracle.decode(w.q[row][None], w.k_cache, w.v_cache, w.block_tables[s][None],
+                                np.array([p + 1], np.int32), w.scale, w.dtype)
+            assert float(np.abs(got[row] - ref[0]).max()) <= TOL[w.dtype], (s, i)
+
+
+def test_prefill_then_decode_continues_the_sequence(pa):
+    # a prompt prefilled in two chunks, then one decode step; each stage
+    # against the oracle on the same pool
+    rng = np.random.default_rng(2)
+    hq, hkv, d, dt = 8, 2, 128, "bf16"
+    nb, L1, L2 = 32, 70, 45
+    k_host = synth.to_bits(rng.standard_normal((nb, hkv, 16, d)).astype(np.float32), dt)
+    v_host = synth.to_bits(rng.standard_normal((nb, hkv, 16, d)).astype(np.float32), dt)
+    k_dev, v_dev = dev_bits(k_host, dt), dev_bits(v_host, dt)
+    table = rng.permutation(nb)[:8].astype(np.int32)[None]
+    tab_d = torch.from_numpy(table).cuda()
+    scale = d ** -0.5
+    done = 0
+    for c in (L1, L2):
+        kn = synth.to_bits(rng.standard_normal((c, hkv, d)).astype(np.float32), dt)
+        vn = synth.to_bits(rng.standard_normal((c, hkv, d)).astype(np.float32), dt)
+        pos = done + np.arange(c)
+        slots = (table[0][pos // 16].astype(np.int64) * 16 + pos % 16)
+        pa.reshape_and_cache(dev_bits(kn, dt), dev_bits(vn, dt), k_dev, v_dev,
+                             torch.from_numpy(slots).cuda())
+        oracle.reshape_and_cache(k_host, v_host, kn, vn, slots)
+        done += c
+        q = synth.to_bits(rng.standard_normal((c, hq, d)).astype(np.float32), dt)
+        qd = dev_bits(q, dt)
+        out = torch.empty_like(qd)
+        lens = np.array([done], np.int32)
+        qs = np.array([0, c], np.int32)
+        pa.prefill(out, qd, k_dev, v_dev, tab_d, torch.from_numpy(lens).cuda(),
+                   torch.from_numpy(qs).cuda(), c, scale)
+        ref = oracle.prefill(q, k_host, v_host, table, lens, qs, scale, dt)
+        assert max_err(out, ref) <= TOL[dt]
+    q = synth.to_bits(rng.standard_normal((1, hq, d)).astype(np.float32), dt)
+    out = torch.empty(1, hq, d, dtype=TORCH_DTYPE[dt], device="cuda")
+    pa.decode(out, dev_bits(q, dt), k_dev, v_dev, tab_d,
+              torch.tensor([done], dtype=torch.int32, device="cuda"), scale)
+    ref = oracle.decode(q, k_host, v_host, table, np.array([done], np.int32), scale, dt)
+    assert max_err(out, ref) <= TOL[dt]
+    assert pa.get_device_error() == 0
