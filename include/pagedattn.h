@@ -155,6 +155,7 @@ int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache
  *   query_start   [num_seqs + 1] int32, non-decreasing, query_start[0] = 0
  *   seq_lens      [num_seqs] int32, chunk <= len <= max_blocks_per_seq * 16
  *   max_query_len host copy of the longest chunk: it sizes the grid
+ *   scale         > 0
  *   other arguments as in pa_decode.
  * Rows are computed on the fifth-generation tensor cores (S = Q.K^T and
  * O += P.V with fp32 accumulators in tensor memory); P is rounded to dtype

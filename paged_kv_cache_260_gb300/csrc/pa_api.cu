@@ -464,7 +464,7 @@ int pa_prefill(void *out, const void *q, const void *k_cache, const void *v_cach
     if (rc != PA_OK)
         return rc;
     if (num_seqs < 0 || max_query_len < 0 || num_heads <= 0 || max_blocks_per_seq <= 0 ||
-        !isfinite(scale) || num_heads % num_kv_heads)
+        !isfinite(scale) || !(scale > 0.f) || num_heads % num_kv_heads)
         return PA_ERR_INVALID_ARG;
     const int group = num_heads / num_kv_heads;
     if (group > kPrefillRows)
@@ -477,7 +477,7 @@ int pa_prefill(void *out, const void *q, const void *k_cache, const void *v_cach
         !aligned(block_tables, 4) || !aligned(seq_lens, 4) || !aligned(query_start, 4))
         return PA_ERR_INVALID_ARG;
     const long long pool_rows = (long long)num_blocks * num_kv_heads * kBlockSize;
-    const int tokens_per_block = kPrefillRows / group;
+    const int tokens_per_block = kPrefillTiles * (kPrefillRows / group);
     const long long q_ranks = (max_query_len + tokens_per_block - 1) / tokens_per_block;
     const long long grid = q_ranks * num_seqs * num_kv_heads;
     if ((long long)max_blocks_per_seq * kBlockSize >= (1LL << 30) || pool_rows >= (1LL << 31) ||

@@ -78,6 +78,15 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     return true;
 }
 
+// 2^x on the special-function unit (PTX ex2.approx.ftz: relative error
+// about 2^-22, subnormal results flushed to zero, 2^-inf = 0).
+__device__ __forceinline__ float ex2_approx(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // L2 policy for data read exactly once (the KV tiles): evict first.
 __device__ __forceinline__ uint64_t l2_evict_first_policy()
 {

@@ -96,7 +96,8 @@ struct PrefillKernel {
 };
 
 bool prefill_kernel(int dtype, int head_dim, PrefillKernel *k);
-constexpr int kPrefillRows = 128;   // (token, head) rows of one prefill thread block
+constexpr int kPrefillRows = 128;   // (token, head) rows of one prefill query tile
+constexpr int kPrefillTiles = 2;    // query tiles of one prefill thread block
 
 bool decode_kernels_f16(int head_dim, int group, KernelSet *ks);
 bool decode_kernels_bf16(int head_dim, int group, KernelSet *ks);

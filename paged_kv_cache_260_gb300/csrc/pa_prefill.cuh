@@ -8,23 +8,33 @@
 // section "Sarathi-Serve：Chunked-Prefill技术".  K/V are reached through the
 // block table of "PagedAttention：vLLM 系统论文", section 核心思想.
 //
-// One thread block computes 128 rows = (token, q head) pairs of one sequence
-// and one kv head: 128 / G consecutive chunk tokens times the G q heads that
-// share the kv head, so every K/V tile it stages serves all of them.
-// Warp roles (192 threads):
-//   warp 0    one lane: TMA producer of K and V tiles of 64 keys (4 pool
-//             blocks x 16 rows x 128-byte boxes) into a ring of 3 slots;
-//   warp 1    TMEM owner; one lane issues the MMAs:
-//               S_j = Q . K_j^T            (M 128, N 64, K = head_dim)
-//               O  += P_j . V_j            (M 128, N head_dim, K 64)
-//             S is double-buffered in TMEM so S_{j+1} runs while the
-//             softmax warps work on S_j;
-//   warps 2-5 one thread per row (its TMEM lane): scores from TMEM, causal
-//             mask, online softmax in base 2 with a lazy rescale of O (only
-//             when the running maximum grows by more than 2^8), P written to
-//             shared memory as the A operand of the next MMA, and the final
-//             O / l written out.
-// TMEM: columns [0, 128) hold the two S buffers, [128, 128 + head_dim) O.
+// One thread block (one per SM) computes 256 rows = (token, q head) pairs of
+// one sequence and one kv head, as two 128-row query tiles ("groups") of
+// 128 / G consecutive chunk tokens times the G q heads that share the kv
+// head.  Both groups consume every K/V tile the block stages.
+//
+// What bounds the kernel is the shared-memory bandwidth the tensor core
+// reads its operands with, so the design keeps operand bytes per flop low:
+// key tiles of 128 (Q is read once per 128 keys), and P never goes through
+// shared memory -- the softmax writes it into tensor memory over the score
+// columns it has consumed, and P.V takes its A operand from there.
+// Warp roles (320 threads):
+//   warp 0    TMA producer of K and V tiles of 128 keys (8 pool blocks x 16
+//             rows x 128-byte boxes) into a ring of slots;
+//   warp 1    TMEM owner; one lane issues the MMAs of both groups:
+//               S_g,j = Q_g . K_j^T        (M 128, N 128, K = head_dim)
+//               O_g  += P_g,j . V_j        (M 128, N head_dim, K 128; A in TMEM)
+//             S_g,j+1 overwrites the columns P_g,j is read from, so it is
+//             issued once P_g,j . V_j has completed; the two groups
+//             alternate on the tensor core (one group's softmax runs while
+//             the other group's MMAs do);
+//   warps 2-5 group 0, warps 6-9 group 1: one thread per row (its TMEM
+//             lane): scores from TMEM, causal mask, online softmax in base 2
+//             with a lazy rescale of O (only when the running maximum grows
+//             by more than 2^8), P into TMEM, and the final O / l written out.
+// TMEM (512 columns): group g uses [256g, 256g + 128) for S (P packed two
+// per column in the first 64 of them) and [256g + 128, 256g + 128 + head_dim)
+// for O.
 // Every wait is bounded; a wait that gives up records PA_DEVERR_TIMEOUT and
 // the block drains its copies and MMAs before it frees TMEM and exits.
 #pragma once
@@ -39,57 +49,66 @@ namespace pa {
 
 template <int D>
 struct PrefillShape {
-    static constexpr int BM = kPrefillRows;                 // rows per block
-    static constexpr int BN = 64;                           // keys per tile
-    static constexpr int NSLOT = 3;                         // K/V ring
+    static constexpr int BM = kPrefillRows;                 // rows per group (tile)
+    static constexpr int NG = kPrefillTiles;                // groups per block
+    static constexpr int BN = 128;                          // keys per tile
+    static constexpr int NB = BN / kBlockSize;              // pool blocks per tile
     static constexpr int HALVES = D / 64;                   // 128-byte column boxes
     static constexpr int BOX = 2048;                        // 16 rows x 128 B
-    static constexpr int Q_BYTES = BM * D * 2;              // [half][128 rows][128 B]
-    static constexpr int SLOT_BYTES = BN * D * 2;           // [half][4 blocks][16 rows][128 B]
-    static constexpr int P_BYTES = BM * BN * 2;             // [128 rows][128 B]
-    static constexpr int OFF_SLOT = Q_BYTES;
-    static constexpr int OFF_P = OFF_SLOT + NSLOT * SLOT_BYTES;
-    static constexpr int OFF_BAR = OFF_P + P_BYTES;
-    static constexpr int NBAR = 11;                         // full[3] empty[3] s[2] p o drain
-    static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16 + 1024;   // + alignment slack
-    static constexpr int THREADS = 192;
-    static constexpr uint32_t TMEM_COLS = 256;
-    static constexpr uint32_t COL_S = 0;
+    static constexpr int Q_BYTES = BM * D * 2;              // per group: [half][128 rows][128 B]
+    static constexpr int SLOT_BYTES = BN * D * 2;           // [half][8 blocks][16 rows][128 B]
+    static constexpr int NSLOT = (227 * 1024 - 1024 - NG * Q_BYTES) / SLOT_BYTES;   // K/V ring
+    static constexpr int OFF_SLOT = NG * Q_BYTES;
+    static constexpr int DATA = OFF_SLOT + NSLOT * SLOT_BYTES;   // 1024-aligned operand region
+    // full[NSLOT] empty[NSLOT] s[2] p[2] o[2] drain, then TMEM base and abort flag
+    static constexpr int NBAR = 2 * NSLOT + 3 * NG + 1;
+    static constexpr int BAR_BYTES = NBAR * 8 + 8;
+    // The operand region is aligned up to 1024 bytes inside the dynamic
+    // allocation; the barriers sit in whichever end of the 1024-byte slack
+    // has room.
+    static constexpr int SMEM = DATA + 1024;
+    static constexpr int THREADS = 64 + NG * 128;
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr uint32_t GROUP_COLS = 256;
+    static constexpr uint32_t COL_S = 0;                    // S, then P over its first half
     static constexpr uint32_t COL_O = 128;
     static_assert(D == 64 || D == 128, "head_dim");
-    static_assert(OFF_P % 1024 == 0 && OFF_SLOT % 1024 == 0, "swizzle atoms");
+    static_assert(NSLOT >= 4, "at least two tiles of K/V in flight");
+    static_assert(OFF_SLOT % 1024 == 0 && SLOT_BYTES % 1024 == 0, "swizzle atoms");
+    static_assert(BAR_BYTES <= 512, "barriers fit either end of the slack");
+    static_assert(SMEM <= 227 * 1024, "one block per SM");
 };
 
 template <typename T, int D>
-__global__ void __launch_bounds__(192, 2)
+__global__ void __launch_bounds__(PrefillShape<D>::THREADS)
 prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk,
                   const __grid_constant__ CUtensorMap tmv)
 {
     using Sh = PrefillShape<D>;
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
     constexpr uint32_t FULL = 0xffffffffu;
+    constexpr int NS = Sh::NSLOT;
 
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
     unsigned char *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
     const uint32_t sbase = smem_addr(smem);
-    const uint32_t q_addr = sbase;
     const uint32_t slot_addr = sbase + Sh::OFF_SLOT;
-    const uint32_t p_addr = sbase + Sh::OFF_P;
-    const uint32_t bar_addr = sbase + Sh::OFF_BAR;
-    // barrier addresses
+    unsigned char *bars = (smem - smem_raw) >= Sh::BAR_BYTES ? smem_raw : smem + Sh::DATA;
+    const uint32_t bar_addr = smem_addr(bars);
     auto full_bar = [&](int s) { return bar_addr + 8u * s; };
-    auto empty_bar = [&](int s) { return bar_addr + 8u * (3 + s); };
-    auto s_bar = [&](int b) { return bar_addr + 8u * (6 + b); };
-    const uint32_t p_bar = bar_addr + 8u * 8;
-    const uint32_t o_bar = bar_addr + 8u * 9;
-    const uint32_t drain_bar = bar_addr + 8u * 10;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Sh::OFF_BAR + Sh::NBAR * 8);
+    auto empty_bar = [&](int s) { return bar_addr + 8u * (NS + s); };
+    auto s_bar = [&](int g) { return bar_addr + 8u * (2 * NS + g); };
+    auto p_bar = [&](int g) { return bar_addr + 8u * (2 * NS + Sh::NG + g); };
+    auto o_bar = [&](int g) { return bar_addr + 8u * (2 * NS + 2 * Sh::NG + g); };
+    const uint32_t drain_bar = bar_addr + 8u * (2 * NS + 3 * Sh::NG);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + Sh::NBAR * 8);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int Hkv = p.num_kv_heads, Hq = p.num_heads, G = Hq / Hkv;
-    const int TPC = Sh::BM / G;                   // chunk tokens per block
+    const int TPG = Sh::BM / G;                   // chunk tokens per group
+    const int TPB = Sh::NG * TPG;                 // chunk tokens per block
     const int per_rank = p.num_seqs * Hkv;
     const int rank = blockIdx.x / per_rank;
     const int s = (blockIdx.x % per_rank) / Hkv;
@@ -109,27 +128,28 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
             record_error(p.err, PA_DEVERR_QUERY_RANGE);
         return;
     }
-    const int nq = (c + TPC - 1) / TPC;
+    const int nq = (c + TPB - 1) / TPB;
     if (nq > p.q_ranks && rank == 0 && h == 0 && tid == 0)
         record_error(p.err, PA_DEVERR_QUERY_RANGE);   // max_query_len too small
     if (rank >= nq)
         return;
     const int tile = nq - 1 - rank;               // rank 0 = the last (longest) tile
-    const int t0 = tile * TPC;
-    const int t_end = min(t0 + TPC, c);
+    const int t0 = tile * TPB;
+    const int t_end = min(t0 + TPB, c);
     const int p_last = L - c + t_end - 1;         // position of the block's last row
-    const int nt = p_last / Sh::BN + 1;           // key tiles
+    const int nt = p_last / Sh::BN + 1;           // key tiles (both groups)
     const int nblk = (L + kBlockSize - 1) / kBlockSize;
 
     if (tid == 0) {
-        for (int i = 0; i < Sh::NSLOT; ++i) {
+        for (int i = 0; i < NS; ++i) {
             mbar_init(full_bar(i), 1);
             mbar_init(empty_bar(i), 1);
         }
-        mbar_init(s_bar(0), 1);
-        mbar_init(s_bar(1), 1);
-        mbar_init(p_bar, 128);
-        mbar_init(o_bar, 1);
+        for (int g = 0; g < Sh::NG; ++g) {
+            mbar_init(s_bar(g), 1);
+            mbar_init(p_bar(g), 128);
+            mbar_init(o_bar(g), 1);
+        }
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
         mbar_init_fence();
@@ -139,22 +159,24 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
         tc::tmem_relinquish();
     }
 
-    // ---- Q tile -> shared memory, K-major with the 128-byte swizzle --------
-    // row r = (token t0 + r / G, q head h*G + r % G); rows past the chunk and
-    // the rows 128 - TPC*G that do not fill a token are zero
+    // ---- Q tiles -> shared memory, K-major with the 128-byte swizzle -------
+    // row rr of group g = (token t0 + g*TPG + rr / G, q head h*G + rr % G);
+    // rows past the chunk and the rows 128 - TPG*G that do not fill a token
+    // are zero
     {
         constexpr int CPR = D / 8;                // 16-byte chunks per row
         const T *qg = reinterpret_cast<const T *>(p.q);
-        for (int idx = tid; idx < Sh::BM * CPR; idx += Sh::THREADS) {
+        for (int idx = tid; idx < Sh::NG * Sh::BM * CPR; idx += Sh::THREADS) {
             const int r = idx / CPR, ch = idx % CPR;
-            const int tok = r / G, g = r % G;
+            const int g = r / Sh::BM, rr = r % Sh::BM;
+            const int tok = g * TPG + rr / G, hg = rr % G;
             uint4 v = make_uint4(0, 0, 0, 0);
-            if (r < TPC * G && t0 + tok < c)
+            if (rr < TPG * G && t0 + tok < c)
                 v = __ldg(reinterpret_cast<const uint4 *>(
-                    qg + ((size_t)(qs + t0 + tok) * Hq + h * G + g) * D + ch * 8));
+                    qg + ((size_t)(qs + t0 + tok) * Hq + h * G + hg) * D + ch * 8));
             const int hf = ch >> 3, c8 = ch & 7;
-            *reinterpret_cast<uint4 *>(smem + hf * (Sh::BM * 128) + r * 128 +
-                                       ((c8 ^ (r & 7)) << 4)) = v;
+            *reinterpret_cast<uint4 *>(smem + g * Sh::Q_BYTES + hf * (Sh::BM * 128) + rr * 128 +
+                                       ((c8 ^ (rr & 7)) << 4)) = v;
         }
     }
     fence_proxy_async_shared();
@@ -170,103 +192,128 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
 
     if (warp == 0) {
         // ---------------- producer: K_j, V_j into the slot ring ----------------
-        if (lane == 0) {
-            const int32_t *table = p.block_tables + (size_t)s * p.max_blocks;
-            int last[Sh::NSLOT] = {-1, -1, -1};
-            for (int i = 0; i < 2 * nt; ++i) {
-                if (*abort_flag)
-                    break;
-                const int j = i >> 1, sl = i % Sh::NSLOT;
-                if (i >= Sh::NSLOT && !mbar_wait_bounded(empty_bar(sl), ((i / Sh::NSLOT) - 1) & 1)) {
+        // The whole warp works: lane l holds the pool row of block NB*win + l
+        // of a window of WT tiles (the next window's entries are already in
+        // flight), lane 0 waits for the slot and arms its barrier, and lanes
+        // (hf, b) issue the tile's boxes in parallel.
+        constexpr int NB = Sh::NB, WT = 32 / NB;
+        const int32_t *table = p.block_tables + (size_t)s * p.max_blocks;
+        auto fetch = [&](int w0) {
+            const int lb = NB * w0 + lane;
+            return lb < nblk ? __ldg(table + lb) : 0;
+        };
+        auto to_row = [&](int w0, int phys) {
+            if (NB * w0 + lane >= nblk)
+                return -1;                  // blocks past the sequence are not loaded
+            if ((unsigned)phys >= (unsigned)p.num_blocks) {
+                record_error(p.err, PA_DEVERR_TABLE_RANGE);
+                phys = 0;
+            }
+            return (phys * Hkv + h) * kBlockSize;
+        };
+        int win = 0;
+        int cur = to_row(0, fetch(0));
+        int nxt = fetch(WT);
+        int last = -1;                          // lane sl < NS: last item put in slot sl
+        for (int i = 0; i < 2 * nt; ++i) {
+            const int j = i >> 1, sl = i % NS;
+            if (j == win + WT) {
+                win += WT;
+                cur = to_row(win, nxt);
+                nxt = fetch(win + WT);
+            }
+            bool ready = true;
+            if (lane == 0)
+                ready = !*abort_flag &&
+                        (i < NS || mbar_wait_bounded(empty_bar(sl), ((i / NS) - 1) & 1));
+            if (!__shfl_sync(FULL, ready, 0)) {
+                if (lane == 0 && !*abort_flag)
                     give_up();
-                    break;
-                }
-                int rows[4];
-                int nv = 0;
-#pragma unroll
-                for (int b = 0; b < 4; ++b) {
-                    const int lb = 4 * j + b;
-                    rows[b] = -1;
-                    if (lb < nblk) {        // blocks past the sequence are not loaded
-                        int phys = __ldg(table + lb);
-                        if ((unsigned)phys >= (unsigned)p.num_blocks) {
-                            record_error(p.err, PA_DEVERR_TABLE_RANGE);
-                            phys = 0;
-                        }
-                        rows[b] = (phys * Hkv + h) * kBlockSize;
-                        ++nv;
-                    }
-                }
+                break;
+            }
+            const int nv = min(NB, nblk - NB * j);
+            if (lane == 0)
                 mbar_arrive_expect_tx(full_bar(sl), (uint32_t)(nv * Sh::HALVES * Sh::BOX));
+            const int b = lane % NB, hf = lane / NB;
+            const int row = __shfl_sync(FULL, cur, NB * (j - win) + b);
+            __syncwarp();
+            if (hf < Sh::HALVES && row >= 0) {
                 const void *tm = (i & 1) ? static_cast<const void *>(&tmv)
                                          : static_cast<const void *>(&tmk);
-                const uint32_t dst = slot_addr + sl * Sh::SLOT_BYTES;
-#pragma unroll
-                for (int b = 0; b < 4; ++b)
-                    if (rows[b] >= 0)
-#pragma unroll
-                        for (int hf = 0; hf < Sh::HALVES; ++hf)
-                            tma_load_2d(dst + (hf * 4 + b) * Sh::BOX, tm, 64 * hf, rows[b],
-                                        full_bar(sl));
-                last[sl] = i;
+                tma_load_2d(slot_addr + sl * Sh::SLOT_BYTES + (hf * NB + b) * Sh::BOX, tm,
+                            64 * hf, row, full_bar(sl));
             }
-            // every issued copy lands before the block may exit
-            for (int sl = 0; sl < Sh::NSLOT; ++sl)
-                if (last[sl] >= 0 &&
-                    !mbar_wait_bounded(full_bar(sl), (last[sl] / Sh::NSLOT) & 1))
-                    give_up();
+            if (lane == sl)
+                last = i;
         }
+        // every issued copy lands before the block may exit
+        if (lane < NS && last >= 0 && !mbar_wait_bounded(full_bar(lane), (last / NS) & 1))
+            give_up();
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
             constexpr uint32_t idS = tc::idesc_f16(kBf16, Sh::BM, Sh::BN, false, false);
             constexpr uint32_t idO = tc::idesc_f16(kBf16, Sh::BM, D, false, true);
-            auto issue_s = [&](int j) -> bool {
-                const int i = 2 * j, sl = i % Sh::NSLOT;
-                if (!mbar_wait_bounded(full_bar(sl), (i / Sh::NSLOT) & 1))
+            // S_g,j = Q_g . K_j^T; the K slot is released after the last group
+            auto issue_s = [&](int g, int j) -> bool {
+                const int i = 2 * j, sl = i % NS;
+                if (!mbar_wait_bounded(full_bar(sl), (i / NS) & 1))
                     return false;
                 tc::fence_after_sync();
+                const uint32_t qa = sbase + g * Sh::Q_BYTES;
                 const uint32_t kb = slot_addr + sl * Sh::SLOT_BYTES;
-                const uint32_t d = tmem + Sh::COL_S + (uint32_t)(j & 1) * Sh::BN;
+                const uint32_t d = tmem + g * Sh::GROUP_COLS + Sh::COL_S;
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
                     const uint32_t hf = k >> 2, w = (k & 3) * 32;
-                    const uint64_t a = tc::sdesc_sw128(q_addr + hf * (Sh::BM * 128) + w, 16, 1024);
-                    const uint64_t b = tc::sdesc_sw128(kb + hf * (4 * Sh::BOX) + w, 16, 1024);
+                    const uint64_t a = tc::sdesc_sw128(qa + hf * (Sh::BM * 128) + w, 16, 1024);
+                    const uint64_t b = tc::sdesc_sw128(kb + hf * (Sh::NB * Sh::BOX) + w, 16, 1024);
                     tc::mma_ss(d, a, b, idS, k > 0);
                 }
-                tc::commit(s_bar(j & 1));
-                tc::commit(empty_bar(sl));
+                tc::commit(s_bar(g));
+                if (g == Sh::NG - 1)
+                    tc::commit(empty_bar(sl));
                 return true;
             };
-            bool ok = issue_s(0);
+            // O_g += P_g,j . V_j once the group's softmax has written P
+            auto issue_pv = [&](int g, int j) -> bool {
+                const int i = 2 * j + 1, sl = i % NS;
+                if (!mbar_wait_bounded(p_bar(g), j & 1) ||
+                    !mbar_wait_bounded(full_bar(sl), (i / NS) & 1))
+                    return false;
+                tc::fence_after_sync();
+                const uint32_t vb = slot_addr + sl * Sh::SLOT_BYTES;
+                const uint32_t gc = tmem + g * Sh::GROUP_COLS;
+#pragma unroll
+                for (int kk = 0; kk < Sh::BN / 16; ++kk) {
+                    // A = P: keys 16kk.. = 8 packed columns; B = V block kk
+                    // (MN-major: 64-channel groups NB boxes apart, 8-key
+                    // groups 1 KB apart)
+                    const uint64_t b = tc::sdesc_sw128(vb + kk * Sh::BOX, Sh::NB * Sh::BOX, 1024);
+                    tc::mma_ts(gc + Sh::COL_O, gc + Sh::COL_S + 8 * kk, b, idO,
+                               (j > 0 || kk > 0) ? 1u : 0u);
+                }
+                tc::commit(o_bar(g));
+                if (g == Sh::NG - 1)
+                    tc::commit(empty_bar(sl));
+                return true;
+            };
+            bool ok = true;
+            for (int g = 0; ok && g < Sh::NG; ++g)
+                ok = issue_s(g, 0);
             for (int j = 0; ok && j < nt; ++j) {
                 if (*abort_flag) {
                     ok = false;
                     break;
                 }
-                if (j + 1 < nt && !issue_s(j + 1)) {
-                    ok = false;
-                    break;
+                for (int g = 0; ok && g < Sh::NG; ++g) {
+                    ok = issue_pv(g, j);
+                    // S_g,j+1 reuses the TMEM columns P_g,j . V_j reads
+                    if (ok && j + 1 < nt) {
+                        ok = mbar_wait_bounded(o_bar(g), j & 1);
+                        ok = ok && issue_s(g, j + 1);
+                    }
                 }
-                const int i = 2 * j + 1, sl = i % Sh::NSLOT;
-                if (!mbar_wait_bounded(p_bar, j & 1) ||
-                    !mbar_wait_bounded(full_bar(sl), (i / Sh::NSLOT) & 1)) {
-                    ok = false;
-                    break;
-                }
-                tc::fence_after_sync();
-                const uint32_t vb = slot_addr + sl * Sh::SLOT_BYTES;
-#pragma unroll
-                for (int kk = 0; kk < Sh::BN / 16; ++kk) {
-                    // A = P (K-major, keys 16kk..), B = V block kk (MN-major:
-                    // 64-channel groups 4 boxes apart, 8-key groups 1 KB apart)
-                    const uint64_t a = tc::sdesc_sw128(p_addr + kk * 32, 16, 1024);
-                    const uint64_t b = tc::sdesc_sw128(vb + kk * Sh::BOX, 4 * Sh::BOX, 1024);
-                    tc::mma_ss(tmem + Sh::COL_O, a, b, idO, (j > 0 || kk > 0) ? 1u : 0u);
-                }
-                tc::commit(o_bar);
-                tc::commit(empty_bar(sl));
             }
             if (!ok)
                 give_up();
@@ -276,13 +323,15 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
                 give_up();
         }
     } else {
-        // ---------------- softmax: one thread per row ----------------
+        // ---------------- softmax: one thread per row of its group ----------
+        const int grp = (warp - 2) >> 2;
         const int q4 = warp & 3;                   // TMEM lane quarter of this warp
-        const int r = q4 * 32 + lane;
-        const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-        const int tok = r / G, g = r % G;
-        const bool row_valid = r < TPC * G && t0 + tok < c;
+        const int rr = q4 * 32 + lane;             // row within the group
+        const uint32_t tg = tmem + ((uint32_t)(q4 * 32) << 16) + grp * Sh::GROUP_COLS;
+        const int tok = grp * TPG + rr / G, hg = rr % G;
+        const bool row_valid = rr < TPG * G && t0 + tok < c;
         const int pos = row_valid ? L - c + t0 + tok : L - 1;
+        const float sl2 = p.scale_log2;
         float m = 0.f, l = 0.f;
         bool ok = true;
         for (int j = 0; j < nt; ++j) {
@@ -290,115 +339,117 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
                 ok = false;
                 break;
             }
-            if (!__all_sync(FULL, mbar_wait_bounded(s_bar(j & 1), (j >> 1) & 1))) {
+            if (!__all_sync(FULL, mbar_wait_bounded(s_bar(grp), j & 1))) {
                 ok = false;
                 break;
             }
             tc::fence_after_sync();
-            __syncwarp();                        // tcgen05.ld is warp-collective
-            float x[Sh::BN];
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t v[32];
-                tc::tmem_ld32(tmem + lane_off + Sh::COL_S + (uint32_t)(j & 1) * Sh::BN + 32 * half, v);
-#pragma unroll
-                for (int e = 0; e < 32; ++e)
-                    x[32 * half + e] = __uint_as_float(v[e]) * p.scale_log2;
-            }
             const int k0 = j * Sh::BN;
-            if (k0 + Sh::BN - 1 > pos) {
+            const int vis = pos - k0;              // keys [0, vis] of the tile are visible
+            // pass 1: row maximum of the visible scores, as a tree
+            float mt = -INFINITY;
 #pragma unroll
-                for (int e = 0; e < Sh::BN; ++e)
-                    if (k0 + e > pos)
-                        x[e] = -INFINITY;   // causal mask (and keys >= L)
-            }
-            float mt = x[0];
+            for (int hb = 0; hb < 2; ++hb) {
+                uint32_t v[64];
+                __syncwarp();                    // tcgen05.ld is warp-collective
+                tc::tmem_ld64(tg + Sh::COL_S + 64 * hb, v);
+                float mx[8];
 #pragma unroll
-            for (int e = 1; e < Sh::BN; ++e)
-                mt = fmaxf(mt, x[e]);
-            // O and P may be touched only after the previous P.V has completed
-            if (j > 0) {
-                if (!__all_sync(FULL, mbar_wait_bounded(o_bar, (j - 1) & 1))) {
-                    ok = false;
-                    break;
+                for (int e = 0; e < 8; ++e)
+                    mx[e] = -INFINITY;
+#pragma unroll
+                for (int e = 0; e < 64; ++e) {
+                    const float x = 64 * hb + e <= vis ? __uint_as_float(v[e]) : -INFINITY;
+                    mx[e & 7] = fmaxf(mx[e & 7], x);
                 }
-                tc::fence_after_sync();
+                mt = fmaxf(mt, fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                     fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))));
             }
+            mt *= sl2;                           // scale > 0: max commutes with it
+            // running maximum, raised lazily: only when the tile's maximum
+            // exceeds it by more than 8 (P stays below 2^8 otherwise)
             bool grow = false;
-            if (j == 0)
-                m = mt;                  // finite: key 0 is visible to every row
-            else
-                grow = mt > m + 8.f;
-            __syncwarp();
-            if (__any_sync(FULL, grow)) {
-                const float mn = grow ? mt : m;
-                const float alpha = exp2f(m - mn);
-                m = mn;
-                l *= alpha;
-#pragma unroll
-                for (int cc = 0; cc < D; cc += 32) {
-                    uint32_t v[32];
-                    tc::tmem_ld32(tmem + lane_off + Sh::COL_O + cc, v);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-                    tc::tmem_st32(tmem + lane_off + Sh::COL_O + cc, v);
-                }
+            float alpha = 1.f;
+            if (j == 0) {
+                m = mt;                          // finite: key 0 is visible to every row
+            } else if (mt > m + 8.f) {
+                grow = true;
+                alpha = ex2_approx(m - mt);
+                m = mt;
             }
+            // pass 2: P = 2^(scale*s - m) packed to the operand type, written
+            // into TMEM over score columns already read (keys 0-63 -> columns
+            // 0-31, keys 64-127 -> 32-63)
+            float sum[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int hb = 0; hb < 2; ++hb) {
+                uint32_t v[64];
+                __syncwarp();
+                tc::tmem_ld64(tg + Sh::COL_S + 64 * hb, v);
+                uint32_t pw[32];
+#pragma unroll
+                for (int e = 0; e < 64; e += 2) {
+                    const float x0 = 64 * hb + e <= vis ? __uint_as_float(v[e]) : -INFINITY;
+                    const float x1 = 64 * hb + e + 1 <= vis ? __uint_as_float(v[e + 1]) : -INFINITY;
+                    const float p0 = ex2_approx(fmaf(x0, sl2, -m));
+                    const float p1 = ex2_approx(fmaf(x1, sl2, -m));
+                    sum[(e >> 1) & 3] += p0 + p1;
+                    pw[e / 2] = Mma<T>::pack(p0, p1);
+                }
+                __syncwarp();
+                tc::tmem_st32(tg + Sh::COL_S + 32 * hb, pw);
+            }
+            l = fmaf(l, alpha, (sum[0] + sum[1]) + (sum[2] + sum[3]));
             // the tile that reaches the end of the sequence: value rows of
-            // keys >= L are zeroed (0 * NaN is NaN in the MMA)
-            if (k0 + Sh::BN > L) {
-                const int i = 2 * j + 1, sl = i % Sh::NSLOT;
-                if (!__all_sync(FULL, mbar_wait_bounded(full_bar(sl), (i / Sh::NSLOT) & 1))) {
+            // keys >= L are zeroed (0 * NaN is NaN in the MMA).  Group 0 does
+            // it; group 1's P.V is issued after group 0's barrier, which
+            // orders these stores before it.
+            if (grp == 0 && k0 + Sh::BN > L) {
+                const int i = 2 * j + 1, sl = i % NS;
+                if (!__all_sync(FULL, mbar_wait_bounded(full_bar(sl), (i / NS) & 1))) {
                     ok = false;
                     break;
                 }
-                // 128 threads of 4 warps zero the rows; their own barrier below
-                // (p_bar) orders the stores before the MMA
                 const int first = L - k0;
                 const int n16 = (Sh::BN - first) * Sh::HALVES * 8;
                 unsigned char *vb = smem + Sh::OFF_SLOT + sl * Sh::SLOT_BYTES;
-                for (int idx = r; idx < n16; idx += 128) {
+                for (int idx = rr; idx < n16; idx += 128) {
                     const int row = first + idx / (Sh::HALVES * 8);
                     const int rem = idx % (Sh::HALVES * 8);
-                    *reinterpret_cast<uint4 *>(vb + ((rem >> 3) * 4 + (row >> 4)) * Sh::BOX +
+                    *reinterpret_cast<uint4 *>(vb + ((rem >> 3) * Sh::NB + (row >> 4)) * Sh::BOX +
                                                (row & 15) * 128 + (rem & 7) * 16) =
                         make_uint4(0, 0, 0, 0);
                 }
+                fence_proxy_async_shared();
             }
-            // P = exp2(x - m) as the A operand: row r, 8-key chunks swizzled
-            float rs = 0.f;
-            unsigned char *prow = smem + Sh::OFF_P + r * 128;
+            // O rescale: P_g,j-1 . V_j-1 completed before S_g,j was issued
+            __syncwarp();
+            if (__any_sync(FULL, grow)) {
 #pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8) {
-                uint32_t w[4];
+                for (int cc = 0; cc < D; cc += 32) {
+                    uint32_t v[32];
+                    tc::tmem_ld32(tg + Sh::COL_O + cc, v);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float p0 = exp2f(x[8 * c8 + 2 * e] - m);
-                    const float p1 = exp2f(x[8 * c8 + 2 * e + 1] - m);
-                    rs += p0 + p1;
-                    w[e] = Mma<T>::pack(p0, p1);
+                    for (int e = 0; e < 32; ++e)
+                        v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+                    tc::tmem_st32(tg + Sh::COL_O + cc, v);
                 }
-                *reinterpret_cast<uint4 *>(prow + ((c8 ^ (r & 7)) << 4)) =
-                    make_uint4(w[0], w[1], w[2], w[3]);
             }
-            l += rs;
-            fence_proxy_async_shared();
             tc::fence_before_sync();
-            mbar_arrive(p_bar);
+            mbar_arrive(p_bar(grp));
         }
-        if (ok && !__all_sync(FULL, mbar_wait_bounded(o_bar, (nt - 1) & 1)))
+        if (ok && !__all_sync(FULL, mbar_wait_bounded(o_bar(grp), (nt - 1) & 1)))
             ok = false;
         if (ok) {
             tc::fence_after_sync();
             __syncwarp();
             const float inv = 1.f / l;
             T *orow = reinterpret_cast<T *>(p.out) +
-                      ((size_t)(qs + t0 + tok) * Hq + h * G + g) * D;
+                      ((size_t)(qs + t0 + tok) * Hq + h * G + hg) * D;
 #pragma unroll
             for (int cc = 0; cc < D; cc += 32) {
                 uint32_t v[32];
-                tc::tmem_ld32(tmem + lane_off + Sh::COL_O + cc, v);
+                tc::tmem_ld32(tg + Sh::COL_O + cc, v);
                 if (row_valid) {
 #pragma unroll
                     for (int e = 0; e < 32; e += 8) {

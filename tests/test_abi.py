@@ -129,6 +129,7 @@ def test_prefill_rejects_bad_scalars(lib):
     assert call(hq=7) == 1
     assert call(hq=258, hkv=1) == 2                  # group over 128 rows
     assert call(scale=float("inf")) == 1
+    assert call(scale=-0.1) == 1 and call(scale=0.0) == 1
     assert call(max_q=-1) == 1
     assert call(num_seqs=0) == 0 and call(max_q=0) == 0
     assert call() == 1                               # null pointers
