@@ -21,7 +21,8 @@
 // Warp roles (320 threads):
 //   warp 0    TMA producer of K and V tiles of 128 keys (8 pool blocks x 16
 //             rows x 128-byte boxes) into a ring of slots;
-//   warp 1    TMEM owner; one lane issues the MMAs of both groups:
+//   warp 1    TMEM owner; issues the MMAs of both groups (the warp runs the
+//             loop, one elected lane issues):
 //               S_g,j = Q_g . K_j^T        (M 128, N 128, K = head_dim)
 //               O_g  += P_g,j . V_j        (M 128, N head_dim, K 128; A in TMEM)
 //             S_g,j+1 overwrites the columns P_g,j is read from, so it is
@@ -250,78 +251,84 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
         if (lane < NS && last >= 0 && !mbar_wait_bounded(full_bar(lane), (last / NS) & 1))
             give_up();
     } else if (warp == 1) {
-        // ---------------- MMA issuer ----------------
-        if (lane == 0) {
-            constexpr uint32_t idS = tc::idesc_f16(kBf16, Sh::BM, Sh::BN, false, false);
-            constexpr uint32_t idO = tc::idesc_f16(kBf16, Sh::BM, D, false, true);
-            // S_g,j = Q_g . K_j^T; the K slot is released after the last group
-            auto issue_s = [&](int g, int j) -> bool {
-                const int i = 2 * j, sl = i % NS;
-                if (!mbar_wait_bounded(full_bar(sl), (i / NS) & 1))
-                    return false;
-                tc::fence_after_sync();
-                const uint32_t qa = sbase + g * Sh::Q_BYTES;
-                const uint32_t kb = slot_addr + sl * Sh::SLOT_BYTES;
-                const uint32_t d = tmem + g * Sh::GROUP_COLS + Sh::COL_S;
+        // ---------------- MMA issuer (the whole warp, one elected lane issues) ------
+        // The warp stays converged and every operand is warp-uniform, so the
+        // descriptors live in uniform registers and the MMAs issue back to
+        // back (a single-lane loop issues them at a fraction of the rate).
+        constexpr uint32_t idS = tc::idesc_f16(kBf16, Sh::BM, Sh::BN, false, false);
+        constexpr uint32_t idO = tc::idesc_f16(kBf16, Sh::BM, D, false, true);
+        // descriptors of slot 0 / group 0; offsets are added in 16-byte units
+        const uint64_t q_desc = tc::sdesc_sw128(sbase, 16, 1024);
+        const uint64_t k_desc = tc::sdesc_sw128(slot_addr, 16, 1024);
+        const uint64_t v_desc = tc::sdesc_sw128(slot_addr, Sh::NB * Sh::BOX, 1024);
+        auto wait_all = [&](uint32_t bar, uint32_t parity) {
+            return __all_sync(FULL, mbar_wait_bounded(bar, parity));
+        };
+        // S_g,j = Q_g . K_j^T; the K slot is released after the last group
+        auto issue_s = [&](int g, int j) -> bool {
+            const int i = 2 * j, sl = i % NS;
+            if (!wait_all(full_bar(sl), (i / NS) & 1))
+                return false;
+            tc::fence_after_sync();
+            const uint64_t qd = q_desc + (uint64_t)((g * Sh::Q_BYTES) >> 4);
+            const uint64_t kd = k_desc + (uint64_t)((sl * Sh::SLOT_BYTES) >> 4);
+            const uint32_t d = tmem + g * Sh::GROUP_COLS + Sh::COL_S;
 #pragma unroll
-                for (int k = 0; k < D / 16; ++k) {
-                    const uint32_t hf = k >> 2, w = (k & 3) * 32;
-                    const uint64_t a = tc::sdesc_sw128(qa + hf * (Sh::BM * 128) + w, 16, 1024);
-                    const uint64_t b = tc::sdesc_sw128(kb + hf * (Sh::NB * Sh::BOX) + w, 16, 1024);
-                    tc::mma_ss(d, a, b, idS, k > 0);
-                }
-                tc::commit(s_bar(g));
-                if (g == Sh::NG - 1)
-                    tc::commit(empty_bar(sl));
-                return true;
-            };
-            // O_g += P_g,j . V_j once the group's softmax has written P
-            auto issue_pv = [&](int g, int j) -> bool {
-                const int i = 2 * j + 1, sl = i % NS;
-                if (!mbar_wait_bounded(p_bar(g), j & 1) ||
-                    !mbar_wait_bounded(full_bar(sl), (i / NS) & 1))
-                    return false;
-                tc::fence_after_sync();
-                const uint32_t vb = slot_addr + sl * Sh::SLOT_BYTES;
-                const uint32_t gc = tmem + g * Sh::GROUP_COLS;
-#pragma unroll
-                for (int kk = 0; kk < Sh::BN / 16; ++kk) {
-                    // A = P: keys 16kk.. = 8 packed columns; B = V block kk
-                    // (MN-major: 64-channel groups NB boxes apart, 8-key
-                    // groups 1 KB apart)
-                    const uint64_t b = tc::sdesc_sw128(vb + kk * Sh::BOX, Sh::NB * Sh::BOX, 1024);
-                    tc::mma_ts(gc + Sh::COL_O, gc + Sh::COL_S + 8 * kk, b, idO,
-                               (j > 0 || kk > 0) ? 1u : 0u);
-                }
-                tc::commit(o_bar(g));
-                if (g == Sh::NG - 1)
-                    tc::commit(empty_bar(sl));
-                return true;
-            };
-            bool ok = true;
-            for (int g = 0; ok && g < Sh::NG; ++g)
-                ok = issue_s(g, 0);
-            for (int j = 0; ok && j < nt; ++j) {
-                if (*abort_flag) {
-                    ok = false;
-                    break;
-                }
-                for (int g = 0; ok && g < Sh::NG; ++g) {
-                    ok = issue_pv(g, j);
-                    // S_g,j+1 reuses the TMEM columns P_g,j . V_j reads
-                    if (ok && j + 1 < nt) {
-                        ok = mbar_wait_bounded(o_bar(g), j & 1);
-                        ok = ok && issue_s(g, j + 1);
-                    }
-                }
+            for (int k = 0; k < D / 16; ++k) {
+                // K step k: 32 bytes along the 128-byte row; the next 64
+                // channels are 16 KB further (Q: 128 rows, K: 8 boxes)
+                const uint64_t ko = (uint64_t)(((k & 3) * 32 + (k >> 2) * (Sh::BM * 128)) >> 4);
+                tc::mma_ss_warp(d, qd + ko, kd + ko, idS, k > 0);
             }
-            if (!ok)
-                give_up();
-            // no MMA may still run when TMEM is freed
-            tc::commit(drain_bar);
-            if (!mbar_wait_bounded(drain_bar, 0))
-                give_up();
+            tc::commit_warp(s_bar(g));
+            if (g == Sh::NG - 1)
+                tc::commit_warp(empty_bar(sl));
+            return true;
+        };
+        static_assert(Sh::BM * 128 == Sh::NB * Sh::BOX, "Q and K halves 16 KB apart");
+        // O_g += P_g,j . V_j once the group's softmax has written P
+        auto issue_pv = [&](int g, int j) -> bool {
+            const int i = 2 * j + 1, sl = i % NS;
+            if (!wait_all(p_bar(g), j & 1) || !wait_all(full_bar(sl), (i / NS) & 1))
+                return false;
+            tc::fence_after_sync();
+            const uint64_t vd = v_desc + (uint64_t)((sl * Sh::SLOT_BYTES) >> 4);
+            const uint32_t gc = tmem + g * Sh::GROUP_COLS;
+#pragma unroll
+            for (int kk = 0; kk < Sh::BN / 16; ++kk) {
+                // A = P: keys 16kk.. = 8 packed columns; B = V block kk
+                // (MN-major: 64-channel groups NB boxes apart, 8-key groups
+                // 1 KB apart)
+                tc::mma_ts_warp(gc + Sh::COL_O, gc + Sh::COL_S + 8 * kk,
+                                vd + (uint64_t)((kk * Sh::BOX) >> 4), idO,
+                                (j > 0 || kk > 0) ? 1u : 0u);
+            }
+            tc::commit_warp(o_bar(g));
+            if (g == Sh::NG - 1)
+                tc::commit_warp(empty_bar(sl));
+            return true;
+        };
+        bool ok = true;
+        for (int g = 0; ok && g < Sh::NG; ++g)
+            ok = issue_s(g, 0);
+        for (int j = 0; ok && j < nt; ++j) {
+            if (__any_sync(FULL, *abort_flag != 0)) {
+                ok = false;
+                break;
+            }
+            for (int g = 0; ok && g < Sh::NG; ++g) {
+                ok = issue_pv(g, j);
+                // S_g,j+1 reuses the TMEM columns P_g,j . V_j reads
+                if (ok && j + 1 < nt)
+                    ok = wait_all(o_bar(g), j & 1) && issue_s(g, j + 1);
+            }
         }
+        if (!ok && lane == 0)
+            give_up();
+        // no MMA may still run when TMEM is freed
+        tc::commit_warp(drain_bar);
+        if (!wait_all(drain_bar, 0) && lane == 0)
+            give_up();
     } else {
         // ---------------- softmax: one thread per row of its group ----------
         const int grp = (warp - 2) >> 2;
@@ -346,25 +353,29 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
             tc::fence_after_sync();
             const int k0 = j * Sh::BN;
             const int vis = pos - k0;              // keys [0, vis] of the tile are visible
-            // pass 1: row maximum of the visible scores, as a tree
-            float mt = -INFINITY;
+            // the 128 scores of the row, both halves held in registers
+            uint32_t v[2][64];
+            __syncwarp();                        // tcgen05.ld is warp-collective
+            tc::tmem_ld64(tg + Sh::COL_S, v[0]);
+            tc::tmem_ld64(tg + Sh::COL_S + 64, v[1]);
+            // tiles left of the diagonal (the common case) need no mask
+            const bool full = __all_sync(FULL, vis >= Sh::BN - 1);
+            if (!full) {
 #pragma unroll
-            for (int hb = 0; hb < 2; ++hb) {
-                uint32_t v[64];
-                __syncwarp();                    // tcgen05.ld is warp-collective
-                tc::tmem_ld64(tg + Sh::COL_S + 64 * hb, v);
-                float mx[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    mx[e] = -INFINITY;
-#pragma unroll
-                for (int e = 0; e < 64; ++e) {
-                    const float x = 64 * hb + e <= vis ? __uint_as_float(v[e]) : -INFINITY;
-                    mx[e & 7] = fmaxf(mx[e & 7], x);
-                }
-                mt = fmaxf(mt, fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                     fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))));
+                for (int e = 0; e < Sh::BN; ++e)
+                    if (e > vis)
+                        v[e >> 6][e & 63] = __float_as_uint(-INFINITY);
             }
+            // row maximum as a tree
+            float mx[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                mx[e] = fmaxf(__uint_as_float(v[0][e]), __uint_as_float(v[1][e]));
+#pragma unroll
+            for (int e = 8; e < 64; ++e)
+                mx[e & 7] = fmaxf(mx[e & 7], fmaxf(__uint_as_float(v[0][e]), __uint_as_float(v[1][e])));
+            float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
             mt *= sl2;                           // scale > 0: max commutes with it
             // running maximum, raised lazily: only when the tile's maximum
             // exceeds it by more than 8 (P stays below 2^8 otherwise)
@@ -377,22 +388,17 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
                 alpha = ex2_approx(m - mt);
                 m = mt;
             }
-            // pass 2: P = 2^(scale*s - m) packed to the operand type, written
-            // into TMEM over score columns already read (keys 0-63 -> columns
-            // 0-31, keys 64-127 -> 32-63)
+            // P = 2^(scale*s - m) packed to the operand type, written into
+            // TMEM over score columns already read: keys 0-63 -> columns
+            // 0-31, keys 64-127 -> 32-63
             float sum[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int hb = 0; hb < 2; ++hb) {
-                uint32_t v[64];
-                __syncwarp();
-                tc::tmem_ld64(tg + Sh::COL_S + 64 * hb, v);
                 uint32_t pw[32];
 #pragma unroll
                 for (int e = 0; e < 64; e += 2) {
-                    const float x0 = 64 * hb + e <= vis ? __uint_as_float(v[e]) : -INFINITY;
-                    const float x1 = 64 * hb + e + 1 <= vis ? __uint_as_float(v[e + 1]) : -INFINITY;
-                    const float p0 = ex2_approx(fmaf(x0, sl2, -m));
-                    const float p1 = ex2_approx(fmaf(x1, sl2, -m));
+                    const float p0 = ex2_approx(fmaf(__uint_as_float(v[hb][e]), sl2, -m));
+                    const float p1 = ex2_approx(fmaf(__uint_as_float(v[hb][e + 1]), sl2, -m));
                     sum[(e >> 1) & 3] += p0 + p1;
                     pw[e / 2] = Mma<T>::pack(p0, p1);
                 }

@@ -1,7 +1,8 @@
 // pa_tcgen05.cuh -- sm_100-family tensor-core helpers (inline PTX): the
-// fifth-generation MMA (tcgen05.mma) with operands in shared memory (and A
-// optionally in tensor memory, TMEM) and fp32 accumulators in TMEM, TMEM allocation, TMEM <->
-// register moves, and the fences that order them against thread barriers.
+// fifth-generation MMA (tcgen05.mma) with operands in shared memory (A
+// optionally in tensor memory, TMEM) and fp32 accumulators in TMEM, TMEM
+// allocation, TMEM <-> register moves, and the fences that order them
+// against thread barriers.
 //
 // Descriptor formats (PTX ISA, tcgen05 "instruction descriptor" and "shared
 // memory descriptor"):
@@ -44,39 +45,49 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
            ((uint64_t)((sbo & 0x3ffffu) >> 4) << 32) | (1ull << 46) | (2ull << 61);
 }
 
-// D[tmem] (+)= A[smem] . B[smem]^T, issued by one thread.
-__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
-                                       uint32_t accumulate)
+// MMA issue: every lane of a converged warp executes these with the same
+// (warp-uniform) operands and one elected lane issues the instruction, so
+// descriptors stay in uniform registers and MMAs issue back to back (a loop
+// run by a single lane issues them at a fraction of the tensor core's rate).
+// The elected lane is the same every time (the lowest lane of a full warp),
+// as tcgen05.commit needs: it tracks the MMAs its own thread issued.
+//   mma_ss_warp  D[tmem] (+)= A[smem] . B[smem]^T
+//   mma_ts_warp  D[tmem] (+)= A[tmem] . B[smem]^T, A being M rows in TMEM
+//                lanes 0..M-1, its K 16-bit elements packed two per 32-bit
+//                column (lower element in the low half) from column a_tmem
+//   commit_warp  arrive once on `bar` when every tcgen05 operation the
+//                issuing thread started so far has completed
+__device__ __forceinline__ void mma_ss_warp(uint32_t d_tmem, uint64_t a, uint64_t b,
+                                            uint32_t idesc, uint32_t accumulate)
 {
     asm volatile(
-        "{\n\t.reg .pred p;\n\t"
+        "{\n\t.reg .pred p, e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
-// D[tmem] (+)= A[tmem] . B[smem]^T: A is M rows in TMEM lanes 0..M-1, its K
-// 16-bit elements packed two per 32-bit column (lower element in the low
-// half), K/2 columns from a_tmem.
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
-                                       uint32_t idesc, uint32_t accumulate)
+__device__ __forceinline__ void mma_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                            uint32_t idesc, uint32_t accumulate)
 {
     asm volatile(
-        "{\n\t.reg .pred p;\n\t"
+        "{\n\t.reg .pred p, e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
         "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
-// Arrive once on `bar` when every tcgen05 operation this thread issued so far
-// has completed.
-__device__ __forceinline__ void commit(uint32_t bar)
+__device__ __forceinline__ void commit_warp(uint32_t bar)
 {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::
-                     "r"(bar)
-                 : "memory");
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
+        : "memory");
 }
 
 // Warp-wide: allocate `ncols` TMEM columns (a power of two >= 32); the base
