@@ -159,15 +159,28 @@ int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache
  *   other arguments as in pa_decode.
  * Rows are computed on the fifth-generation tensor cores (S = Q.K^T and
  * O += P.V with fp32 accumulators in tensor memory); P is rounded to dtype
- * before P.V.  A chunk longer than its sequence or than max_query_len is
- * skipped and sets PA_DEVERR_QUERY_RANGE; table entries outside the pool set
- * PA_DEVERR_TABLE_RANGE (block 0 is read instead).  No workspace; one launch.
+ * before P.V.  A chunk longer than its sequence is skipped and sets
+ * PA_DEVERR_QUERY_RANGE; so does one longer than max_query_len, of which
+ * only the last max_query_len-ish rows (whole 256-row tiles) are computed.
+ * Table entries outside the pool set PA_DEVERR_TABLE_RANGE (block 0 is read
+ * instead).
+ *
+ * workspace (optional, 256-byte aligned, caller-owned, no initialisation
+ * needed): at least pa_prefill_workspace_size(...) bytes.  With it a small
+ * planning kernel first sorts the (sequence, query tile) work by its length,
+ * longest first, so the grid ends on short work (the greedy longest-first
+ * schedule); without it (NULL) the work runs in a fixed order.  Results are
+ * bit-identical either way.  Calls sharing a workspace must be ordered on
+ * one stream.  PA_ERR_WORKSPACE if it is too small or misaligned.
  */
+size_t pa_prefill_workspace_size(int num_seqs, int max_query_len, int num_heads,
+                                 int num_kv_heads);
+
 int pa_prefill(void *out, const void *q, const void *k_cache, const void *v_cache,
                const int32_t *block_tables, const int32_t *seq_lens, const int32_t *query_start,
                int num_seqs, int max_query_len, int num_heads, int num_kv_heads, int head_dim,
                int block_size, int max_blocks_per_seq, int num_blocks, float scale, int dtype,
-               void *stream);
+               void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * One decode step with the new tokens appended on the way: the result equals

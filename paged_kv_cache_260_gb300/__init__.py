@@ -78,7 +78,10 @@ def load(path: str = LIB_PATH):
         L.pa_validate_tables.restype = i
         L.pa_validate_tables.argtypes = [vp, vp, i, i, i, i, vp, vp]
         L.pa_prefill.restype = i
-        L.pa_prefill.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i, vp]
+        L.pa_prefill.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i, vp,
+                                 sz, vp]
+        L.pa_prefill_workspace_size.restype = sz
+        L.pa_prefill_workspace_size.argtypes = [i, i, i, i]
         L.pa_selftest_bounded_wait.restype = i
         L.pa_selftest_bounded_wait.argtypes = [i, vp]
         L.pa_get_device_error.restype = i
@@ -198,13 +201,19 @@ def decode_append(out, q, k_cache, v_cache, block_tables, seq_lens, k_new, v_new
     return out
 
 
+def prefill_workspace_size(num_seqs, max_query_len, num_heads, num_kv_heads) -> int:
+    return int(load().pa_prefill_workspace_size(num_seqs, max_query_len, num_heads, num_kv_heads))
+
+
 def prefill(out, q, k_cache, v_cache, block_tables, seq_lens, query_start, max_query_len, scale,
-            stream=None):
+            workspace="auto", stream=None):
     """pa_prefill: causal attention of each sequence's newest chunk over the paged pool.
 
     q, out [total_q, num_heads, head_dim], the chunks packed back to back;
     query_start int32 [num_seqs + 1]; seq_lens int32 [num_seqs] counts the
-    chunk; max_query_len (host int) is the longest chunk.
+    chunk; max_query_len (host int) is the longest chunk.  workspace: "auto"
+    allocates the work-order buffer, None runs without it, or a CUDA uint8
+    tensor of at least prefill_workspace_size(...) bytes.
     """
     t, hq, d = q.shape
     nb, hkv, bs, d2 = k_cache.shape
@@ -214,10 +223,15 @@ def prefill(out, q, k_cache, v_cache, block_tables, seq_lens, query_start, max_q
              query_start.shape == (n + 1,), "table shapes")
     for x in (out, q, k_cache, v_cache, block_tables, seq_lens, query_start):
         _require(x.is_cuda and x.is_contiguous(), "tensors must be contiguous CUDA tensors")
+    if isinstance(workspace, str):
+        nbytes = prefill_workspace_size(n, int(max_query_len), hq, hkv)
+        workspace = (_torch().empty(nbytes, dtype=_torch().uint8, device=q.device)
+                     if nbytes else None)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = load().pa_prefill(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
                            _ptr(seq_lens), _ptr(query_start), n, int(max_query_len), hq, hkv, d,
                            bs, block_tables.shape[1], nb, float(scale), _dtype_code(q),
-                           _stream(stream))
+                           _ptr(workspace), wbytes, _stream(stream))
     _check("pa_prefill", rc)
     return out
 

@@ -454,11 +454,32 @@ int pa_decode_append(void *out, const void *q, void *k_cache, void *v_cache,
                        slot_mapping);
 }
 
+// Query tiles per (sequence, kv head) of a prefill grid, 0 on bad arguments.
+static long long prefill_q_ranks(int max_query_len, int num_heads, int num_kv_heads)
+{
+    if (max_query_len <= 0 || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads ||
+        num_heads / num_kv_heads > kPrefillRows)
+        return 0;
+    const int tokens_per_block = kPrefillTiles * (kPrefillRows / (num_heads / num_kv_heads));
+    return (max_query_len + tokens_per_block - 1) / tokens_per_block;
+}
+
+// Work-order workspace: the pair count, then one word per (sequence, query
+// tile) pair.
+size_t pa_prefill_workspace_size(int num_seqs, int max_query_len, int num_heads,
+                                 int num_kv_heads)
+{
+    const long long q_ranks = prefill_q_ranks(max_query_len, num_heads, num_kv_heads);
+    if (num_seqs <= 0 || q_ranks <= 0)
+        return 0;
+    return round_up(16 + 4 * (size_t)num_seqs * (size_t)q_ranks, 256);
+}
+
 int pa_prefill(void *out, const void *q, const void *k_cache, const void *v_cache,
                const int32_t *block_tables, const int32_t *seq_lens, const int32_t *query_start,
                int num_seqs, int max_query_len, int num_heads, int num_kv_heads, int head_dim,
                int block_size, int max_blocks_per_seq, int num_blocks, float scale, int dtype,
-               void *stream)
+               void *workspace, size_t workspace_bytes, void *stream)
 {
     int rc = check_common(num_kv_heads, head_dim, block_size, num_blocks, dtype);
     if (rc != PA_OK)
@@ -477,12 +498,21 @@ int pa_prefill(void *out, const void *q, const void *k_cache, const void *v_cach
         !aligned(block_tables, 4) || !aligned(seq_lens, 4) || !aligned(query_start, 4))
         return PA_ERR_INVALID_ARG;
     const long long pool_rows = (long long)num_blocks * num_kv_heads * kBlockSize;
-    const int tokens_per_block = kPrefillTiles * (kPrefillRows / group);
-    const long long q_ranks = (max_query_len + tokens_per_block - 1) / tokens_per_block;
+    const long long q_ranks = prefill_q_ranks(max_query_len, num_heads, num_kv_heads);
     const long long grid = q_ranks * num_seqs * num_kv_heads;
     if ((long long)max_blocks_per_seq * kBlockSize >= (1LL << 30) || pool_rows >= (1LL << 31) ||
         grid >= (1LL << 31))
         return PA_ERR_UNSUPPORTED;
+    const bool planned = workspace != nullptr;
+    if (planned) {
+        // plan entries pack (sequence, tile) into 16 + 16 bits
+        if (num_seqs > 65535 || q_ranks > 65535)
+            return PA_ERR_UNSUPPORTED;
+        if (!aligned(workspace, 256) ||
+            workspace_bytes < pa_prefill_workspace_size(num_seqs, max_query_len, num_heads,
+                                                        num_kv_heads))
+            return PA_ERR_WORKSPACE;
+    }
     PrefillKernel kk{};
     if (!prefill_kernel(dtype, head_dim, &kk))
         return PA_ERR_UNSUPPORTED;
@@ -517,9 +547,22 @@ int pa_prefill(void *out, const void *q, const void *k_cache, const void *v_cach
     p.num_blocks = num_blocks;
     p.q_ranks = (int)q_ranks;
     p.scale_log2 = scale * 1.4426950408889634f;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (planned) {
+        int *count = static_cast<int *>(workspace);
+        uint32_t *plan = reinterpret_cast<uint32_t *>(static_cast<char *>(workspace) + 16);
+        p.plan = plan;
+        p.plan_count = count;
+        int tpb = kPrefillTiles * (kPrefillRows / group), bn = kPrefillKeys;
+        void *pargs[] = {&p, &tpb, &bn, &plan, &count};
+        rc = cuda_status(cudaLaunchKernel(kk.plan_fn, dim3(1), dim3(1024), pargs, 0, st));
+        if (rc != PA_OK)
+            return rc;
+    }
+    // a programmatic dependent launch: its blocks may be scheduled while the
+    // plan finishes and read no global memory before it has completed
     void *args[] = {&p, &tmk, &tmv};
-    return cuda_status(cudaLaunchKernel(kk.fn, dim3((unsigned)grid), dim3(kk.threads), args,
-                                        kk.smem, static_cast<cudaStream_t>(stream)));
+    return launch_dependent(kk.fn, dim3((unsigned)grid), dim3(kk.threads), kk.smem, st, args);
 }
 
 int pa_reshape_and_cache(const void *k_new, const void *v_new, void *k_cache, void *v_cache,

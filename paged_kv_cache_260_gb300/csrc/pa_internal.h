@@ -87,17 +87,26 @@ struct PrefillParams {
     int num_blocks;
     int q_ranks;                   // query tiles per (sequence, kv head) in the grid
     float scale_log2;
+    // optional work order (a planning kernel writes it): block b computes
+    // pair plan[b / num_kv_heads] = (sequence << 16 | query tile), for
+    // b / num_kv_heads < *plan_count, heaviest pairs first; null: the grid
+    // is walked as (query tile from the end, sequence, kv head)
+    const uint32_t *plan;
+    const int *plan_count;
 };
 
 struct PrefillKernel {
     const void *fn;
     int threads;
     size_t smem;
+    const void *plan_fn;           // prefill_plan_kernel: (PrefillParams, tokens per block,
+                                   // keys per tile, uint32_t *plan, int *count)
 };
 
 bool prefill_kernel(int dtype, int head_dim, PrefillKernel *k);
 constexpr int kPrefillRows = 128;   // (token, head) rows of one prefill query tile
 constexpr int kPrefillTiles = 2;    // query tiles of one prefill thread block
+constexpr int kPrefillKeys = 128;   // keys per prefill key tile
 
 bool decode_kernels_f16(int head_dim, int group, KernelSet *ks);
 bool decode_kernels_bf16(int head_dim, int group, KernelSet *ks);

@@ -9,6 +9,7 @@ static void prefill_entry(PrefillKernel *k)
     k->fn = reinterpret_cast<const void *>(&prefill_tc_kernel<T, D>);
     k->threads = PrefillShape<D>::THREADS;
     k->smem = PrefillShape<D>::SMEM;
+    k->plan_fn = reinterpret_cast<const void *>(&prefill_plan_kernel);
 }
 
 bool prefill_kernel(int dtype, int head_dim, PrefillKernel *k)

@@ -52,7 +52,7 @@ template <int D>
 struct PrefillShape {
     static constexpr int BM = kPrefillRows;                 // rows per group (tile)
     static constexpr int NG = kPrefillTiles;                // groups per block
-    static constexpr int BN = 128;                          // keys per tile
+    static constexpr int BN = kPrefillKeys;                 // keys per tile
     static constexpr int NB = BN / kBlockSize;              // pool blocks per tile
     static constexpr int HALVES = D / 64;                   // 128-byte column boxes
     static constexpr int BOX = 2048;                        // 16 rows x 128 B
@@ -110,31 +110,46 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
     const int Hkv = p.num_kv_heads, Hq = p.num_heads, G = Hq / Hkv;
     const int TPG = Sh::BM / G;                   // chunk tokens per group
     const int TPB = Sh::NG * TPG;                 // chunk tokens per block
-    const int per_rank = p.num_seqs * Hkv;
-    const int rank = blockIdx.x / per_rank;
-    const int s = (blockIdx.x % per_rank) / Hkv;
     const int h = blockIdx.x % Hkv;
 
     // ---- the block's rows and key range (uniform over the block) ----------
+    // no global memory is read before the preceding kernel (the plan) is done
+    grid_dependency_wait();
+    int s, rank = 0, tile = 0;
+    if (p.plan) {
+        const int k = blockIdx.x / Hkv;
+        if (k >= *p.plan_count)
+            return;
+        const uint32_t e = p.plan[k];
+        s = (int)(e >> 16);
+        tile = (int)(e & 0xffffu);
+    } else {
+        const int per_rank = p.num_seqs * Hkv;
+        rank = blockIdx.x / per_rank;
+        s = (blockIdx.x % per_rank) / Hkv;
+    }
     const int L = __ldg(p.seq_lens + s);
     const int qs = __ldg(p.query_start + s);
     const int c = __ldg(p.query_start + s + 1) - qs;
+    const bool reporter = !p.plan && rank == 0 && h == 0 && tid == 0;   // the plan reports itself
     if (L < 0 || L > p.max_blocks * kBlockSize) {
-        if (rank == 0 && h == 0 && tid == 0)
+        if (reporter)
             record_error(p.err, PA_DEVERR_SEQLEN_RANGE);
         return;
     }
     if (c < 0 || c > L) {
-        if (rank == 0 && h == 0 && tid == 0)
+        if (reporter)
             record_error(p.err, PA_DEVERR_QUERY_RANGE);
         return;
     }
-    const int nq = (c + TPB - 1) / TPB;
-    if (nq > p.q_ranks && rank == 0 && h == 0 && tid == 0)
-        record_error(p.err, PA_DEVERR_QUERY_RANGE);   // max_query_len too small
-    if (rank >= nq)
-        return;
-    const int tile = nq - 1 - rank;               // rank 0 = the last (longest) tile
+    if (!p.plan) {
+        const int nq = (c + TPB - 1) / TPB;
+        if (nq > p.q_ranks && reporter)
+            record_error(p.err, PA_DEVERR_QUERY_RANGE);   // max_query_len too small
+        if (rank >= nq)
+            return;
+        tile = nq - 1 - rank;                     // rank 0 = the last (longest) tile
+    }
     const int t0 = tile * TPB;
     const int t_end = min(t0 + TPB, c);
     const int p_last = L - c + t_end - 1;         // position of the block's last row
@@ -478,6 +493,93 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
     if (warp == 1) {
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem, Sh::TMEM_COLS);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Work order of a prefill: the (sequence, query tile) pairs sorted by their
+// key-tile count, heaviest first (a counting sort on the count, one block).
+// The hardware hands thread blocks to SMs in index order as SMs free up, so
+// blocks that walk this order give the greedy longest-first schedule, and
+// the run ends on the lightest pairs.  Pairs of one count keep no particular
+// order (their results do not depend on it).
+// ---------------------------------------------------------------------------
+constexpr int kPlanBuckets = 2048;   // key-tile counts above this share the top bucket
+
+__global__ void __launch_bounds__(1024)
+prefill_plan_kernel(const PrefillParams p, int tpb, int bn, uint32_t *plan, int *count)
+{
+    __shared__ int hist[kPlanBuckets];
+    const int tid = threadIdx.x, lane = tid & 31;
+    grid_dependents_launch();                // the prefill may be scheduled; it waits for us
+    for (int i = tid; i < kPlanBuckets; i += 1024)
+        hist[i] = 0;
+    __syncthreads();
+    // the query tiles of sequence s that run: [first, last); errors reported once
+    auto tiles = [&](int s, bool report, int &L, int &c, int &first) {
+        L = p.seq_lens[s];
+        const int qs = p.query_start[s];
+        c = p.query_start[s + 1] - qs;
+        first = 0;
+        if (L < 0 || L > p.max_blocks * kBlockSize) {
+            if (report)
+                record_error(p.err, PA_DEVERR_SEQLEN_RANGE);
+            return 0;
+        }
+        if (c < 0 || c > L) {
+            if (report)
+                record_error(p.err, PA_DEVERR_QUERY_RANGE);
+            return 0;
+        }
+        const int nq = (c + tpb - 1) / tpb;
+        if (nq > p.q_ranks) {                // the grid covers the last q_ranks tiles
+            if (report)
+                record_error(p.err, PA_DEVERR_QUERY_RANGE);
+            first = nq - p.q_ranks;
+        }
+        return nq;
+    };
+    auto bucket = [&](int L, int c, int t) {
+        const int t_end = min((t + 1) * tpb, c);
+        return min((L - c + t_end - 1) / bn + 1, kPlanBuckets - 1);
+    };
+    for (int s = tid; s < p.num_seqs; s += 1024) {
+        int L, c, first;
+        const int nq = tiles(s, true, L, c, first);
+        for (int t = first; t < nq; ++t)
+            atomicAdd(&hist[bucket(L, c, t)], 1);
+    }
+    __syncthreads();
+    // start of each bucket in descending order: lane l scans buckets
+    // [B - 64(l+1), B - 64 l) from the top, then a warp scan joins the lanes
+    if (tid < 32) {
+        constexpr int PER = kPlanBuckets / 32;
+        const int hi = kPlanBuckets - lane * PER;
+        int local = 0;
+        for (int b = hi - 1; b >= hi - PER; --b)
+            local += hist[b];
+        int incl = local;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o)
+                incl += y;
+        }
+        int run = incl - local;
+        for (int b = hi - 1; b >= hi - PER; --b) {
+            const int n = hist[b];
+            hist[b] = run;
+            run += n;
+        }
+        if (lane == 31)
+            *count = incl;
+    }
+    __syncthreads();
+    for (int s = tid; s < p.num_seqs; s += 1024) {
+        int L, c, first;
+        const int nq = tiles(s, false, L, c, first);
+        for (int t = first; t < nq; ++t)
+            plan[atomicAdd(&hist[bucket(L, c, t)], 1)] = ((uint32_t)s << 16) | (uint32_t)t;
     }
 }
 

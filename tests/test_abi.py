@@ -122,7 +122,8 @@ def test_prefill_rejects_bad_scalars(lib):
                  nb=64, scale=0.1, dtype=1)
         a.update(kw)
         return lib.pa_prefill(*a["ptrs"], a["num_seqs"], a["max_q"], a["hq"], a["hkv"], a["d"],
-                              a["bs"], a["maxb"], a["nb"], C.c_float(a["scale"]), a["dtype"], None)
+                              a["bs"], a["maxb"], a["nb"], C.c_float(a["scale"]), a["dtype"],
+                              a.get("ws"), a.get("ws_bytes", 0), None)
 
     assert call(d=96) == 2
     assert call(bs=32) == 2
@@ -134,3 +135,15 @@ def test_prefill_rejects_bad_scalars(lib):
     assert call(num_seqs=0) == 0 and call(max_q=0) == 0
     assert call() == 1                               # null pointers
     assert call(ptrs=[fake, C.c_void_p(0x1008)] + [fake] * 5) == 1   # misaligned q
+    # a workspace smaller than pa_prefill_workspace_size, or misaligned
+    assert call(ptrs=[fake] * 7, ws=fake, ws_bytes=16) == 3
+    assert call(ptrs=[fake] * 7, ws=C.c_void_p(0x1010), ws_bytes=4096) == 3
+
+
+def test_prefill_workspace_size(lib):
+    lib.pa_prefill_workspace_size.restype = C.c_size_t
+    # 32 q heads over 8 kv heads: 4 per group, 64 chunk tokens per block
+    assert lib.pa_prefill_workspace_size(8, 512, 32, 8) == 512          # 16 + 4*8*8 -> 512
+    assert lib.pa_prefill_workspace_size(100, 1000, 32, 8) == 6656      # 16 + 4*100*16 -> 6656
+    assert lib.pa_prefill_workspace_size(0, 512, 32, 8) == 0
+    assert lib.pa_prefill_workspace_size(8, 512, 30, 8) == 0            # not a multiple

@@ -145,3 +145,26 @@ def test_prefill_then_decode_continues_the_sequence(pa):
     ref = oracle.decode(q, k_host, v_host, table, np.array([done], np.int32), scale, dt)
     assert max_err(out, ref) <= TOL[dt]
     assert pa.get_device_error() == 0
+
+
+def test_prefill_work_order_does_not_change_results(pa):
+    # with the planning workspace (longest work first) and without it, the
+    # output is bit-identical; a too-small workspace is refused
+    w = synth.build_prefill("pf", 32, 8, 128, "bf16", [900, 130, 2000, 64, 700],
+                            [600, 130, 200, 1, 333], seed=21, poison=True)
+    q = dev_bits(w.q, w.dtype)
+    k, v = dev_bits(w.k_cache, w.dtype), dev_bits(w.v_cache, w.dtype)
+    t = torch.from_numpy(w.block_tables).cuda()
+    lens = torch.from_numpy(w.seq_lens).cuda()
+    qs = torch.from_numpy(w.query_start).cuda()
+    mq = int(np.diff(w.query_start).max())
+    a, b = torch.empty_like(q), torch.empty_like(q)
+    pa.prefill(a, q, k, v, t, lens, qs, mq, w.scale, workspace=None)
+    pa.prefill(b, q, k, v, t, lens, qs, mq, w.scale)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert pa.get_device_error() == 0
+    assert max_err(a, _ref(w)) <= TOL["bf16"]
+    small = torch.empty(64, dtype=torch.uint8, device="cuda")
+    with pytest.raises(pa.PagedAttnError) as e:
+        pa.prefill(b, q, k, v, t, lens, qs, mq, w.scale, workspace=small)
+    assert e.value.status == 3
