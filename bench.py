@@ -603,6 +603,155 @@ def run_swap(args):
     }), flush=True)
 
 
+PREFILL_METRIC = ("paged chunked prefill: causal attention TFLOP/s on tcgen05 tensor cores, "
+                  "% of GB300 dense bf16 peak")
+PREFILL_DESCRIPTION = ("chunked prefill: 8 seqs, 32/8 heads, head_dim 128, bf16, contexts "
+                       "U[512,4096] ending in a 512-token chunk (4096 query rows)")
+
+
+def measured_bf16_peak():
+    """(TFLOP/s, source) from MEASURED_PEAKS.json (cuBLAS bf16 burst), else the
+    recipe's fallback."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
+def prefill_flops(w, rows=None):
+    """Algorithmic flops of a causal chunked prefill (2 for q.k and 2 for p.v per
+    visible key, channel and head); rows: only the last `rows` rows of each chunk."""
+    total = 0
+    for s in range(w.num_seqs):
+        c = int(w.query_start[s + 1] - w.query_start[s])
+        L = int(w.seq_lens[s])
+        r = c if rows is None else min(rows, c)
+        # rows i = c-r .. c-1 see L-c+i+1 keys
+        total += sum(L - c + i + 1 for i in range(c - r, c))
+    return 4 * w.head_dim * w.num_heads * total
+
+
+def prefill_cpu_baseline(w, rows=32):
+    """The fp64 oracle on the last `rows` rows of every chunk (a prefill whose
+    chunks are those rows, over the same contexts)."""
+    import oracle
+    oracle.build()
+    threads = min(oracle.num_threads(), w.num_seqs)
+    idx = []
+    qs = [0]
+    for s in range(w.num_seqs):
+        a, b = int(w.query_start[s]), int(w.query_start[s + 1])
+        r = min(rows, b - a)
+        idx.extend(range(b - r, b))
+        qs.append(qs[-1] + r)
+    q = np.ascontiguousarray(w.q[idx])
+    t0 = time.perf_counter()
+    oracle.prefill(q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens,
+                   np.array(qs, np.int32), w.scale, w.dtype, threads=threads)
+    dt = time.perf_counter() - t0
+    sample = (f"fp64 oracle prefill of the last {rows} rows of each of the {w.num_seqs} chunks "
+              f"({len(idx)} rows x {w.num_heads} heads) in {dt:.1f} s")
+    return prefill_flops(w, rows) / dt / 1e12, sample, threads
+
+
+def run_prefill(args):
+    """One pa_prefill (plan + kernel) per step on the chunked-prefill workload,
+    each launch timed with CUDA events and L2 flushed between launches."""
+    import torch
+    from paged_kv_cache_260_gb300 import _build
+    _build.build()
+    import paged_kv_cache_260_gb300 as pa
+    import synth
+    pa.load()
+    device = torch.device("cuda:0")
+    torch.cuda.set_device(device)
+    w = synth.prefill_chunks()
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float16
+
+    def dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(tdt).to(device)
+
+    q, k, v = dev(w.q), dev(w.k_cache), dev(w.v_cache)
+    tables = torch.from_numpy(w.block_tables).to(device)
+    lens = torch.from_numpy(w.seq_lens).to(device)
+    qs = torch.from_numpy(w.query_start).to(device)
+    out = torch.empty_like(q)
+    mq = int(np.diff(w.query_start).max())
+    ws = torch.empty(pa.prefill_workspace_size(w.num_seqs, mq, w.num_heads, w.num_kv_heads),
+                     dtype=torch.uint8, device=device)
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=device)
+    flops = prefill_flops(w)
+
+    def call():
+        pa.prefill(out, q, k, v, tables, lens, qs, mq, w.scale, workspace=ws)
+
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize(device)
+    assert pa.get_device_error() == 0
+    steps = max(3, min(args.steps, 200))
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        for e0, e1 in ev:
+            flush.zero_()                      # K/V (90 MB) would otherwise stay in L2
+            e0.record()
+            call()
+            e1.record()
+        torch.cuda.synchronize(device)
+    ms = sum(e0.elapsed_time(e1) for e0, e1 in ev) / steps
+    assert pa.get_device_error() == 0
+    value = flops / (ms * 1e-3) / 1e12
+    peak, peak_src = measured_bf16_peak()
+
+    # end to end through the public API: q, tables, lengths and query starts
+    # from pinned host memory, the output back to it, every step
+    hq = torch.from_numpy(np.ascontiguousarray(w.q).view(np.int16)).view(tdt).pin_memory()
+    ht = torch.from_numpy(w.block_tables).pin_memory()
+    hl = torch.from_numpy(w.seq_lens).pin_memory()
+    hs = torch.from_numpy(w.query_start).pin_memory()
+    hout = torch.empty_like(hq).pin_memory()
+    h2d = sum(x.numel() * x.element_size() for x in (hq, ht, hl, hs))
+    d2h = hout.numel() * hout.element_size()
+    e2e_steps = max(3, min(steps, 50))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_ms = 0.0
+    for _ in range(e2e_steps):
+        flush.zero_()
+        e0.record()
+        q.copy_(hq, non_blocking=True)
+        tables.copy_(ht, non_blocking=True)
+        lens.copy_(hl, non_blocking=True)
+        qs.copy_(hs, non_blocking=True)
+        call()
+        hout.copy_(out, non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize(device)
+        e2e_ms += e0.elapsed_time(e1)
+    e2e_ms /= e2e_steps
+    cpu = None
+    if not args.no_cpu_baseline:
+        cv, sample, cores = prefill_cpu_baseline(w)
+        cpu = {"value": cv, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample}
+    print(json.dumps({
+        "metric": PREFILL_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": 1,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": PREFILL_DESCRIPTION, "name": "prefill",
+                   "l2": "flushed (256 MB write) before every timed launch",
+                   "flops": "causal: 4 * head_dim * heads * visible keys per row"},
+        "roofline": {"bound": "tensor", "achieved": value, "peak": peak, "unit": "TFLOP/s",
+                     "frac": value / peak, "traffic": None,
+                     "peak_source": peak_src + " (MEASURED_PEAKS.json bf16_tflops, cuBLAS burst)"},
+        "e2e": {"value": flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "cpu_baseline": cpu,
+        "clocks": clk.summary(),
+        "gpu_launches": 2 * steps,
+    }), flush=True)
+
+
 def run_reference(args):
     """The oracle as the reference arm: each step is a bounded sample of the
     workload (whole sequences in order) on the host cores."""
@@ -648,13 +797,36 @@ def run_reference(args):
     }), flush=True)
 
 
+def run_reference_prefill(args):
+    """The oracle as the reference arm of the prefill line: each step is the
+    bounded sample of prefill_cpu_baseline."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import synth
+    w = synth.prefill_chunks()
+    vals = [prefill_cpu_baseline(w, rows=8) for _ in range(min(4, args.warmup + args.steps))]
+    value, sample, cores = vals[-1]
+    print(json.dumps({
+        "impl": "reference", "metric": PREFILL_METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": len(vals), "warmup": 0, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": PREFILL_DESCRIPTION, "name": "prefill"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=list(DESCRIPTION) + ["swap"], default="gqa8b")
+    ap.add_argument("--workload", choices=list(DESCRIPTION) + ["swap", "prefill"],
+                    default="gqa8b")
     ap.add_argument("--partition", type=int, default=None,
                     help="-1 no split, 0 balanced split, >0 fixed partition tokens")
     ap.add_argument("--no-graph", action="store_true")
@@ -663,9 +835,17 @@ def main(argv=None):
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
-        run_reference(args)
+        if args.workload == "prefill":
+            run_reference_prefill(args)
+        elif args.workload == "swap":
+            print(json.dumps({"impl": "reference", "unavailable": "swap_blocks moves bytes "
+                              "between memories; the oracle has no timed counterpart"}))
+        else:
+            run_reference(args)
     elif args.workload == "swap":
         run_swap(args)
+    elif args.workload == "prefill":
+        run_prefill(args)
     else:
         run_ours(args)
 
