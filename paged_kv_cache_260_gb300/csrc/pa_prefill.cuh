@@ -13,11 +13,12 @@
 // 128 / G consecutive chunk tokens times the G q heads that share the kv
 // head.  Both groups consume every K/V tile the block stages.
 //
-// What bounds the kernel is the shared-memory bandwidth the tensor core
-// reads its operands with, so the design keeps operand bytes per flop low:
-// key tiles of 128 (Q is read once per 128 keys), and P never goes through
-// shared memory -- the softmax writes it into tensor memory over the score
-// columns it has consumed, and P.V takes its A operand from there.
+// Operand bytes per flop are kept low: key tiles of 128 (Q is read from
+// shared memory once per 128 keys), and P never goes through shared memory
+// -- the softmax writes it into tensor memory over the score columns it has
+// consumed, and P.V takes its A operand from there.  What bounds the kernel
+// is each group's chain S -> softmax -> P.V -> next S against the other
+// group's MMA work.
 // Warp roles (320 threads):
 //   warp 0    TMA producer of K and V tiles of 128 keys (8 pool blocks x 16
 //             rows x 128-byte boxes) into a ring of slots;
