@@ -168,3 +168,70 @@ def test_prefill_work_order_does_not_change_results(pa):
     with pytest.raises(pa.PagedAttnError) as e:
         pa.prefill(b, q, k, v, t, lens, qs, mq, w.scale, workspace=small)
     assert e.value.status == 3
+
+
+def test_prefill_in_a_cuda_graph(pa):
+    # the planning kernel and the dependent prefill launch are captured and
+    # replayed; replays match the eager call bit for bit
+    w = synth.build_prefill("pf", 32, 8, 128, "bf16", [700, 300, 1200], [300, 300, 64], seed=23)
+    q = dev_bits(w.q, w.dtype)
+    k, v = dev_bits(w.k_cache, w.dtype), dev_bits(w.v_cache, w.dtype)
+    t = torch.from_numpy(w.block_tables).cuda()
+    lens = torch.from_numpy(w.seq_lens).cuda()
+    qs = torch.from_numpy(w.query_start).cuda()
+    mq = int(np.diff(w.query_start).max())
+    ws = torch.empty(pa.prefill_workspace_size(w.num_seqs, mq, w.num_heads, w.num_kv_heads),
+                     dtype=torch.uint8, device="cuda")
+    eager, out = torch.empty_like(q), torch.zeros_like(q)
+    pa.prefill(eager, q, k, v, t, lens, qs, mq, w.scale, workspace=ws)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        pa.prefill(out, q, k, v, t, lens, qs, mq, w.scale, workspace=ws, stream=s)   # warm-up
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            pa.prefill(out, q, k, v, t, lens, qs, mq, w.scale, workspace=ws, stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    for _ in range(3):
+        out.zero_()
+        g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
+    assert pa.get_device_error() == 0
+
+
+def test_prefill_of_single_token_chunks_is_a_decode(pa):
+    # 200 sequences whose chunk is their newest token: the prefill is a
+    # decode batch; both kernels agree with the oracle's decode
+    rng = np.random.default_rng(8)
+    lens = rng.integers(1, 900, size=200)
+    w = synth.build_prefill("pf", 32, 8, 128, "bf16", lens, np.ones(200, int), seed=24, poison=True)
+    out = _run(pa, w)
+    assert pa.get_device_error() == 0
+    ref = oracle.decode(w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.scale, w.dtype)
+    assert max_err(out, ref) <= TOL["bf16"]
+    dec = torch.empty_like(out)
+    pa.decode(dec, dev_bits(w.q, w.dtype), dev_bits(w.k_cache, w.dtype),
+              dev_bits(w.v_cache, w.dtype), torch.from_numpy(w.block_tables).cuda(),
+              torch.from_numpy(w.seq_lens).cuda(), w.scale)
+    assert max_err(dec, ref) <= TOL["bf16"]
+
+
+def test_prefill_long_prompt_sampled_rows(pa):
+    # an 8192-token prompt prefilled as one chunk (64 blocks of 256 rows per
+    # kv head), plus a 2048-token chunk over 14000 tokens of context; rows
+    # sampled along the chunk against the oracle's decode of their prefix
+    w = synth.build_prefill("pf", 16, 4, 128, "f16", [8192, 16048], [8192, 2048], seed=25)
+    out = _run(pa, w)
+    assert pa.get_device_error() == 0
+    got = out.float().cpu().numpy().astype(np.float64)
+    assert np.isfinite(got).all()
+    for s in range(w.num_seqs):
+        c = int(w.query_start[s + 1] - w.query_start[s])
+        for i in (0, 1, 127, 128, 129, c // 2, c - 257, c - 2, c - 1):
+            row = int(w.query_start[s]) + i
+            p = int(w.seq_lens[s]) - c + i
+            ref = oracle.decode(w.q[row][None], w.k_cache, w.v_cache, w.block_tables[s][None],
+                                np.array([p + 1], np.int32), w.scale, w.dtype)
+            assert float(np.abs(got[row] - ref[0]).max()) <= TOL["f16"], (s, i)
