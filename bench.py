@@ -319,9 +319,19 @@ def pick_steps_per_graph(steps: int, cap: int = 32) -> int:
     return 1
 
 
+def pool_utilisation(w):
+    """Slots of the pool holding a live token (shared blocks counted once)."""
+    per_token = w.num_kv_heads * w.head_dim * 2 * 2
+    unique = w.unique_kv_read_bytes() // per_token
+    return {"live_tokens": int(unique), "pool_slots": int(w.num_blocks * 16),
+            "frac_slots_live": float(unique) / (w.num_blocks * 16),
+            "table_tokens": int(w.seq_lens.sum())}
+
+
 def cpu_baseline(w, budget_s: float = 12.0):
     """The fp64 oracle on a bounded sample: whole sequences in order, repeated
-    until ~budget_s of CPU work; returns (GB/s of KV processed, sample text, cores)."""
+    until ~budget_s of CPU work; returns (GB/s of KV processed, sample text,
+    cores, {sequence: oracle output row} of the first pass)."""
     import oracle
     oracle.build()
     threads = oracle.num_threads()
@@ -334,11 +344,15 @@ def cpu_baseline(w, budget_s: float = 12.0):
     per_seq = 2 * w.num_kv_heads * w.head_dim * 2
     done_bytes, seqs, reps = 0, 0, 0
     chunk = max(1, threads // 2)
+    rows = {}
     while True:
         for s0 in range(0, w.num_seqs, chunk):
             sel = list(range(s0, min(w.num_seqs, s0 + chunk)))
-            oracle.decode(w.q, k, v, w.block_tables, w.seq_lens, w.scale, w.dtype, seqs=sel,
-                          threads=threads)
+            out = oracle.decode(w.q, k, v, w.block_tables, w.seq_lens, w.scale, w.dtype,
+                                seqs=sel, threads=threads)
+            if reps == 0:
+                for s in sel:
+                    rows[s] = out[s]
             done_bytes += int(sum(int(w.seq_lens[s]) for s in sel)) * per_seq
             seqs += len(sel)
             if time.perf_counter() - t0 > budget_s:
@@ -351,7 +365,7 @@ def cpu_baseline(w, budget_s: float = 12.0):
     dt = time.perf_counter() - t0
     sample = (f"fp64 oracle step (copy/reshape once, then decode of {seqs} sequences in order, "
               f"{reps} full passes) in {dt:.1f} s")
-    return done_bytes / dt / 1e9, sample, threads
+    return done_bytes / dt / 1e9, sample, threads, rows
 
 
 def e2e_measure(st, steps: int, device):
@@ -477,9 +491,15 @@ def run_ours(args):
     achieved = kv_bytes / (dec * 1e-3) / 1e9
     traffic = ncu_traffic(args.workload)
     cpu = None
+    parity = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, sample, cores = cpu_baseline(w)
+        v, sample, cores, rows = cpu_baseline(w)
         cpu = {"value": v, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample}
+        # the timed step's own output against the oracle rows the sample computed
+        got = st.out.float().cpu().numpy().astype(np.float64)
+        err = max(float(np.abs(got[s] - r).max()) for s, r in rows.items())
+        parity = {"max_abs_err": err, "sequences": len(rows),
+                  "tolerance": 4e-3 if w.dtype == "f16" else 1.6e-2, "ok": err <= (4e-3 if w.dtype == "f16" else 1.6e-2)}
     if rank != 0:
         return
     line = {
@@ -523,6 +543,8 @@ def run_ours(args):
                      "algorithmic_bytes_per_launch": kv_bytes, "decode_ms": dec,
                      "traffic": traffic},
         "cpu_baseline": cpu,
+        "parity_vs_oracle": parity,
+        "pool_utilisation": pool_utilisation(w),
         "gpu_launches": st.launches_per_step * args.steps,
         "clocks": clk.summary(),
     }
@@ -647,12 +669,12 @@ def prefill_cpu_baseline(w, rows=32):
         qs.append(qs[-1] + r)
     q = np.ascontiguousarray(w.q[idx])
     t0 = time.perf_counter()
-    oracle.prefill(q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens,
-                   np.array(qs, np.int32), w.scale, w.dtype, threads=threads)
+    ref = oracle.prefill(q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens,
+                         np.array(qs, np.int32), w.scale, w.dtype, threads=threads)
     dt = time.perf_counter() - t0
     sample = (f"fp64 oracle prefill of the last {rows} rows of each of the {w.num_seqs} chunks "
               f"({len(idx)} rows x {w.num_heads} heads) in {dt:.1f} s")
-    return prefill_flops(w, rows) / dt / 1e12, sample, threads
+    return prefill_flops(w, rows) / dt / 1e12, sample, threads, (idx, ref)
 
 
 def run_prefill(args):
@@ -731,9 +753,14 @@ def run_prefill(args):
         e2e_ms += e0.elapsed_time(e1)
     e2e_ms /= e2e_steps
     cpu = None
+    parity = None
     if not args.no_cpu_baseline:
-        cv, sample, cores = prefill_cpu_baseline(w)
+        cv, sample, cores, (idx, ref) = prefill_cpu_baseline(w)
         cpu = {"value": cv, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample}
+        got = out.float().cpu().numpy().astype(np.float64)[idx]
+        err = float(np.abs(got - ref).max())
+        tol = 4e-3 if w.dtype == "f16" else 1.6e-2
+        parity = {"max_abs_err": err, "rows": len(idx), "tolerance": tol, "ok": err <= tol}
     print(json.dumps({
         "metric": PREFILL_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": 1,
         "steps": steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
@@ -747,6 +774,7 @@ def run_prefill(args):
         "e2e": {"value": flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "cpu_baseline": cpu,
+        "parity_vs_oracle": parity,
         "clocks": clk.summary(),
         "gpu_launches": 2 * steps,
     }), flush=True)
@@ -805,7 +833,7 @@ def run_reference_prefill(args):
         return
     import synth
     w = synth.prefill_chunks()
-    vals = [prefill_cpu_baseline(w, rows=8) for _ in range(min(4, args.warmup + args.steps))]
+    vals = [prefill_cpu_baseline(w, rows=8)[:3] for _ in range(min(4, args.warmup + args.steps))]
     value, sample, cores = vals[-1]
     print(json.dumps({
         "impl": "reference", "metric": PREFILL_METRIC, "value": value, "unit": "TFLOP/s",
