@@ -382,16 +382,19 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
                     if (e > vis)
                         v[e >> 6][e & 63] = __float_as_uint(-INFINITY);
             }
-            // row maximum as a tree
+            // row maximum as a tree, three operands per instruction
             float mx[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-                mx[e] = fmaxf(__uint_as_float(v[0][e]), __uint_as_float(v[1][e]));
+            for (int a = 0; a < 8; ++a) {
+                auto x = [&](int i) { return __uint_as_float(v[i >> 6][i & 63]); };
+                float t = fmax3(x(a), x(a + 8), x(a + 16));
 #pragma unroll
-            for (int e = 8; e < 64; ++e)
-                mx[e & 7] = fmaxf(mx[e & 7], fmaxf(__uint_as_float(v[0][e]), __uint_as_float(v[1][e])));
-            float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+                for (int i = a + 24; i < 120; i += 16)
+                    t = fmax3(t, x(i), x(i + 8));
+                mx[a] = fmaxf(t, x(a + 120));
+            }
+            float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
+                             fmaxf(mx[6], mx[7]));
             mt *= sl2;                           // scale > 0: max commutes with it
             // running maximum, raised lazily: only when the tile's maximum
             // exceeds it by more than 8 (P stays below 2^8 otherwise)
@@ -406,20 +409,33 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
             }
             // P = 2^(scale*s - m) packed to the operand type, written into
             // TMEM over score columns already read: keys 0-63 -> columns
-            // 0-31, keys 64-127 -> 32-63
-            float sum[4] = {0.f, 0.f, 0.f, 0.f};
+            // 0-31, keys 64-127 -> 32-63.  Scale-and-subtract and the row sum
+            // run two values per instruction.
+            const uint64_t sl2x2 = f2_pack(sl2, sl2), nmx2 = f2_pack(-m, -m);
+            uint64_t sum2[4] = {0, 0, 0, 0};
 #pragma unroll
             for (int hb = 0; hb < 2; ++hb) {
                 uint32_t pw[32];
 #pragma unroll
                 for (int e = 0; e < 64; e += 2) {
-                    const float p0 = ex2_approx(fmaf(__uint_as_float(v[hb][e]), sl2, -m));
-                    const float p1 = ex2_approx(fmaf(__uint_as_float(v[hb][e + 1]), sl2, -m));
-                    sum[(e >> 1) & 3] += p0 + p1;
+                    float y0, y1;
+                    f2_unpack(f2_fma(f2_pack(__uint_as_float(v[hb][e]), __uint_as_float(v[hb][e + 1])),
+                                     sl2x2, nmx2),
+                              y0, y1);
+                    const float p0 = ex2_approx(y0);
+                    const float p1 = ex2_approx(y1);
+                    sum2[(e >> 1) & 3] = f2_add(sum2[(e >> 1) & 3], f2_pack(p0, p1));
                     pw[e / 2] = Mma<T>::pack(p0, p1);
                 }
                 __syncwarp();
                 tc::tmem_st32(tg + Sh::COL_S + 32 * hb, pw);
+            }
+            float sum[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                float a, b;
+                f2_unpack(sum2[q], a, b);
+                sum[q] = a + b;
             }
             l = fmaf(l, alpha, (sum[0] + sum[1]) + (sum[2] + sum[3]));
             // the tile that reaches the end of the sequence: value rows of
