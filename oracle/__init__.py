@@ -1,4 +1,5 @@
-"""fp64 CPU oracle for paged decode attention and the KV-pool kernels.
+"""fp64 CPU oracle for paged decode attention, chunked prefill over the same
+pool, and the KV-pool kernels.
 
 TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the
 benchmark's CPU-baseline leg are the only users.  The library never imports

@@ -1,6 +1,7 @@
 /*
- * oracle.c -- plain, slow, fp64 CPU reference for paged decode attention and
- * the two KV-pool maintenance operations.
+ * oracle.c -- plain, slow, fp64 CPU reference for paged decode attention,
+ * chunked-prefill attention over the same pool, and the KV-pool maintenance
+ * operations (slot scatter, block copy, swap between pools).
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing in the library calls this code; only the
  * tests, the smoke check and the benchmark's CPU-baseline leg load it.  It
@@ -22,9 +23,16 @@
  *   - Split-K over the sequence (FlashDecoding, ICML tutorial notes, section
  *     "内核优化"): a partition's partial result and the log-sum-exp merge of
  *     partials, each written as its plain definition.
+ *   - Chunked prefill (vLLM deep notes, section "调度优化：Continuous /
+ *     Chunked / Disaggregated"): the newest c tokens of a sequence of length
+ *     L are a chunk whose K/V are already in the pool; chunk row i sits at
+ *     position L - c + i and attends to positions 0 .. L - c + i, the same
+ *     single-row attention as a decode over that prefix.
  *
  * Layouts (shared with the library by convention, not by code):
  *   q        [num_seqs][num_heads][D]                 fp16/bf16 bits
+ *            (prefill: [total_rows][num_heads][D], chunks back to back,
+ *            query_start [num_seqs + 1] int32)
  *   k/v pool [num_blocks][num_kv_heads][16][D]         fp16/bf16 bits
  *   block_tables [num_seqs][max_blocks_per_seq] int32, seq_lens [num_seqs] int32
  *
