@@ -627,18 +627,24 @@ def run_swap(args):
 
 PREFILL_METRIC = ("paged chunked prefill: causal attention TFLOP/s on tcgen05 tensor cores, "
                   "% of GB300 dense bf16 peak")
-PREFILL_DESCRIPTION = ("chunked prefill: 8 seqs, 32/8 heads, head_dim 128, bf16, contexts "
-                       "U[512,4096] ending in a 512-token chunk (4096 query rows)")
+PREFILL_DESCRIPTION = {
+    "prefill": ("chunked prefill: 8 seqs, 32/8 heads, head_dim 128, bf16, contexts "
+                "U[512,4096] ending in a 512-token chunk (4096 query rows)"),
+    "prefill_long": ("chunked prefill deep into long prompts: 16 seqs, 32/8 heads, head_dim 128, "
+                     "bf16, 16384-token contexts ending in a 2048-token chunk (32768 query rows)"),
+}
 
 
-def measured_bf16_peak():
-    """(TFLOP/s, source) from MEASURED_PEAKS.json (cuBLAS bf16 burst), else the
-    recipe's fallback."""
+def measured_bf16_peak(sustained: bool):
+    """(TFLOP/s, source) from MEASURED_PEAKS.json: the cuBLAS bf16 burst figure
+    for a kernel timed alone, the sustained one (seconds under the power cap)
+    for a long timed region; else the fallbacks (1.9 / 1.7 PFLOP/s)."""
+    key = "bf16_tflops_sustained" if sustained else "bf16_tflops"
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
-            return float(json.load(f)["bf16_tflops"]), "measured"
+            return float(json.load(f)[key]), f"measured (MEASURED_PEAKS.json {key})"
     except Exception:
-        return 1900.0, "fallback"
+        return (1700.0 if sustained else 1900.0), "fallback"
 
 
 def prefill_flops(w, rows=None):
@@ -688,7 +694,7 @@ def run_prefill(args):
     pa.load()
     device = torch.device("cuda:0")
     torch.cuda.set_device(device)
-    w = synth.prefill_chunks()
+    w = synth.by_name(args.workload)
     tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float16
 
     def dev(a):
@@ -725,7 +731,9 @@ def run_prefill(args):
     ms = sum(e0.elapsed_time(e1) for e0, e1 in ev) / steps
     assert pa.get_device_error() == 0
     value = flops / (ms * 1e-3) / 1e12
-    peak, peak_src = measured_bf16_peak()
+    # a timed region of seconds runs under the power cap: compare it with the
+    # sustained peak, a short one with the burst peak
+    peak, peak_src = measured_bf16_peak(sustained=ms * steps > 500.0)
 
     # end to end through the public API: q, tables, lengths and query starts
     # from pinned host memory, the output back to it, every step
@@ -765,12 +773,13 @@ def run_prefill(args):
         "metric": PREFILL_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": 1,
         "steps": steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-        "config": {"workload": PREFILL_DESCRIPTION, "name": "prefill",
+        "config": {"workload": PREFILL_DESCRIPTION[args.workload], "name": args.workload,
                    "l2": "flushed (256 MB write) before every timed launch",
                    "flops": "causal: 4 * head_dim * heads * visible keys per row"},
         "roofline": {"bound": "tensor", "achieved": value, "peak": peak, "unit": "TFLOP/s",
                      "frac": value / peak, "traffic": None,
-                     "peak_source": peak_src + " (MEASURED_PEAKS.json bf16_tflops, cuBLAS burst)"},
+                     "peak_source": peak_src + ", cuBLAS bf16 GEMM",
+                     "timed_device_ms": ms * steps},
         "e2e": {"value": flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "cpu_baseline": cpu,
@@ -832,14 +841,14 @@ def run_reference_prefill(args):
     if rank != 0:
         return
     import synth
-    w = synth.prefill_chunks()
+    w = synth.by_name(args.workload)
     vals = [prefill_cpu_baseline(w, rows=8)[:3] for _ in range(min(4, args.warmup + args.steps))]
     value, sample, cores = vals[-1]
     print(json.dumps({
         "impl": "reference", "metric": PREFILL_METRIC, "value": value, "unit": "TFLOP/s",
         "n_gpus": world, "steps": len(vals), "warmup": 0, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": PREFILL_DESCRIPTION, "name": "prefill"},
+        "config": {"workload": PREFILL_DESCRIPTION[args.workload], "name": args.workload},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -853,7 +862,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=list(DESCRIPTION) + ["swap", "prefill"],
+    ap.add_argument("--workload", choices=list(DESCRIPTION) + ["swap", "prefill", "prefill_long"],
                     default="gqa8b")
     ap.add_argument("--partition", type=int, default=None,
                     help="-1 no split, 0 balanced split, >0 fixed partition tokens")
@@ -863,7 +872,7 @@ def main(argv=None):
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
-        if args.workload == "prefill":
+        if args.workload.startswith("prefill"):
             run_reference_prefill(args)
         elif args.workload == "swap":
             print(json.dumps({"impl": "reference", "unavailable": "swap_blocks moves bytes "
@@ -872,7 +881,7 @@ def main(argv=None):
             run_reference(args)
     elif args.workload == "swap":
         run_swap(args)
-    elif args.workload == "prefill":
+    elif args.workload.startswith("prefill"):
         run_prefill(args)
     else:
         run_ours(args)

@@ -434,6 +434,13 @@ def prefill_chunks(seed=1006):
     return build_prefill("prefill", 32, 8, 128, BF16, lens, np.full(8, 512), seed)
 
 
+def prefill_long(seed=1007):
+    """Chunked prefill deep into long prompts: 16 sequences, 32/8 heads,
+    head_dim 128, bf16; each 16384 tokens long, ending in a 2048-token chunk."""
+    return build_prefill("prefill_long", 32, 8, 128, BF16, np.full(16, 16384), np.full(16, 2048),
+                         seed)
+
+
 WORKLOADS = {
     "tiny": tiny,
     "mha7b": mha7b,
@@ -441,6 +448,7 @@ WORKLOADS = {
     "long": long,
     "parsamp": parsamp,
     "prefill": prefill_chunks,
+    "prefill_long": prefill_long,
 }
 
 
