@@ -1,4 +1,5 @@
-"""GB300 (sm_103a) paged KV cache: decode attention, reshape_and_cache, copy_blocks.
+"""GB300 (sm_103a) paged KV cache: decode attention, chunked prefill,
+reshape_and_cache, copy_blocks, swap_blocks.
 
 A thin ctypes binding over ``libpagedattn.so`` (the C ABI in
 ``include/pagedattn.h``).  Functions take torch CUDA tensors, pass their data
@@ -17,8 +18,9 @@ import threading
 
 __all__ = [
     "PagedAttnError", "load", "version", "decode", "decode_workspace_size", "workspace_for",
-    "decode_noalloc", "decode_append",
-    "reshape_and_cache", "copy_blocks", "swap_blocks", "gather_kv", "validate_tables", "get_device_error",
+    "decode_noalloc", "decode_append", "prefill", "prefill_workspace_size",
+    "reshape_and_cache", "copy_blocks", "swap_blocks", "gather_kv", "validate_tables",
+    "selftest_bounded_wait", "get_device_error",
     "PA_DTYPE_F16", "PA_DTYPE_BF16", "DEVERR", "STATUS",
 ]
 
@@ -122,6 +124,17 @@ def _stream(stream):
     return C.c_void_p(stream.cuda_stream)
 
 
+def _scratch(nbytes, device, stream):
+    """A uint8 scratch tensor for one call.  It is tied to the call's stream,
+    so the caching allocator does not hand its memory out again before the
+    kernels that use it have run."""
+    torch = _torch()
+    t = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    if stream is not None:
+        t.record_stream(stream)
+    return t
+
+
 def _check(fn: str, rc: int):
     if rc != 0:
         raise PagedAttnError(fn, rc)
@@ -141,15 +154,14 @@ def decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim, max_block
                                                max_blocks_per_seq, partition_size))
 
 
-def workspace_for(q, k_cache, block_tables, partition_size=0):
+def workspace_for(q, k_cache, block_tables, partition_size=0, stream=None):
     """A workspace tensor sized for pa_decode on these shapes (None when none is needed)."""
-    torch = _torch()
     n, hq, d = q.shape
     nbytes = decode_workspace_size(n, hq, k_cache.shape[1], d, block_tables.shape[1],
                                    partition_size)
     if nbytes == 0:
         return None
-    return torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    return _scratch(nbytes, q.device, stream)
 
 
 def decode(out, q, k_cache, v_cache, block_tables, seq_lens, scale, partition_size=0,
@@ -168,7 +180,7 @@ def decode(out, q, k_cache, v_cache, block_tables, seq_lens, scale, partition_si
     for t in (out, q, k_cache, v_cache, block_tables, seq_lens):
         _require(t.is_cuda and t.is_contiguous(), "tensors must be contiguous CUDA tensors")
     if workspace is None:
-        workspace = workspace_for(q, k_cache, block_tables, partition_size)
+        workspace = workspace_for(q, k_cache, block_tables, partition_size, stream)
     wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = load().pa_decode(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
                           _ptr(seq_lens), n, hq, hkv, d, bs, block_tables.shape[1], nb,
@@ -190,7 +202,7 @@ def decode_append(out, q, k_cache, v_cache, block_tables, seq_lens, k_new, v_new
     _require(k_new.shape == (n, hkv, d) and v_new.shape == k_new.shape and
              slot_mapping.shape == (n,), "new-token shapes")
     if workspace is None:
-        workspace = workspace_for(q, k_cache, block_tables, partition_size)
+        workspace = workspace_for(q, k_cache, block_tables, partition_size, stream)
     wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = load().pa_decode_append(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
                                  _ptr(block_tables), _ptr(seq_lens), _ptr(k_new), _ptr(v_new),
@@ -225,8 +237,7 @@ def prefill(out, q, k_cache, v_cache, block_tables, seq_lens, query_start, max_q
         _require(x.is_cuda and x.is_contiguous(), "tensors must be contiguous CUDA tensors")
     if isinstance(workspace, str):
         nbytes = prefill_workspace_size(n, int(max_query_len), hq, hkv)
-        workspace = (_torch().empty(nbytes, dtype=_torch().uint8, device=q.device)
-                     if nbytes else None)
+        workspace = _scratch(nbytes, q.device, stream) if nbytes else None
     wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = load().pa_prefill(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
                            _ptr(seq_lens), _ptr(query_start), n, int(max_query_len), hq, hkv, d,
