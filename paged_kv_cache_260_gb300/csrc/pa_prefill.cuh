@@ -30,8 +30,9 @@
 //             issued once P_g,j . V_j has completed; the two groups
 //             alternate on the tensor core (one group's softmax runs while
 //             the other group's MMAs do);
-//   warps 2-5 group 0, warps 6-9 group 1: one thread per row (its TMEM
-//             lane): scores from TMEM, causal mask, online softmax in base 2
+//   warps 2-5 group 0, warps 6-9 group 1: first load the Q tiles into
+//             shared memory (while the producer's first K/V copies are in
+//             flight); then one thread per row (its TMEM lane): scores from TMEM, causal mask, online softmax in base 2
 //             with a lazy rescale of O (only when the running maximum grows
 //             by more than 2^8), P into TMEM, and the final O / l written out.
 // TMEM (512 columns): group g uses [256g, 256g + 128) for S (P packed two
@@ -62,8 +63,8 @@ struct PrefillShape {
     static constexpr int NSLOT = (227 * 1024 - 1024 - NG * Q_BYTES) / SLOT_BYTES;   // K/V ring
     static constexpr int OFF_SLOT = NG * Q_BYTES;
     static constexpr int DATA = OFF_SLOT + NSLOT * SLOT_BYTES;   // 1024-aligned operand region
-    // full[NSLOT] empty[NSLOT] s[2] p[2] o[2] drain, then TMEM base and abort flag
-    static constexpr int NBAR = 2 * NSLOT + 3 * NG + 1;
+    // full[NSLOT] empty[NSLOT] s[2] p[2] o[2] drain q, then TMEM base and abort flag
+    static constexpr int NBAR = 2 * NSLOT + 3 * NG + 2;
     static constexpr int BAR_BYTES = NBAR * 8 + 8;
     // The operand region is aligned up to 1024 bytes inside the dynamic
     // allocation; the barriers sit in whichever end of the 1024-byte slack
@@ -104,6 +105,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
     auto p_bar = [&](int g) { return bar_addr + 8u * (2 * NS + Sh::NG + g); };
     auto o_bar = [&](int g) { return bar_addr + 8u * (2 * NS + 2 * Sh::NG + g); };
     const uint32_t drain_bar = bar_addr + 8u * (2 * NS + 3 * Sh::NG);
+    const uint32_t q_bar = drain_bar + 8u;        // the Q tiles are in shared memory
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + Sh::NBAR * 8);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -168,6 +170,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
             mbar_init(o_bar(g), 1);
         }
         mbar_init(drain_bar, 1);
+        mbar_init(q_bar, Sh::NG * 128);
         *abort_flag = 0;
         mbar_init_fence();
     }
@@ -176,27 +179,8 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
         tc::tmem_relinquish();
     }
 
-    // ---- Q tiles -> shared memory, K-major with the 128-byte swizzle -------
-    // row rr of group g = (token t0 + g*TPG + rr / G, q head h*G + rr % G);
-    // rows past the chunk and the rows 128 - TPG*G that do not fill a token
-    // are zero
-    {
-        constexpr int CPR = D / 8;                // 16-byte chunks per row
-        const T *qg = reinterpret_cast<const T *>(p.q);
-        for (int idx = tid; idx < Sh::NG * Sh::BM * CPR; idx += Sh::THREADS) {
-            const int r = idx / CPR, ch = idx % CPR;
-            const int g = r / Sh::BM, rr = r % Sh::BM;
-            const int tok = g * TPG + rr / G, hg = rr % G;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (rr < TPG * G && t0 + tok < c)
-                v = __ldg(reinterpret_cast<const uint4 *>(
-                    qg + ((size_t)(qs + t0 + tok) * Hq + h * G + hg) * D + ch * 8));
-            const int hf = ch >> 3, c8 = ch & 7;
-            *reinterpret_cast<uint4 *>(smem + g * Sh::Q_BYTES + hf * (Sh::BM * 128) + rr * 128 +
-                                       ((c8 ^ (rr & 7)) << 4)) = v;
-        }
-    }
-    fence_proxy_async_shared();
+    // the barriers and the TMEM base are visible to every thread; the Q
+    // tiles are loaded by the softmax warps while K/V stream in
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
@@ -324,7 +308,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
                 tc::commit_warp(empty_bar(sl));
             return true;
         };
-        bool ok = true;
+        bool ok = wait_all(q_bar, 0);
         for (int g = 0; ok && g < Sh::NG; ++g)
             ok = issue_s(g, 0);
         for (int j = 0; ok && j < nt; ++j) {
@@ -346,6 +330,43 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
         if (!wait_all(drain_bar, 0) && lane == 0)
             give_up();
     } else {
+        // ---------------- Q tiles -> shared memory ----------------
+        // K-major with the 128-byte swizzle.  Row rr of group g = (token
+        // t0 + g*TPG + rr / G, q head h*G + rr % G); rows past the chunk and
+        // the rows 128 - TPG*G that do not fill a token are zero.  Thread lt
+        // takes 16-byte chunk lt % CPR of every (NG*128 / CPR)-th row, all its
+        // loads in flight at once, and the MMA warp waits on q_bar.
+        {
+            constexpr int CPR = D / 8;            // 16-byte chunks per row
+            constexpr int RSTEP = Sh::NG * 128 / CPR;
+            constexpr int NPT = Sh::NG * Sh::BM / RSTEP;
+            const T *qg = reinterpret_cast<const T *>(p.q);
+            const int lt = tid - 64, ch = lt % CPR, hf = ch >> 3, c8 = ch & 7;
+            uint4 qv[NPT];
+#pragma unroll
+            for (int i = 0; i < NPT; ++i) {
+                const int r = lt / CPR + i * RSTEP;
+                const int g = r / Sh::BM, rr = r % Sh::BM;
+                const int tok = g * TPG + rr / G, hg = rr % G;
+                qv[i] = make_uint4(0, 0, 0, 0);
+                if (rr < TPG * G && t0 + tok < c)
+                    qv[i] = __ldg(reinterpret_cast<const uint4 *>(
+                        qg + ((size_t)(qs + t0 + tok) * Hq + h * G + hg) * D + ch * 8));
+            }
+#pragma unroll
+            for (int i = 0; i < NPT; ++i) {
+                const int r = lt / CPR + i * RSTEP;
+                const int g = r / Sh::BM, rr = r % Sh::BM;
+                *reinterpret_cast<uint4 *>(smem + g * Sh::Q_BYTES + hf * (Sh::BM * 128) +
+                                           rr * 128 + ((c8 ^ (rr & 7)) << 4)) = qv[i];
+            }
+            fence_proxy_async_shared();
+            mbar_arrive(q_bar);
+        }
+        static_assert(Sh::THREADS == 64 + Sh::NG * 128 && (Sh::NG * 128) % (D / 8) == 0 &&
+                          (Sh::NG * Sh::BM) % (Sh::NG * 128 / (D / 8)) == 0,
+                      "Q chunks divide evenly over the softmax warps");
+
         // ---------------- softmax: one thread per row of its group ----------
         const int grp = (warp - 2) >> 2;
         const int q4 = warp & 3;                   // TMEM lane quarter of this warp
@@ -560,41 +581,62 @@ prefill_plan_kernel(const PrefillParams p, int tpb, int bn, uint32_t *plan, int 
         const int t_end = min((t + 1) * tpb, c);
         return min((L - c + t_end - 1) / bn + 1, kPlanBuckets - 1);
     };
+    // pass 1: histogram of the counts; a thread keeps its first sequence's
+    // tiles in registers for pass 2 (every sequence when num_seqs <= 1024)
+    int L0 = 0, c0 = 0, first0 = 0, nq0 = 0;
     for (int s = tid; s < p.num_seqs; s += 1024) {
         int L, c, first;
         const int nq = tiles(s, true, L, c, first);
+        if (s == tid) {
+            L0 = L;
+            c0 = c;
+            first0 = first;
+            nq0 = nq;
+        }
         for (int t = first; t < nq; ++t)
             atomicAdd(&hist[bucket(L, c, t)], 1);
     }
     __syncthreads();
-    // start of each bucket in descending order: lane l scans buckets
-    // [B - 64(l+1), B - 64 l) from the top, then a warp scan joins the lanes
-    if (tid < 32) {
-        constexpr int PER = kPlanBuckets / 32;
-        const int hi = kPlanBuckets - lane * PER;
-        int local = 0;
-        for (int b = hi - 1; b >= hi - PER; --b)
-            local += hist[b];
-        int incl = local;
+    // start of each bucket in descending order of the count: thread t owns
+    // buckets B-1-2t and B-2-2t; warp scans, then a scan of the warp totals
+    {
+        __shared__ int warp_sum[32];
+        static_assert(kPlanBuckets == 2 * 1024, "two buckets per thread");
+        const int hi = kPlanBuckets - 1 - 2 * tid;
+        const int n0 = hist[hi], n1 = hist[hi - 1];
+        int incl = n0 + n1;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int y = __shfl_up_sync(0xffffffffu, incl, o);
             if (lane >= o)
                 incl += y;
         }
-        int run = incl - local;
-        for (int b = hi - 1; b >= hi - PER; --b) {
-            const int n = hist[b];
-            hist[b] = run;
-            run += n;
-        }
         if (lane == 31)
-            *count = incl;
+            warp_sum[tid >> 5] = incl;
+        __syncthreads();
+        if (tid < 32) {
+            const int own = warp_sum[lane];
+            int w = own;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, w, o);
+                if (lane >= o)
+                    w += y;
+            }
+            warp_sum[lane] = w - own;            // exclusive
+            if (lane == 31)
+                *count = w;
+        }
+        __syncthreads();
+        const int start = warp_sum[tid >> 5] + incl - (n0 + n1);
+        hist[hi] = start;
+        hist[hi - 1] = start + n0;
     }
     __syncthreads();
     for (int s = tid; s < p.num_seqs; s += 1024) {
-        int L, c, first;
-        const int nq = tiles(s, false, L, c, first);
+        int L = L0, c = c0, first = first0, nq = nq0;
+        if (s != tid)
+            nq = tiles(s, false, L, c, first);
         for (int t = first; t < nq; ++t)
             plan[atomicAdd(&hist[bucket(L, c, t)], 1)] = ((uint32_t)s << 16) | (uint32_t)t;
     }
