@@ -63,8 +63,8 @@ struct PrefillShape {
     static constexpr int NSLOT = (227 * 1024 - 1024 - NG * Q_BYTES) / SLOT_BYTES;   // K/V ring
     static constexpr int OFF_SLOT = NG * Q_BYTES;
     static constexpr int DATA = OFF_SLOT + NSLOT * SLOT_BYTES;   // 1024-aligned operand region
-    // full[NSLOT] empty[NSLOT] s[2] p[2] o[2] drain q, then TMEM base and abort flag
-    static constexpr int NBAR = 2 * NSLOT + 3 * NG + 2;
+    // full[NSLOT] empty[NSLOT] s[2] p[2] o[2] drain q[2], then TMEM base and abort flag
+    static constexpr int NBAR = 2 * NSLOT + 4 * NG + 1;
     static constexpr int BAR_BYTES = NBAR * 8 + 8;
     // The operand region is aligned up to 1024 bytes inside the dynamic
     // allocation; the barriers sit in whichever end of the 1024-byte slack
@@ -105,7 +105,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
     auto p_bar = [&](int g) { return bar_addr + 8u * (2 * NS + Sh::NG + g); };
     auto o_bar = [&](int g) { return bar_addr + 8u * (2 * NS + 2 * Sh::NG + g); };
     const uint32_t drain_bar = bar_addr + 8u * (2 * NS + 3 * Sh::NG);
-    const uint32_t q_bar = drain_bar + 8u;        // the Q tiles are in shared memory
+    auto q_bar = [&](int g) { return drain_bar + 8u * (1 + g); };   // Q_g is in shared memory
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + Sh::NBAR * 8);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -170,7 +170,8 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
             mbar_init(o_bar(g), 1);
         }
         mbar_init(drain_bar, 1);
-        mbar_init(q_bar, Sh::NG * 128);
+        for (int g = 0; g < Sh::NG; ++g)
+            mbar_init(q_bar(g), Sh::NG * 128);
         *abort_flag = 0;
         mbar_init_fence();
     }
@@ -308,9 +309,9 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
                 tc::commit_warp(empty_bar(sl));
             return true;
         };
-        bool ok = wait_all(q_bar, 0);
+        bool ok = true;
         for (int g = 0; ok && g < Sh::NG; ++g)
-            ok = issue_s(g, 0);
+            ok = wait_all(q_bar(g), 0) && issue_s(g, 0);
         for (int j = 0; ok && j < nt; ++j) {
             if (__any_sync(FULL, *abort_flag != 0)) {
                 ok = false;
@@ -334,12 +335,15 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
         // K-major with the 128-byte swizzle.  Row rr of group g = (token
         // t0 + g*TPG + rr / G, q head h*G + rr % G); rows past the chunk and
         // the rows 128 - TPG*G that do not fill a token are zero.  Thread lt
-        // takes 16-byte chunk lt % CPR of every (NG*128 / CPR)-th row, all its
-        // loads in flight at once, and the MMA warp waits on q_bar.
+        // takes 16-byte chunk lt % CPR of every (NG*128 / CPR)-th row, group
+        // 0's rows first, with all its loads in flight at once; it arrives on
+        // q_bar(g) once its rows of group g are stored, and the MMA warp
+        // issues S_g,0 after that barrier.
         {
             constexpr int CPR = D / 8;            // 16-byte chunks per row
             constexpr int RSTEP = Sh::NG * 128 / CPR;
             constexpr int NPT = Sh::NG * Sh::BM / RSTEP;
+            constexpr int PER_G = NPT / Sh::NG;   // a thread's chunks in each group
             const T *qg = reinterpret_cast<const T *>(p.q);
             const int lt = tid - 64, ch = lt % CPR, hf = ch >> 3, c8 = ch & 7;
             uint4 qv[NPT];
@@ -359,13 +363,18 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
                 const int g = r / Sh::BM, rr = r % Sh::BM;
                 *reinterpret_cast<uint4 *>(smem + g * Sh::Q_BYTES + hf * (Sh::BM * 128) +
                                            rr * 128 + ((c8 ^ (rr & 7)) << 4)) = qv[i];
+                if (i % PER_G == PER_G - 1) {
+                    fence_proxy_async_shared();
+                    mbar_arrive(q_bar(i / PER_G));
+                }
             }
-            fence_proxy_async_shared();
-            mbar_arrive(q_bar);
         }
         static_assert(Sh::THREADS == 64 + Sh::NG * 128 && (Sh::NG * 128) % (D / 8) == 0 &&
                           (Sh::NG * Sh::BM) % (Sh::NG * 128 / (D / 8)) == 0,
                       "Q chunks divide evenly over the softmax warps");
+        static_assert((Sh::BM * (D / 8)) % (Sh::NG * 128) == 0 &&
+                          Sh::BM % (Sh::NG * 128 / (D / 8)) == 0,
+                      "each thread's chunks of a group are consecutive in its loop");
 
         // ---------------- softmax: one thread per row of its group ----------
         const int grp = (warp - 2) >> 2;
