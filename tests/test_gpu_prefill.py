@@ -235,3 +235,40 @@ def test_prefill_long_prompt_sampled_rows(pa):
             ref = oracle.decode(w.q[row][None], w.k_cache, w.v_cache, w.block_tables[s][None],
                                 np.array([p + 1], np.int32), w.scale, w.dtype)
             assert float(np.abs(got[row] - ref[0]).max()) <= TOL["f16"], (s, i)
+
+
+
+@pytest.mark.parametrize("dt,every,step", [("bf16", 64, 10.0), ("bf16", 128, 6.5), ("f16", 64, 10.0)])
+def test_prefill_scores_that_keep_growing(pa, dt, every, step):
+    # Every query row leans along one direction u, and every `every`-th key
+    # (at offset 37, so the spikes fall in both halves of 128-key tiles when
+    # every = 64) lies along u with a length that raises its score by about
+    # `step` natural-log units over the previous spike.  Each row's running
+    # maximum therefore keeps rising past the kernel's lazy-rescale
+    # threshold (2^8), inside tiles and at their boundaries, and the result
+    # depends on the rescale of O, of the row sum and of P already written.
+    # The keys are aligned with the queries, so the large scores carry no
+    # cancellation; V is scaled by 1/4 so that |O| stays near 1 and the
+    # dtype's tolerance (derived for outputs of that size) applies.
+    w = synth.build_prefill("pf", 8, 2, 128, dt, [700, 300, 1000, 129], [300, 300, 200, 129],
+                            seed=77, poison=True)
+    rng = np.random.default_rng(78)
+    d = w.head_dim
+    u = rng.standard_normal(d)
+    u /= np.linalg.norm(u)
+    beta = 3.0
+    q = dev_bits(w.q, dt, device="cpu").float().numpy() + (beta * u).astype(np.float32)
+    w.q = synth.to_bits(q, dt)
+    k = dev_bits(w.k_cache, dt, device="cpu").float().numpy()
+    v = dev_bits(w.v_cache, dt, device="cpu").float().numpy()
+    for s in range(w.num_seqs):
+        for p in range(int(w.seq_lens[s])):
+            b, r = w.block_tables[s, p // 16], p % 16
+            v[b, :, r, :] *= 0.25
+            if p % every == 37 % every:
+                target = 4.0 + step * (p // every)          # score of the spike, natural log units
+                k[b, :, r, :] = (target / (beta * w.scale) * u).astype(np.float32)
+    w.k_cache, w.v_cache = synth.to_bits(k, dt), synth.to_bits(v, dt)
+    out = _run(pa, w)
+    assert pa.get_device_error() == 0
+    assert max_err(out, _ref(w)) <= TOL[dt]
