@@ -272,3 +272,29 @@ def test_prefill_scores_that_keep_growing(pa, dt, every, step):
     out = _run(pa, w)
     assert pa.get_device_error() == 0
     assert max_err(out, _ref(w)) <= TOL[dt]
+
+
+HEADS = [(8, 8), (16, 8), (24, 8), (32, 8), (40, 8), (12, 4), (64, 4), (32, 2), (16, 1)]
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_prefill_random_shapes(pa, seed):
+    # seeded sweep: head layout (G = 1, 2, 3, 4, 5, 16), head size, dtype,
+    # 1-5 sequences of 1-700 tokens whose chunk is empty, one token, the whole
+    # prompt or a random length; NaN-poisoned pools
+    rng = np.random.default_rng(900 + seed)
+    hq, hkv = HEADS[rng.integers(len(HEADS))]
+    d = int(rng.choice([64, 128]))
+    dt = str(rng.choice(["f16", "bf16"]))
+    n = int(rng.integers(1, 6))
+    lens = rng.integers(1, 701, size=n)
+    lens[rng.random(n) < 0.2] = rng.integers(1, 17)          # some sequences shorter than a block
+    kind = rng.integers(0, 4, size=n)
+    chunks = np.where(kind == 0, 0, np.where(kind == 1, 1, np.where(kind == 2, lens,
+                                                                     rng.integers(1, lens + 1))))
+    if chunks.sum() == 0:
+        chunks[0] = lens[0]
+    w = synth.build_prefill("pf", hq, hkv, d, dt, lens, chunks, seed=1000 + seed, poison=True)
+    out = _run(pa, w)
+    assert pa.get_device_error() == 0
+    assert max_err(out, _ref(w)) <= TOL[dt], (hq, hkv, d, dt, lens.tolist(), chunks.tolist())
