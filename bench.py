@@ -328,13 +328,14 @@ def pool_utilisation(w):
             "table_tokens": int(w.seq_lens.sum())}
 
 
-def cpu_baseline(w, budget_s: float = 12.0):
+def cpu_baseline(w, budget_s: float = 12.0, threads: int = 0):
     """The fp64 oracle on a bounded sample: whole sequences in order, repeated
-    until ~budget_s of CPU work; returns (GB/s of KV processed, sample text,
-    cores, {sequence: oracle output row} of the first pass)."""
+    until ~budget_s of CPU work, on `threads` host threads (0: all cores);
+    returns (GB/s of KV processed, sample text, cores, {sequence: oracle
+    output row} of the first pass)."""
     import oracle
     oracle.build()
-    threads = oracle.num_threads()
+    threads = threads or oracle.num_threads()
     k, v = w.k_cache.copy(), w.v_cache.copy()
     t0 = time.perf_counter()
     if w.block_mapping is not None and len(w.block_mapping):
@@ -495,6 +496,9 @@ def run_ours(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, sample, cores, rows = cpu_baseline(w)
         cpu = {"value": v, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample}
+        if args.workload == "tiny":
+            v1, sample1, _, _ = cpu_baseline(w, budget_s=3.0, threads=1)
+            cpu["single_core"] = {"value": v1, "unit": "GB/s", "cores": 1, "sample": sample1}
         # the timed step's own output against the oracle rows the sample computed
         got = st.out.float().cpu().numpy().astype(np.float64)
         err = max(float(np.abs(got[s] - r).max()) for s, r in rows.items())
