@@ -9,6 +9,7 @@
 
 #include "pa_cache.h"
 #include "pa_internal.h"
+#include "pa_prefill_abi.h"
 #include "pa_schedule.cuh"
 #include "pagedattn.h"
 

@@ -70,44 +70,6 @@ constexpr int kMaxSeqs = 8192;        // per-sequence arrays live in shared memo
 constexpr int kMaxWarpsPerSM = 16;    // decode workers <= SMs * this (workspace sizing)
 constexpr int kMinTiles = 8;          // balanced mode: least tiles per thread block
 
-// Chunked prefill: the newest chunk_s = query_start[s+1] - query_start[s]
-// tokens of sequence s (already in the pool) attend causally to positions
-// [0, own position] of the sequence.
-struct PrefillParams {
-    void *out;                     // [total_q][num_heads][head_dim]
-    const void *q;                 // [total_q][num_heads][head_dim]
-    const int32_t *block_tables;
-    const int32_t *seq_lens;
-    const int32_t *query_start;    // [num_seqs + 1]
-    uint32_t *err;
-    int num_seqs;
-    int num_heads;
-    int num_kv_heads;
-    int max_blocks;
-    int num_blocks;
-    int q_ranks;                   // query tiles per (sequence, kv head) in the grid
-    float scale_log2;
-    // optional work order (a planning kernel writes it): block b computes
-    // pair plan[b / num_kv_heads] = (sequence << 16 | query tile), for
-    // b / num_kv_heads < *plan_count, heaviest pairs first; null: the grid
-    // is walked as (query tile from the end, sequence, kv head)
-    const uint32_t *plan;
-    const int *plan_count;
-};
-
-struct PrefillKernel {
-    const void *fn;
-    int threads;
-    size_t smem;
-    const void *plan_fn;           // prefill_plan_kernel: (PrefillParams, tokens per block,
-                                   // keys per tile, uint32_t *plan, int *count)
-};
-
-bool prefill_kernel(int dtype, int head_dim, PrefillKernel *k);
-constexpr int kPrefillRows = 128;   // (token, head) rows of one prefill query tile
-constexpr int kPrefillTiles = 2;    // query tiles of one prefill thread block
-constexpr int kPrefillKeys = 128;   // keys per prefill key tile
-
 bool decode_kernels_f16(int head_dim, int group, KernelSet *ks);
 bool decode_kernels_bf16(int head_dim, int group, KernelSet *ks);
 

@@ -46,6 +46,7 @@
 #include <type_traits>
 
 #include "pa_device.cuh"
+#include "pa_prefill_abi.h"
 #include "pa_tcgen05.cuh"
 
 namespace pa {

@@ -1,0 +1,49 @@
+// pa_prefill_abi.h -- what the host side of pa_prefill shares with the
+// prefill kernels: their parameters, the launch descriptor and the tile
+// sizes.  Kept apart from the decode's declarations.
+#pragma once
+
+#include <stddef.h>
+#include <stdint.h>
+
+namespace pa {
+
+// Chunked prefill: the newest chunk_s = query_start[s+1] - query_start[s]
+// tokens of sequence s (already in the pool) attend causally to positions
+// [0, own position] of the sequence.
+struct PrefillParams {
+    void *out;                     // [total_q][num_heads][head_dim]
+    const void *q;                 // [total_q][num_heads][head_dim]
+    const int32_t *block_tables;
+    const int32_t *seq_lens;
+    const int32_t *query_start;    // [num_seqs + 1]
+    uint32_t *err;
+    int num_seqs;
+    int num_heads;
+    int num_kv_heads;
+    int max_blocks;
+    int num_blocks;
+    int q_ranks;                   // query tiles per (sequence, kv head) in the grid
+    float scale_log2;
+    // optional work order (a planning kernel writes it): block b computes
+    // pair plan[b / num_kv_heads] = (sequence << 16 | query tile), for
+    // b / num_kv_heads < *plan_count, heaviest pairs first; null: the grid
+    // is walked as (query tile from the end, sequence, kv head)
+    const uint32_t *plan;
+    const int *plan_count;
+};
+
+struct PrefillKernel {
+    const void *fn;
+    int threads;
+    size_t smem;
+    const void *plan_fn;           // prefill_plan_kernel: (PrefillParams, tokens per block,
+                                   // keys per tile, uint32_t *plan, int *count)
+};
+
+bool prefill_kernel(int dtype, int head_dim, PrefillKernel *k);
+constexpr int kPrefillRows = 128;   // (token, head) rows of one prefill query tile
+constexpr int kPrefillTiles = 2;    // query tiles of one prefill thread block
+constexpr int kPrefillKeys = 128;   // keys per prefill key tile
+
+}  // namespace pa
