@@ -298,3 +298,27 @@ def test_prefill_random_shapes(pa, seed):
     out = _run(pa, w)
     assert pa.get_device_error() == 0
     assert max_err(out, _ref(w)) <= TOL[dt], (hq, hkv, d, dt, lens.tolist(), chunks.tolist())
+
+
+def test_prefill_on_two_streams(pa):
+    # two different prefills in flight on two side streams, each with its
+    # own automatically allocated work-order workspace
+    ws = [synth.build_prefill("pf", 16, 4, 128, "bf16", [700, 300], [400, 300], seed=31, poison=True),
+          synth.build_prefill("pf", 8, 8, 64, "f16", [90, 1000, 17], [90, 64, 17], seed=32, poison=True)]
+    outs, streams = [], [torch.cuda.Stream(), torch.cuda.Stream()]
+    args = []
+    for w in ws:
+        q = dev_bits(w.q, w.dtype)
+        args.append((q, dev_bits(w.k_cache, w.dtype), dev_bits(w.v_cache, w.dtype),
+                     torch.from_numpy(w.block_tables).cuda(), torch.from_numpy(w.seq_lens).cuda(),
+                     torch.from_numpy(w.query_start).cuda(), int(np.diff(w.query_start).max())))
+        outs.append(torch.full_like(q, float("nan")))
+    torch.cuda.synchronize()
+    for w, s, out, (q, k, v, t, lens, qs, mq) in zip(ws, streams, outs, args):
+        with torch.cuda.stream(s):
+            pa.prefill(out, q, k, v, t, lens, qs, mq, w.scale, stream=s)
+    for s in streams:
+        s.synchronize()
+    assert pa.get_device_error() == 0
+    for w, out in zip(ws, outs):
+        assert max_err(out, _ref(w)) <= TOL[w.dtype]
