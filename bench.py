@@ -133,23 +133,32 @@ def measured_hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def decode_source_hash() -> str:
-    """Hash of the decode kernel sources: ncu counters apply only to this build."""
+DECODE_SOURCES = ("pa_decode_mma.cuh", "pa_schedule.cuh", "pa_device.cuh", "pa_internal.h")
+PREFILL_SOURCES = ("pa_prefill.cuh", "pa_prefill_abi.h", "pa_tcgen05.cuh", "pa_device.cuh")
+
+
+def source_hash(names=DECODE_SOURCES) -> str:
+    """Hash of a kernel's sources: ncu counters apply only to this build."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_cache_260_gb300", "csrc")
-    for name in ("pa_decode_mma.cuh", "pa_schedule.cuh", "pa_device.cuh", "pa_internal.h"):
+    for name in names:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(workload: str):
-    """DRAM bytes per decode launch from the committed ncu summary, if it was
-    taken on the current kernel sources (else None)."""
-    path = os.path.join(ROOT, "profiles", "decode_dram_traffic.txt")
+def decode_source_hash() -> str:
+    return source_hash(DECODE_SOURCES)
+
+
+def ncu_traffic(workload: str, table: str = "decode_dram_traffic.txt", names=DECODE_SOURCES):
+    """DRAM bytes per launch of the workload's dominant kernel from the
+    committed ncu summary, if it was taken on the current kernel sources
+    (else None)."""
+    path = os.path.join(ROOT, "profiles", table)
     if not os.path.exists(path):
         return None
-    src = decode_source_hash()
+    src = source_hash(names)
     for line in open(path):
         parts = line.split()
         if len(parts) >= 3 and not line.startswith("#") and parts[0] == workload and parts[1] == src:
@@ -781,7 +790,9 @@ def run_prefill(args):
                    "l2": "flushed (256 MB write) before every timed launch",
                    "flops": "causal: 4 * head_dim * heads * visible keys per row"},
         "roofline": {"bound": "tensor", "achieved": value, "peak": peak, "unit": "TFLOP/s",
-                     "frac": value / peak, "traffic": None,
+                     "frac": value / peak,
+                     "traffic": ncu_traffic(args.workload, "prefill_dram_traffic.txt",
+                                            PREFILL_SOURCES),
                      "peak_source": peak_src + ", cuBLAS bf16 GEMM",
                      "timed_device_ms": ms * steps},
         "e2e": {"value": flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
