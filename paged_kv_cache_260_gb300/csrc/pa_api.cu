@@ -27,6 +27,7 @@ struct DeviceState {
     int num_sms = 0;
     uint32_t *err = nullptr;   // device address of g_device_error
     size_t smem_optin = 0;     // largest dynamic shared memory per block
+    long long l2_bytes = 0;    // L2 cache size
 };
 
 std::mutex g_mutex;
@@ -65,6 +66,10 @@ int device_state(DeviceState **out)
         if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
             cudaSuccess)
             return PA_ERR_CUDA;
+        int l2 = 0;
+        if (cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess)
+            return PA_ERR_CUDA;
+        st.l2_bytes = l2;
         void *addr = nullptr;
         if (cudaGetSymbolAddress(&addr, g_device_error) != cudaSuccess)
             return PA_ERR_CUDA;
@@ -555,7 +560,11 @@ int pa_prefill(void *out, const void *q, const void *k_cache, const void *v_cach
         p.plan = plan;
         p.plan_count = count;
         int tpb = kPrefillTiles * (kPrefillRows / group), bn = kPrefillKeys;
-        void *pargs[] = {&p, &tpb, &bn, &plan, &count};
+        // K and V bytes a token holds over all kv heads, and the L2 size: the
+        // plan keeps each sequence's tiles together when the batch's K/V
+        // does not fit in L2
+        long long kv_bytes_per_token = 2LL * num_kv_heads * head_dim * 2, l2_bytes = ds->l2_bytes;
+        void *pargs[] = {&p, &tpb, &bn, &plan, &count, &kv_bytes_per_token, &l2_bytes};
         rc = cuda_status(cudaLaunchKernel(kk.plan_fn, dim3(1), dim3(1024), pargs, 0, st));
         if (rc != PA_OK)
             return rc;

@@ -545,23 +545,38 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
 }
 
 // ---------------------------------------------------------------------------
-// Work order of a prefill: the (sequence, query tile) pairs sorted by their
-// key-tile count, heaviest first (a counting sort on the count, one block).
-// The hardware hands thread blocks to SMs in index order as SMs free up, so
-// blocks that walk this order give the greedy longest-first schedule, and
-// the run ends on the lightest pairs.  Pairs of one count keep no particular
-// order (their results do not depend on it).
+// Work order of a prefill, one block.  The hardware hands thread blocks to
+// SMs in index order as SMs free up, and block b computes pair plan[b / Hkv]
+// for kv head b % Hkv, so the order decides both the schedule and what the
+// blocks running at the same time share:
+//  * the (sequence, query tile) pairs sorted by their key-tile count,
+//    heaviest first (a counting sort on the count): the greedy
+//    longest-first schedule, ending on the lightest pairs.  Used when the
+//    batch's K/V fits in L2, so any blocks may run side by side;
+//  * otherwise sequence by sequence, the sequences ordered by their heaviest
+//    tile and each sequence's tiles heaviest first.  The blocks running at
+//    one time then work on few sequences and stream the same K/V prefix, so
+//    L2 serves most of it instead of DRAM.
+// Pairs of one count keep no particular order (their results do not depend
+// on it).
 // ---------------------------------------------------------------------------
 constexpr int kPlanBuckets = 2048;   // key-tile counts above this share the top bucket
 
 __global__ void __launch_bounds__(1024)
-prefill_plan_kernel(const PrefillParams p, int tpb, int bn, uint32_t *plan, int *count)
+prefill_plan_kernel(const PrefillParams p, int tpb, int bn, uint32_t *plan, int *count,
+                    long long kv_bytes_per_token, long long l2_bytes)
 {
-    __shared__ int hist[kPlanBuckets];
+    __shared__ int hist_tile[kPlanBuckets];  // pairs per key-tile count
+    __shared__ int hist_seq[kPlanBuckets];   // pairs of the sequences whose heaviest tile has it
+    __shared__ unsigned long long tokens;
     const int tid = threadIdx.x, lane = tid & 31;
     grid_dependents_launch();                // the prefill may be scheduled; it waits for us
-    for (int i = tid; i < kPlanBuckets; i += 1024)
-        hist[i] = 0;
+    for (int i = tid; i < kPlanBuckets; i += 1024) {
+        hist_tile[i] = 0;
+        hist_seq[i] = 0;
+    }
+    if (tid == 0)
+        tokens = 0;
     __syncthreads();
     // the query tiles of sequence s that run: [first, last); errors reported once
     auto tiles = [&](int s, bool report, int &L, int &c, int &first) {
@@ -591,9 +606,11 @@ prefill_plan_kernel(const PrefillParams p, int tpb, int bn, uint32_t *plan, int 
         const int t_end = min((t + 1) * tpb, c);
         return min((L - c + t_end - 1) / bn + 1, kPlanBuckets - 1);
     };
-    // pass 1: histogram of the counts; a thread keeps its first sequence's
-    // tiles in registers for pass 2 (every sequence when num_seqs <= 1024)
+    // pass 1: both histograms and the batch's token count; a thread keeps
+    // its first sequence's tiles in registers for pass 2 (every sequence
+    // when num_seqs <= 1024)
     int L0 = 0, c0 = 0, first0 = 0, nq0 = 0;
+    unsigned long long my_tokens = 0;
     for (int s = tid; s < p.num_seqs; s += 1024) {
         int L, c, first;
         const int nq = tiles(s, true, L, c, first);
@@ -604,9 +621,17 @@ prefill_plan_kernel(const PrefillParams p, int tpb, int bn, uint32_t *plan, int 
             nq0 = nq;
         }
         for (int t = first; t < nq; ++t)
-            atomicAdd(&hist[bucket(L, c, t)], 1);
+            atomicAdd(&hist_tile[bucket(L, c, t)], 1);
+        if (nq > first) {
+            atomicAdd(&hist_seq[bucket(L, c, nq - 1)], nq - first);
+            my_tokens += (unsigned long long)L;
+        }
     }
+    if (my_tokens)
+        atomicAdd(&tokens, my_tokens);
     __syncthreads();
+    const bool by_sequence = (long long)tokens * kv_bytes_per_token > l2_bytes;
+    int *hist = by_sequence ? hist_seq : hist_tile;
     // start of each bucket in descending order of the count: thread t owns
     // buckets B-1-2t and B-2-2t; warp scans, then a scan of the warp totals
     {
@@ -647,8 +672,16 @@ prefill_plan_kernel(const PrefillParams p, int tpb, int bn, uint32_t *plan, int 
         int L = L0, c = c0, first = first0, nq = nq0;
         if (s != tid)
             nq = tiles(s, false, L, c, first);
-        for (int t = first; t < nq; ++t)
-            plan[atomicAdd(&hist[bucket(L, c, t)], 1)] = ((uint32_t)s << 16) | (uint32_t)t;
+        if (by_sequence) {
+            if (nq > first) {
+                int at = atomicAdd(&hist_seq[bucket(L, c, nq - 1)], nq - first);
+                for (int t = nq - 1; t >= first; --t)
+                    plan[at++] = ((uint32_t)s << 16) | (uint32_t)t;
+            }
+        } else {
+            for (int t = first; t < nq; ++t)
+                plan[atomicAdd(&hist_tile[bucket(L, c, t)], 1)] = ((uint32_t)s << 16) | (uint32_t)t;
+        }
     }
 }
 

@@ -38,7 +38,8 @@ struct PrefillKernel {
     int threads;
     size_t smem;
     const void *plan_fn;           // prefill_plan_kernel: (PrefillParams, tokens per block,
-                                   // keys per tile, uint32_t *plan, int *count)
+                                   // keys per tile, uint32_t *plan, int *count,
+                                   // long long K+V bytes per token, long long L2 bytes)
 };
 
 bool prefill_kernel(int dtype, int head_dim, PrefillKernel *k);
