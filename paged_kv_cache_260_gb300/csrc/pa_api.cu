@@ -553,6 +553,7 @@ int pa_prefill(void *out, const void *q, const void *k_cache, const void *v_cach
     p.num_blocks = num_blocks;
     p.q_ranks = (int)q_ranks;
     p.scale_log2 = scale * 1.4426950408889634f;
+    p.wave = ds->num_sms;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (planned) {
         int *count = static_cast<int *>(workspace);

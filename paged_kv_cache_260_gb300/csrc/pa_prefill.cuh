@@ -310,6 +310,23 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
                 tc::commit_warp(empty_bar(sl));
             return true;
         };
+        // while this block's query rows load: warm L2 with those of the
+        // block one wave later (its pair and kv head from the work order)
+        if (p.plan) {
+            const int nb = (int)blockIdx.x + p.wave;
+            if (nb / Hkv < *p.plan_count) {
+                const uint32_t e = p.plan[nb / Hkv];
+                const int s2 = (int)(e >> 16), h2 = nb % Hkv;
+                const int qs2 = __ldg(p.query_start + s2);
+                const int t02 = (int)(e & 0xffffu) * TPB;
+                const int ntok = min(TPB, __ldg(p.query_start + s2 + 1) - qs2 - t02);
+                const int lines = G * D * 2 / 128;  // 128-byte lines of a token's G heads
+                const T *qg = reinterpret_cast<const T *>(p.q);
+                for (int i = lane; i < ntok * lines; i += 32)
+                    prefetch_l2(qg + ((size_t)(qs2 + t02 + i / lines) * Hq + h2 * G) * D +
+                                (i % lines) * 64);
+            }
+        }
         bool ok = true;
         for (int g = 0; ok && g < Sh::NG; ++g)
             ok = wait_all(q_bar(g), 0) && issue_s(g, 0);

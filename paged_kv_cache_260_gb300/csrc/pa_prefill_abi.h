@@ -31,6 +31,10 @@ struct PrefillParams {
     // is walked as (query tile from the end, sequence, kv head)
     const uint32_t *plan;
     const int *plan_count;
+    // blocks in one wave (the SM count): with a work order, block b warms
+    // L2 with the query rows of block b + wave, which starts about when a
+    // block of this wave ends
+    int wave;
 };
 
 struct PrefillKernel {
