@@ -64,8 +64,9 @@ struct PrefillShape {
     static constexpr int NSLOT = (227 * 1024 - 1024 - NG * Q_BYTES) / SLOT_BYTES;   // K/V ring
     static constexpr int OFF_SLOT = NG * Q_BYTES;
     static constexpr int DATA = OFF_SLOT + NSLOT * SLOT_BYTES;   // 1024-aligned operand region
-    // full[NSLOT] empty[NSLOT] s[2] p[2] o[2] drain q[2], then TMEM base and abort flag
-    static constexpr int NBAR = 2 * NSLOT + 4 * NG + 1;
+    // full[NSLOT] empty[NSLOT] s[2] p[2] o[2] drain q[2] read[2], then TMEM
+    // base and abort flag
+    static constexpr int NBAR = 2 * NSLOT + 5 * NG + 1;
     static constexpr int BAR_BYTES = NBAR * 8 + 8;
     // The operand region is aligned up to 1024 bytes inside the dynamic
     // allocation; the barriers sit in whichever end of the 1024-byte slack
@@ -74,8 +75,12 @@ struct PrefillShape {
     static constexpr int THREADS = 64 + NG * 128;
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t GROUP_COLS = 256;
-    static constexpr uint32_t COL_S = 0;                    // S, then P over its first half
+    static constexpr uint32_t COL_S = 0;                    // S
     static constexpr uint32_t COL_O = 128;
+    // P (BN/2 packed columns) gets its own columns when they fit beside S and
+    // O (head_dim 64); otherwise it overwrites S's first half
+    static constexpr bool SEPARATE_P = COL_O + D + BN / 2 <= GROUP_COLS;
+    static constexpr uint32_t COL_P = SEPARATE_P ? COL_O + D : COL_S;
     static_assert(D == 64 || D == 128, "head_dim");
     static_assert(NSLOT >= 4, "at least two tiles of K/V in flight");
     static_assert(OFF_SLOT % 1024 == 0 && SLOT_BYTES % 1024 == 0, "swizzle atoms");
@@ -107,6 +112,8 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
     auto o_bar = [&](int g) { return bar_addr + 8u * (2 * NS + 2 * Sh::NG + g); };
     const uint32_t drain_bar = bar_addr + 8u * (2 * NS + 3 * Sh::NG);
     auto q_bar = [&](int g) { return drain_bar + 8u * (1 + g); };   // Q_g is in shared memory
+    // with P in its own columns: the group's softmax has read S_g,j
+    auto read_bar = [&](int g) { return drain_bar + 8u * (1 + Sh::NG + g); };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + Sh::NBAR * 8);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -171,8 +178,10 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
             mbar_init(o_bar(g), 1);
         }
         mbar_init(drain_bar, 1);
-        for (int g = 0; g < Sh::NG; ++g)
+        for (int g = 0; g < Sh::NG; ++g) {
             mbar_init(q_bar(g), Sh::NG * 128);
+            mbar_init(read_bar(g), 128);
+        }
         *abort_flag = 0;
         mbar_init_fence();
     }
@@ -301,7 +310,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
                 // A = P: keys 16kk.. = 8 packed columns; B = V block kk
                 // (MN-major: 64-channel groups NB boxes apart, 8-key groups
                 // 1 KB apart)
-                tc::mma_ts_warp(gc + Sh::COL_O, gc + Sh::COL_S + 8 * kk,
+                tc::mma_ts_warp(gc + Sh::COL_O, gc + Sh::COL_P + 8 * kk,
                                 vd + (uint64_t)((kk * Sh::BOX) >> 4), idO,
                                 (j > 0 || kk > 0) ? 1u : 0u);
             }
@@ -336,10 +345,17 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
                 break;
             }
             for (int g = 0; ok && g < Sh::NG; ++g) {
-                ok = issue_pv(g, j);
-                // S_g,j+1 reuses the TMEM columns P_g,j . V_j reads
-                if (ok && j + 1 < nt)
-                    ok = wait_all(o_bar(g), j & 1) && issue_s(g, j + 1);
+                if constexpr (Sh::SEPARATE_P) {
+                    // S_g,j+1 only needs the softmax to have read S_g,j
+                    if (j + 1 < nt)
+                        ok = wait_all(read_bar(g), j & 1) && issue_s(g, j + 1);
+                    ok = ok && issue_pv(g, j);
+                } else {
+                    ok = issue_pv(g, j);
+                    // S_g,j+1 reuses the TMEM columns P_g,j . V_j reads
+                    if (ok && j + 1 < nt)
+                        ok = wait_all(o_bar(g), j & 1) && issue_s(g, j + 1);
+                }
             }
         }
         if (!ok && lane == 0)
@@ -422,6 +438,10 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
             __syncwarp();                        // tcgen05.ld is warp-collective
             tc::tmem_ld64(tg + Sh::COL_S, v[0]);
             tc::tmem_ld64(tg + Sh::COL_S + 64, v[1]);
+            if constexpr (Sh::SEPARATE_P) {
+                tc::fence_before_sync();
+                mbar_arrive(read_bar(grp));      // S_g,j+1 may go in
+            }
             // tiles left of the diagonal (the common case) need no mask
             const bool full = __all_sync(FULL, vis >= Sh::BN - 1);
             if (!full) {
@@ -459,6 +479,16 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
             // TMEM over score columns already read: keys 0-63 -> columns
             // 0-31, keys 64-127 -> 32-63.  Scale-and-subtract and the row sum
             // run two values per instruction.
+            if constexpr (Sh::SEPARATE_P) {
+                // P_g,j overwrites P_g,j-1, and O may be rescaled below: both
+                // wait for P_g,j-1 . V_j-1 (with P apart from S, S_g,j was
+                // issued without it)
+                if (j > 0 && !__all_sync(FULL, mbar_wait_bounded(o_bar(grp), (j - 1) & 1))) {
+                    ok = false;
+                    break;
+                }
+                tc::fence_after_sync();
+            }
             const uint64_t sl2x2 = f2_pack(sl2, sl2), nmx2 = f2_pack(-m, -m);
             uint64_t sum2[4] = {0, 0, 0, 0};
 #pragma unroll
@@ -476,7 +506,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
                     pw[e / 2] = Mma<T>::pack(p0, p1);
                 }
                 __syncwarp();
-                tc::tmem_st32(tg + Sh::COL_S + 32 * hb, pw);
+                tc::tmem_st32(tg + Sh::COL_P + 32 * hb, pw);
             }
             float sum[4];
 #pragma unroll
@@ -508,7 +538,8 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
                 }
                 fence_proxy_async_shared();
             }
-            // O rescale: P_g,j-1 . V_j-1 completed before S_g,j was issued
+            // O rescale: P_g,j-1 . V_j-1 has completed (before S_g,j was
+            // issued, or, with P in its own columns, by the wait above)
             __syncwarp();
             if (__any_sync(FULL, grow)) {
 #pragma unroll

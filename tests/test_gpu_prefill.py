@@ -238,8 +238,9 @@ def test_prefill_long_prompt_sampled_rows(pa):
 
 
 
-@pytest.mark.parametrize("dt,every,step", [("bf16", 64, 10.0), ("bf16", 128, 6.5), ("f16", 64, 10.0)])
-def test_prefill_scores_that_keep_growing(pa, dt, every, step):
+@pytest.mark.parametrize("dt,every,step,d", [("bf16", 64, 10.0, 128), ("bf16", 128, 6.5, 128),
+                                             ("f16", 64, 10.0, 128), ("bf16", 64, 10.0, 64)])
+def test_prefill_scores_that_keep_growing(pa, dt, every, step, d):
     # Every query row leans along one direction u, and every `every`-th key
     # (at offset 37, so the spikes fall in both halves of 128-key tiles when
     # every = 64) lies along u with a length that raises its score by about
@@ -250,10 +251,9 @@ def test_prefill_scores_that_keep_growing(pa, dt, every, step):
     # The keys are aligned with the queries, so the large scores carry no
     # cancellation; V is scaled by 1/4 so that |O| stays near 1 and the
     # dtype's tolerance (derived for outputs of that size) applies.
-    w = synth.build_prefill("pf", 8, 2, 128, dt, [700, 300, 1000, 129], [300, 300, 200, 129],
+    w = synth.build_prefill("pf", 8, 2, d, dt, [700, 300, 1000, 129], [300, 300, 200, 129],
                             seed=77, poison=True)
     rng = np.random.default_rng(78)
-    d = w.head_dim
     u = rng.standard_normal(d)
     u /= np.linalg.norm(u)
     beta = 3.0
