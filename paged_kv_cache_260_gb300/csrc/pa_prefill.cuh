@@ -35,9 +35,11 @@
 //             flight); then one thread per row (its TMEM lane): scores from TMEM, causal mask, online softmax in base 2
 //             with a lazy rescale of O (only when the running maximum grows
 //             by more than 2^8), P into TMEM, and the final O / l written out.
-// TMEM (512 columns): group g uses [256g, 256g + 128) for S (P packed two
-// per column in the first 64 of them) and [256g + 128, 256g + 128 + head_dim)
-// for O.
+// TMEM (512 columns): group g uses [256g, 256g + 128) for S and
+// [256g + 128, 256g + 128 + head_dim) for O.  P, packed two per column,
+// overwrites S's first 64 columns at head_dim 128; at head_dim 64 it has the
+// group's last 64 columns, and S_g,j+1 is then issued as soon as the softmax
+// has read S_g,j.
 // Every wait is bounded; a wait that gives up records PA_DEVERR_TIMEOUT and
 // the block drains its copies and MMAs before it frees TMEM and exits.
 #pragma once
