@@ -351,3 +351,63 @@ def test_prefill_work_order_by_sequence_when_kv_exceeds_l2(pa):
             ref = oracle.decode(w.q[row][None], w.k_cache, w.v_cache, w.block_tables[s][None],
                                 np.array([p + 1], np.int32), w.scale, w.dtype)
             assert float(np.abs(got[row] - ref[0]).max()) <= TOL["bf16"], (s, i)
+
+
+def _plan_after(pa, w):
+    """Run a prefill with an explicit work-order workspace and read the plan
+    back: the pair count at byte 0, then one uint32 (sequence << 16 | query
+    tile) per pair from byte 16."""
+    q = dev_bits(w.q, w.dtype)
+    k, v = dev_bits(w.k_cache, w.dtype), dev_bits(w.v_cache, w.dtype)
+    mq = int(np.diff(w.query_start).max())
+    nb = pa.prefill_workspace_size(w.num_seqs, mq, w.num_heads, w.num_kv_heads)
+    ws = torch.zeros(nb, dtype=torch.uint8, device="cuda")
+    out = torch.empty_like(q)
+    pa.prefill(out, q, k, v, torch.from_numpy(w.block_tables).cuda(),
+               torch.from_numpy(w.seq_lens).cuda(), torch.from_numpy(w.query_start).cuda(), mq,
+               w.scale, workspace=ws)
+    torch.cuda.synchronize()
+    raw = ws.cpu().numpy()
+    count = int(raw[:4].view(np.int32)[0])
+    plan = raw[16:16 + 4 * count].view(np.uint32)
+    return [(int(e >> 16), int(e & 0xFFFF)) for e in plan]
+
+
+def _tile_counts(w):
+    # key tiles (128 keys) up to the last row of each (sequence, query tile):
+    # the query tile holds 2 * (128 / G) chunk tokens
+    tpb = 2 * (128 // (w.num_heads // w.num_kv_heads))
+    nt = {}
+    for s in range(w.num_seqs):
+        L = int(w.seq_lens[s])
+        c = int(w.query_start[s + 1] - w.query_start[s])
+        for t in range((c + tpb - 1) // tpb):
+            nt[(s, t)] = (L - c + min((t + 1) * tpb, c) - 1) // 128 + 1
+    return nt
+
+
+def test_prefill_work_order_contents(pa):
+    # the plan holds every (sequence, query tile) pair exactly once; a batch
+    # whose K/V fits in L2 is ordered longest first, a larger one sequence by
+    # sequence (sequences by their heaviest tile, each sequence's tiles
+    # heaviest first)
+    small = synth.build_prefill("pf", 32, 8, 128, "bf16", [900, 130, 2000, 64, 700],
+                                [600, 130, 200, 1, 333], seed=21)
+    plan, nt = _plan_after(pa, small), _tile_counts(small)
+    assert sorted(plan) == sorted(nt)
+    counts = [nt[e] for e in plan]
+    assert counts == sorted(counts, reverse=True)
+
+    big = synth.build_prefill("pf", 32, 8, 128, "bf16", [8192, 4096, 8192, 6000, 8192, 7000],
+                              [300, 64, 1, 512, 129, 1000], seed=61)
+    plan, nt = _plan_after(pa, big), _tile_counts(big)
+    assert sorted(plan) == sorted(nt)
+    seqs = [s for s, _ in plan]
+    runs = [s for i, s in enumerate(seqs) if i == 0 or s != seqs[i - 1]]
+    assert len(runs) == len(set(runs))                     # each sequence's pairs together
+    heaviest = [max(nt[(s, t)] for (s2, t) in nt if s2 == s) for s in runs]
+    assert heaviest == sorted(heaviest, reverse=True)
+    for s in runs:
+        tiles = [t for s2, t in plan if s2 == s]
+        assert tiles == sorted(tiles, reverse=True)
+    assert pa.get_device_error() == 0
