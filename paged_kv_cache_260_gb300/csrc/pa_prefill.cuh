@@ -15,10 +15,10 @@
 //
 // Operand bytes per flop are kept low: key tiles of 128 (Q is read from
 // shared memory once per 128 keys), and P never goes through shared memory
-// -- the softmax writes it into tensor memory over the score columns it has
-// consumed, and P.V takes its A operand from there.  What bounds the kernel
-// is each group's chain S -> softmax -> P.V -> next S against the other
-// group's MMA work.
+// -- the softmax writes it into tensor memory (over the score columns it has
+// consumed, or at head_dim 64 into columns of its own), and P.V takes its A
+// operand from there.  What bounds the kernel is each group's chain
+// S -> softmax -> P.V -> next S against the other group's MMA work.
 // Warp roles (320 threads):
 //   warp 0    TMA producer of K and V tiles of 128 keys (8 pool blocks x 16
 //             rows x 128-byte boxes) into a ring of slots;
@@ -26,15 +26,16 @@
 //             loop, one elected lane issues):
 //               S_g,j = Q_g . K_j^T        (M 128, N 128, K = head_dim)
 //               O_g  += P_g,j . V_j        (M 128, N head_dim, K 128; A in TMEM)
-//             S_g,j+1 overwrites the columns P_g,j is read from, so it is
-//             issued once P_g,j . V_j has completed; the two groups
-//             alternate on the tensor core (one group's softmax runs while
-//             the other group's MMAs do);
+//             at head_dim 128 S_g,j+1 overwrites the columns P_g,j is read
+//             from, so it is issued once P_g,j . V_j has completed; the two
+//             groups alternate on the tensor core (one group's softmax runs
+//             while the other group's MMAs do);
 //   warps 2-5 group 0, warps 6-9 group 1: first load the Q tiles into
 //             shared memory (while the producer's first K/V copies are in
-//             flight); then one thread per row (its TMEM lane): scores from TMEM, causal mask, online softmax in base 2
-//             with a lazy rescale of O (only when the running maximum grows
-//             by more than 2^8), P into TMEM, and the final O / l written out.
+//             flight); then one thread per row (its TMEM lane): scores from
+//             TMEM, causal mask, online softmax in base 2 with a lazy
+//             rescale of O (only when the running maximum grows by more than
+//             2^8), P into TMEM, and the final O / l written out.
 // TMEM (512 columns): group g uses [256g, 256g + 128) for S and
 // [256g + 128, 256g + 128 + head_dim) for O.  P, packed two per column,
 // overwrites S's first 64 columns at head_dim 128; at head_dim 64 it has the
