@@ -805,38 +805,64 @@ def run_prefill(args):
 
 
 def run_reference(args):
-    """The oracle as the reference arm: each step is a bounded sample of the
-    workload (whole sequences in order) on the host cores."""
+    """The oracle as the reference arm: W untimed and K timed steps, each a
+    bounded sample of the workload (its first sequences in order, or a prefix
+    of the first sequence when one sequence is more than a step's share),
+    sized so that the whole run takes about two minutes."""
     rank, world, _ = dist_env()
     if rank != 0:
         return
     import oracle
     oracle.build()
     w = make_workload(args.workload, 0)
-    threads = oracle.num_threads()
     per_seq = 2 * w.num_kv_heads * w.head_dim * 2
-    budget = max(0.05, 90.0 / max(1, args.steps + args.warmup))   # seconds per step
-    # sample size: whole sequences, as many as fit the per-step budget (at least one)
-    t0 = time.perf_counter()
-    oracle.decode(w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.scale, w.dtype,
-                  seqs=[0], threads=threads)
-    one = max(1e-4, time.perf_counter() - t0)
-    n = int(max(1, min(w.num_seqs, budget / one)))
-    sel = list(range(n))
+    budget = 120.0 / max(1, args.steps + args.warmup)   # seconds per step
+    # small samples run on one thread: starting threads would dominate them
+    threads = 1 if budget < 0.05 else oracle.num_threads()
 
-    def step():
-        oracle.decode(w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.scale, w.dtype,
+    def run(sel, lens):
+        oracle.decode(w.q, w.k_cache, w.v_cache, w.block_tables, lens, w.scale, w.dtype,
                       seqs=sel, threads=threads)
 
+    lens = w.seq_lens.copy()
+
+    def timed(n):
+        t0 = time.perf_counter()
+        run(list(range(n)), lens)
+        return time.perf_counter() - t0
+
+    # the largest prefix of sequences whose sample fits a step's share
+    # (timed, since lengths differ): doubling, then bisection
+    run([0], lens)                                       # first call: library and pages
+    one = timed(1)
+    if one > budget:
+        lens[0] = max(1, int(int(w.seq_lens[0]) * budget / one))
+        n = 1
+        sample = f"fp64 oracle decode of the first {int(lens[0])} tokens of sequence 0 per step"
+    else:
+        lo, hi = 1, 1
+        while hi < w.num_seqs:
+            hi = min(w.num_seqs, 2 * hi)
+            if timed(hi) > budget:
+                break
+            lo = hi
+        while hi - lo > 1:
+            mid = (lo + hi) // 2
+            if timed(mid) > budget:
+                hi = mid
+            else:
+                lo = mid
+        n = lo
+        sample = f"fp64 oracle decode of sequences 0..{n - 1} of the workload per step"
+    sel = list(range(n))
     for _ in range(args.warmup):
-        step()
+        run(sel, lens)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        step()
+        run(sel, lens)
     dt = time.perf_counter() - t0
-    b = sum(int(w.seq_lens[s]) for s in sel) * per_seq
+    b = sum(int(lens[s]) for s in sel) * per_seq
     value = b * args.steps / dt / 1e9
-    sample = f"fp64 oracle decode of sequences 0..{n - 1} of the workload per step"
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
