@@ -241,6 +241,31 @@ def test_other_stream(pa):
     assert max_err(dw.out, ref) <= TOL["bf16"]
 
 
+def test_balanced_workspace_reused_across_shapes(pa):
+    # The workspace's contents need no initialisation: one buffer, filled with
+    # 0xff bytes (NaN as fp32, -1 as descriptors) before every call, serves
+    # calls of several shapes in turn -- groups 4, 7 and 8, head_dim 64 and
+    # 128, runs cut into one to dozens of pieces -- and every result stays
+    # within tolerance, twice over.
+    rng = np.random.default_rng(74)
+    cases = [
+        synth.build("reuse_a", 6, 32, 8, 128, "bf16", [5, 900, 3000, 17, 1200, 64], seed=71,
+                    append=True, poison=True),
+        synth.build("reuse_b", 5, 14, 2, 64, "f16", [4000, 33, 2500, 1, 700], seed=72,
+                    poison=True),
+        synth.long(poison=True, lens=(8192, 16384 + 3), partition_size=0),
+        synth.build("reuse_d", 40, 16, 2, 128, "f16", rng.integers(0, 2000, size=40), seed=73,
+                    poison=True),
+    ]
+    need = max(pa.decode_workspace_size(w.num_seqs, w.num_heads, w.num_kv_heads, w.head_dim,
+                                        w.block_tables.shape[1], 0) for w in cases)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    for _ in range(2):
+        for w in cases:
+            ws.fill_(0xFF)
+            check(pa, w, 0, ws=ws)
+
+
 # ---------------------------------------------------------------------------
 # pa_decode_append: reshape_and_cache + decode in one launch
 # ---------------------------------------------------------------------------
