@@ -12,7 +12,9 @@ Prints ONE JSON line (rank 0):
              divided by the step time (max over ranks)
   e2e        the same metric through the public API with host buffers: each
              step copies its inputs from pinned host memory and reads the
-             output back inside the timed region
+             output back inside the timed region, the copies on their own
+             streams and double-buffered so that they overlap the
+             neighbouring steps' compute, as a serving loop runs
   roofline   the decode kernel's achieved bytes/s against measured HBM peak
   cpu_baseline  the fp64 oracle on the host cores, on a bounded sample
 
@@ -388,48 +390,111 @@ def cpu_baseline(w, budget_s: float = 12.0, threads: int = 0):
     return done_bytes / dt / 1e9, sample, threads, rows
 
 
-def e2e_measure(st, steps: int, device):
-    """Public-API step with host buffers: the step's inputs are packed in one
-    pinned host buffer and copied in with one H2D copy, the step runs, and the
-    output comes back with one D2H copy.  Returns (ms per step, h2d bytes,
-    d2h bytes)."""
+def pipelined_e2e(inputs, out, bind, step, steps: int, device, before=None):
+    """End-to-end steps through the public API with host buffers, pipelined
+    the way a serving loop runs them.
+
+    Every step copies its inputs in from one packed, pinned host buffer (H2D,
+    on a copy stream) and its output back to pinned host memory (D2H, on a
+    second copy stream); the step itself runs on the current stream.  The
+    device inputs and the output are double-buffered, so step i's H2D
+    overlaps step i-1's compute and step i's D2H overlaps step i+1's; events
+    order every reuse of a buffer.
+
+    inputs: the device tensors a step reads (their contents fill the host
+    buffer); out: the tensor it writes; bind(views, out_buf) points the step
+    at one buffer set; step() enqueues the step; before(), if given, is
+    enqueued on the compute stream ahead of each step (an L2 flush).
+    Returns (ms per step, H2D bytes, D2H bytes, the last step's host output).
+    """
     import torch
-    names = ["q", "tables", "lens", "k_new", "v_new", "slots", "pairs"]
-    dev_t = [getattr(st, n) for n in names if getattr(st, n) is not None]
     offs, total = [], 0
-    for t in dev_t:
+    for t in inputs:
         offs.append(total)
         total += (t.numel() * t.element_size() + 255) // 256 * 256
     host = torch.empty(total, dtype=torch.uint8).pin_memory()
-    dev = torch.empty(total, dtype=torch.uint8, device=device)
-    saved = {}
-    for n, t, o in zip([n for n in names if getattr(st, n) is not None], dev_t, offs):
-        nb = t.numel() * t.element_size()
-        host[o:o + nb].copy_(t.reshape(-1).view(torch.uint8).cpu())
-        saved[n] = t
-        # the step reads its inputs straight from the packed device buffer
-        setattr(st, n, dev[o:o + nb].view(t.dtype).view(t.shape))
-    out_h = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
-    h2d = total
-    d2h = out_h.numel() * out_h.element_size()
+    for t, o in zip(inputs, offs):
+        host[o:o + t.numel() * t.element_size()].copy_(t.reshape(-1).view(torch.uint8).cpu())
+    devs = [torch.empty(total, dtype=torch.uint8, device=device) for _ in range(2)]
+    views = [[d[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+              for t, o in zip(inputs, offs)] for d in devs]
+    outs = [torch.empty_like(out) for _ in range(2)]
+    outs_h = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
+    comp = torch.cuda.current_stream(device)
+    s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    in_ready, in_free, out_ready, out_free = ([torch.cuda.Event(), torch.cuda.Event()]
+                                              for _ in range(4))
+    count = [0]
 
     def one():
-        dev.copy_(host, non_blocking=True)
-        st.run()
-        out_h.copy_(st.out, non_blocking=True)
+        i = count[0]
+        count[0] += 1
+        b = i % 2
+        if i >= 2:                       # the step that last read set b is done
+            s_in.wait_event(in_free[b])
+        with torch.cuda.stream(s_in):
+            devs[b].copy_(host, non_blocking=True)
+        in_ready[b].record(s_in)
+        if before is not None:
+            before()
+        comp.wait_event(in_ready[b])
+        if i >= 2:                       # output buffer b has been read back
+            comp.wait_event(out_free[b])
+        bind(views[b], outs[b])
+        step()
+        in_free[b].record(comp)
+        out_ready[b].record(comp)
+        s_out.wait_event(out_ready[b])
+        with torch.cuda.stream(s_out):
+            outs_h[b].copy_(outs[b], non_blocking=True)
+        out_free[b].record(s_out)
 
     for _ in range(3):
         one()
     torch.cuda.synchronize(device)
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
+    a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(comp)
+    s_in.wait_stream(comp)               # the first copy starts inside the timed region
     for _ in range(steps):
         one()
-    b.record()
+    comp.wait_stream(s_out)              # ... and the last read-back ends inside it
+    z.record(comp)
     torch.cuda.synchronize(device)
-    for n, t in saved.items():
-        setattr(st, n, t)
-    return a.elapsed_time(b) / steps, h2d, d2h
+    h2d = total
+    d2h = outs_h[0].numel() * outs_h[0].element_size()
+    return a.elapsed_time(z) / steps, h2d, d2h, outs_h[(count[0] - 1) % 2].clone()
+
+
+def e2e_measure(st, steps: int, device, flush=None):
+    """The decode step end to end (pipelined_e2e): q, tables, lengths, the new
+    tokens, their slots and the copy-on-write pairs come in from one packed
+    pinned host buffer, the output goes back.  `flush`, when given, is
+    zeroed ahead of every step, as the device-resident timing does for
+    working sets that L2 could hold.  The last step's host output must equal
+    the device-resident step's, bit for bit.  Returns (ms per step, h2d
+    bytes, d2h bytes)."""
+    import torch
+    names = [n for n in ["q", "tables", "lens", "k_new", "v_new", "slots", "pairs"]
+             if getattr(st, n) is not None]
+    saved = [getattr(st, n) for n in names]
+    saved_out = st.out
+
+    def bind(views, out_buf):
+        for n, v in zip(names, views):
+            setattr(st, n, v)
+        st.out = out_buf
+
+    try:
+        ms, h2d, d2h, last = pipelined_e2e(saved, saved_out, bind, st.run, steps, device,
+                                           before=None if flush is None else flush.zero_)
+    finally:
+        bind(saved, saved_out)
+    st.run()
+    torch.cuda.synchronize(device)
+    if not torch.equal(st.out.cpu(), last):
+        raise RuntimeError("the pipelined end-to-end step's output differs from the "
+                           "device-resident step's")
+    return ms, h2d, d2h
 
 
 def run_ours(args):
@@ -516,7 +581,7 @@ def run_ours(args):
     value = total_bytes / (ms_per_step * 1e-3) / 1e9
     dec = float(np.mean(dec_ms))
 
-    e2e_ms, h2d, d2h = e2e_measure(st, max(20, min(args.steps, 300)), device)
+    e2e_ms, h2d, d2h = e2e_measure(st, max(20, min(args.steps, 300)), device, flush)
     e2e_ms = dist_max(e2e_ms, device)
     peak, peak_src = measured_hbm_peak()
     achieved = kv_bytes / (dec * 1e-3) / 1e9
@@ -771,31 +836,27 @@ def run_prefill(args):
     # sustained peak, a short one with the burst peak
     peak, peak_src = measured_bf16_peak(sustained=ms * steps > 500.0)
 
-    # end to end through the public API: q, tables, lengths and query starts
-    # from pinned host memory, the output back to it, every step
-    hq = torch.from_numpy(np.ascontiguousarray(w.q).view(np.int16)).view(tdt).pin_memory()
-    ht = torch.from_numpy(w.block_tables).pin_memory()
-    hl = torch.from_numpy(w.seq_lens).pin_memory()
-    hs = torch.from_numpy(w.query_start).pin_memory()
-    hout = torch.empty_like(hq).pin_memory()
-    h2d = sum(x.numel() * x.element_size() for x in (hq, ht, hl, hs))
-    d2h = hout.numel() * hout.element_size()
+    # end to end through the public API (pipelined_e2e): q, tables, lengths
+    # and query starts from pinned host memory, the output back to it, every
+    # step, with the L2 flush ahead of each step as above
+    cur = {}
+
+    def bind(views, out_buf):
+        cur["q"], cur["tables"], cur["lens"], cur["qs"] = views
+        cur["out"] = out_buf
+
+    def e2e_step():
+        pa.prefill(cur["out"], cur["q"], k, v, cur["tables"], cur["lens"], cur["qs"], mq,
+                   w.scale, workspace=ws)
+
     e2e_steps = max(3, min(steps, 50))
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e2e_ms = 0.0
-    for _ in range(e2e_steps):
-        flush.zero_()
-        e0.record()
-        q.copy_(hq, non_blocking=True)
-        tables.copy_(ht, non_blocking=True)
-        lens.copy_(hl, non_blocking=True)
-        qs.copy_(hs, non_blocking=True)
-        call()
-        hout.copy_(out, non_blocking=True)
-        e1.record()
-        torch.cuda.synchronize(device)
-        e2e_ms += e0.elapsed_time(e1)
-    e2e_ms /= e2e_steps
+    e2e_ms, h2d, d2h, last = pipelined_e2e([q, tables, lens, qs], out, bind, e2e_step, e2e_steps,
+                                           device, before=flush.zero_)
+    call()
+    torch.cuda.synchronize(device)
+    if not torch.equal(out.cpu(), last):
+        raise RuntimeError("the pipelined end-to-end prefill's output differs from the "
+                           "device-resident one's")
     cpu = None
     parity = None
     if not args.no_cpu_baseline:
