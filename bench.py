@@ -298,7 +298,8 @@ class Step:
         of `graph_ev` timestamps every decode.  A record node between two
         kernels also cuts the programmatic dependency between them (the next
         step's decode could otherwise be scheduled while this step's merge
-        drains), so the throughput is timed on `graph`, which has none."""
+        drains), so the timed steps replay `graph`, save for one replay of
+        `graph_ev` at the end."""
         import torch
         self.ev = [(timing_event(), timing_event()) for _ in range(steps_per_graph)]
         s = torch.cuda.Stream(self.dev)
@@ -522,13 +523,11 @@ def run_ours(args):
         st.ev = None
         st.capture(spg)
         replays = args.steps // spg
-        ev_replays = max(1, min(replays, 4))
         for _ in range(max(1, -(-args.warmup // spg))):
             st.graph.replay()
         st.graph_ev.replay()
     else:
         ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-        ev_replays = 0
         for _ in range(args.warmup):
             st.run()
     torch.cuda.synchronize(device)
@@ -543,23 +542,18 @@ def run_ours(args):
         if flush is None:
             t0.record()
             if use_graph:
-                for _ in range(replays):
+                # the last replay is the graph with an event pair around each
+                # call, whose timestamps give the roofline its call durations
+                for _ in range(replays - 1):
                     st.graph.replay()
+                st.graph_ev.replay()
             else:
                 for _ in range(args.steps):
                     st.run(ev)
             t1.record()
             torch.cuda.synchronize(device)
             elapsed = t0.elapsed_time(t1)
-            if use_graph:
-                # the decode call's own duration, for the roofline: the same
-                # steps with an event pair around each call
-                for _ in range(ev_replays):
-                    st.graph_ev.replay()
-                    torch.cuda.synchronize(device)
-                    dec_ms.append(st.decode_ms())
-            else:
-                dec_ms.append(ev[0].elapsed_time(ev[1]))
+            dec_ms.append(st.decode_ms() if use_graph else ev[0].elapsed_time(ev[1]))
         else:
             # small working set: flush L2 before every step, time the steps only
             elapsed = 0.0
@@ -630,8 +624,8 @@ def run_ours(args):
             "l2": ("inputs larger than L2 (KV read per step %.0f MB vs 129 MB L2)" % (unique_bytes / 1e6)
                    if l2_ok else "L2 flushed (258 MB write) before every step; steps timed alone"),
             "timing": ("CUDA graph of %d steps back to back, replayed %d times, CUDA events around "
-                       "the replays; decode duration (roofline) from %d replays of the same steps "
-                       "with an event pair around each call" % (spg, args.steps // spg, ev_replays)
+                       "the replays; the last replay has an event pair around each call, which "
+                       "gives the roofline its call duration" % (spg, args.steps // spg)
                        if use_graph and l2_ok else "CUDA events per step"),
             "parallelism": "replicas" if world > 1 else "single GPU",
         },
