@@ -266,6 +266,76 @@ def test_balanced_workspace_reused_across_shapes(pa):
             check(pa, w, 0, ws=ws)
 
 
+@pytest.mark.parametrize("append", [False, True])
+@pytest.mark.parametrize("mode", [0, 512])
+def test_back_to_back_steps_in_a_cuda_graph(pa, mode, append):
+    # The configuration the bench times: decode calls captured back to back
+    # in one CUDA graph, each a programmatic dependent launch of the call
+    # before, sharing one output buffer, one pool and one workspace.  Every
+    # step has its own queries and lengths (and, with append, its own new
+    # token written into the pool on the way), so the runs are cut in
+    # different places from step to step.  After each replay the output is
+    # the last step's over the pool all the steps left, and it matches the
+    # oracle.  A step that overtook the previous step's merge would leave
+    # that merge's rows, or read its slots, in the result.
+    rng = np.random.default_rng(91 + mode + append)
+    base = np.clip(np.round(rng.lognormal(np.log(600), 1.0, size=48)), 16, 4096).astype(int)
+    w = synth.build("b2b", 48, 32, 8, 128, "bf16", base, seed=92 + mode, poison=True)
+    dw = DevWorkload(w)
+    steps = 5
+    qs, lens, news = [], [], []
+    k_host, v_host = w.k_cache.copy(), w.v_cache.copy()
+    for i in range(steps):
+        q = synth.to_bits(rng.standard_normal(w.q.shape).astype(np.float32), w.dtype)
+        L = np.minimum(w.seq_lens, rng.integers(1, 4097, size=w.num_seqs)).astype(np.int32)
+        if i == steps - 1:
+            L[::7] = w.seq_lens[::7]
+        qs.append(q)
+        lens.append(L)
+        if append:
+            shape = (w.num_seqs, w.num_kv_heads, w.head_dim)
+            kn = synth.to_bits(rng.standard_normal(shape).astype(np.float32), w.dtype)
+            vn = synth.to_bits(rng.standard_normal(shape).astype(np.float32), w.dtype)
+            pos = L - 1
+            slots = (w.block_tables[np.arange(w.num_seqs), pos // 16].astype(np.int64) * 16
+                     + pos % 16)
+            oracle.reshape_and_cache(k_host, v_host, kn, vn, slots)
+            news.append((dev_bits(kn, w.dtype), dev_bits(vn, w.dtype),
+                         torch.from_numpy(slots).cuda()))
+    q_dev = [dev_bits(q, w.dtype) for q in qs]
+    l_dev = [torch.from_numpy(L).cuda() for L in lens]
+    ws = pa.workspace_for(dw.q, dw.k, dw.tables, mode)
+
+    def step(i, stream):
+        if append:
+            kn, vn, sl = news[i]
+            pa.decode_append(dw.out, q_dev[i], dw.k, dw.v, dw.tables, l_dev[i], kn, vn, sl,
+                             w.scale, partition_size=mode, workspace=ws, stream=stream)
+        else:
+            pa.decode(dw.out, q_dev[i], dw.k, dw.v, dw.tables, l_dev[i], w.scale,
+                      partition_size=mode, workspace=ws, stream=stream)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for i in range(steps):                                     # warm-up
+            step(i, s)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for i in range(steps):
+                step(i, s)
+    torch.cuda.current_stream().wait_stream(s)
+    ref = oracle.decode(qs[-1], k_host, v_host, w.block_tables, lens[-1], w.scale, w.dtype)
+    for _ in range(3):
+        dw.out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert max_err(dw.out, ref) <= TOL[w.dtype]
+    assert pa.get_device_error() == 0
+    if append:
+        assert np.array_equal(host_bits(dw.k), k_host) and np.array_equal(host_bits(dw.v), v_host)
+
+
 # ---------------------------------------------------------------------------
 # pa_decode_append: reshape_and_cache + decode in one launch
 # ---------------------------------------------------------------------------
