@@ -68,7 +68,7 @@ inline size_t decode_smem_bytes(size_t smem_fixed, int num_seqs)
 
 constexpr int kMaxSeqs = 8192;        // per-sequence arrays live in shared memory
 constexpr int kMaxWarpsPerSM = 16;    // decode workers <= SMs * this (workspace sizing)
-constexpr int kMinTiles = 8;          // balanced mode: least tiles per thread block
+constexpr int kMinTiles = 2;          // split modes: least tiles per worker (warp)
 
 bool decode_kernels_f16(int head_dim, int group, KernelSet *ks);
 bool decode_kernels_bf16(int head_dim, int group, KernelSet *ks);
