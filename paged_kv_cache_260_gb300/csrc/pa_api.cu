@@ -1,6 +1,7 @@
 // pa_api.cu -- the C ABI declared in include/pagedattn.h: host-side argument
 // checks, per-device state and kernel dispatch.  Nothing here allocates
 // device memory or synchronises, except pa_get_device_error().
+#include <algorithm>
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <math.h>
@@ -41,6 +42,15 @@ struct AttrEntry {
 constexpr int kMaxAttr = 256;
 AttrEntry g_attr[kMaxAttr];
 int g_attr_count = 0;
+
+struct StaticEntry {
+    const void *func;
+    int device;
+    size_t bytes;              // the kernel's static shared memory
+};
+constexpr int kMaxStatic = 64;
+StaticEntry g_static[kMaxStatic];
+int g_static_count = 0;
 
 struct OccEntry {
     const void *func;
@@ -101,6 +111,34 @@ int ensure_smem(const void *func, int dev, size_t smem)
         return PA_ERR_CUDA;
     if (g_attr_count < kMaxAttr)
         g_attr[g_attr_count++] = AttrEntry{func, dev, smem};
+    return PA_OK;
+}
+
+// Dynamic shared memory a block of this kernel may use on the device: the
+// per-block limit less the kernel's static shared memory.
+int dynamic_smem_limit(const void *func, int dev, size_t optin, size_t *limit)
+{
+    size_t bytes = 0;
+    bool found = false;
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        for (int i = 0; i < g_static_count; ++i)
+            if (g_static[i].func == func && g_static[i].device == dev) {
+                bytes = g_static[i].bytes;
+                found = true;
+                break;
+            }
+    }
+    if (!found) {
+        cudaFuncAttributes attr{};
+        if (cudaFuncGetAttributes(&attr, func) != cudaSuccess)
+            return PA_ERR_CUDA;
+        bytes = attr.sharedSizeBytes;
+        std::lock_guard<std::mutex> lock(g_mutex);
+        if (g_static_count < kMaxStatic)
+            g_static[g_static_count++] = StaticEntry{func, dev, bytes};
+    }
+    *limit = bytes < optin ? optin - bytes : 0;
     return PA_OK;
 }
 
@@ -344,21 +382,38 @@ static int decode_impl(void *out, const void *q, const void *k_cache, const void
         return rc;
     int dev = 0;
     cudaGetDevice(&dev);
+    // the wide variant unless the per-sequence arrays leave it too little
+    // shared memory (static shared memory counts against the limit too)
     int var = 0;
+    size_t limit = 0;
     size_t smem = decode_smem_bytes(ks.smem_fixed[0], num_seqs);
-    if (smem > ds->smem_optin) {
+    rc = dynamic_smem_limit(ks.decode[0], dev, ds->smem_optin, &limit);
+    if (rc != PA_OK)
+        return rc;
+    if (smem > limit) {
         var = 1;
         smem = decode_smem_bytes(ks.smem_fixed[1], num_seqs);
+        rc = dynamic_smem_limit(ks.decode[1], dev, ds->smem_optin, &limit);
+        if (rc != PA_OK)
+            return rc;
     }
-    if (smem > ds->smem_optin)
+    if (smem > limit)
         return PA_ERR_UNSUPPORTED;
     const void *decode_fn = ks.decode[var];
     const int warps = ks.warps[var];
-    rc = ensure_smem(decode_fn, dev, smem);
+    // Blocks per SM, looked up for the shared memory rounded up to 2 KiB
+    // (within the kernel's limit): a serving loop's batch size changes every
+    // step, and the rounding keeps the cache of occupancy results to ~100
+    // entries per kernel.  A larger footprint can only lower the count, so
+    // every block of the grid still fits.  The kernel's dynamic shared
+    // memory limit is raised to the rounded figure too, since the occupancy
+    // query counts no block that would exceed it.
+    const size_t smem_key = std::min(round_up(smem, 2048), limit);
+    rc = ensure_smem(decode_fn, dev, smem_key);
     if (rc != PA_OK)
         return rc;
     int per_sm = 0;
-    rc = occupancy(decode_fn, dev, warps * 32, smem, &per_sm);
+    rc = occupancy(decode_fn, dev, warps * 32, smem_key, &per_sm);
     if (rc != PA_OK)
         return rc;
     if (per_sm < 1)
@@ -528,7 +583,11 @@ int pa_prefill(void *out, const void *q, const void *k_cache, const void *v_cach
         return rc;
     int dev = 0;
     cudaGetDevice(&dev);
-    if (kk.smem > ds->smem_optin)
+    size_t limit = 0;
+    rc = dynamic_smem_limit(kk.fn, dev, ds->smem_optin, &limit);
+    if (rc != PA_OK)
+        return rc;
+    if (kk.smem > limit)
         return PA_ERR_UNSUPPORTED;
     rc = ensure_smem(kk.fn, dev, kk.smem);
     if (rc != PA_OK)

@@ -203,6 +203,20 @@ def test_many_short_sequences(pa):
     check(pa, w, -1)
 
 
+@pytest.mark.parametrize("n", [1, 7, 100, 3300, 3307, 3308, 5000])
+def test_batch_sizes_across_kernel_variants(pa, n):
+    # The decode keeps each sequence's length and prefix in shared memory, so
+    # the block's footprint grows with the batch: at head_dim 128 it reaches
+    # the 227 KiB limit near 3,307 sequences, past which the compact 4-warp
+    # variant runs.  Batch sizes on both sides of that edge (where the
+    # footprint rounded up for the occupancy lookup would pass the limit)
+    # match the oracle.
+    rng = np.random.default_rng(n)
+    lens = rng.integers(0, 48, size=n)
+    w = synth.build("sizes", n, 16, 4, 128, "bf16", lens, seed=n, poison=True)
+    check(pa, w, 0)
+
+
 def test_bad_table_entry_is_flagged_not_faulting(pa):
     w = synth.build("badtab", 3, 8, 2, 64, "f16", [20, 40, 60], seed=9)
     w.block_tables = w.block_tables.copy()
