@@ -1,22 +1,31 @@
-"""Benchmark of one paged-decode step on GB300.
+"""Benchmark of the paged-decode step on GB300.
 
 A step is one pass of the whole hot path over one batch: copy_blocks (if the
 workload has copy-on-write pairs), reshape_and_cache (if it appends a token)
-and the decode (with its split-K merge).  The default workload is the GQA
+and the decode (with its split-K merge).  The default run measures the GQA
 batch-128 decode (128 sequences, 32 query / 8 kv heads, head_dim 128, bf16,
-lognormal lengths); ``--workload`` picks another.
+lognormal lengths) as the headline, and the other four decode workloads
+(long-context split-K, MHA 7B-shaped, parallel sampling, tiny) the same way,
+nested under "workloads" in the same line.  ``--workload`` runs one workload
+alone (also the chunked-prefill and swap lines).
 
 Prints ONE JSON line (rank 0):
   value      effective KV-read GB/s of the whole job: sum over ranks of the
              K/V bytes a step must read (every live token, every kv head)
-             divided by the step time (max over ranks)
+             divided by the step time (max over ranks); steps run back to
+             back with no event node between them
   e2e        the same metric through the public API with host buffers: each
              step copies its inputs from pinned host memory and reads the
              output back inside the timed region, the copies on their own
              streams and double-buffered so that they overlap the
              neighbouring steps' compute, as a serving loop runs
-  roofline   the decode kernel's achieved bytes/s against measured HBM peak
-  cpu_baseline  the fp64 oracle on the host cores, on a bounded sample
+  roofline   one decode call (decode + merge kernels) against the measured
+             HBM peak, on the bytes that must leave HBM (a block shared by
+             several sequences counts once)
+  cpu_baseline  the fp64 oracle's step on the host cores, sized and timed
+             the same way as ``--impl reference``
+  parity_vs_oracle  the timed step's output, every sequence, against the
+             oracle's
 
 ``--impl reference`` times the oracle instead (the only reference this
 method has), on the same workload, metric and unit.
@@ -260,8 +269,6 @@ class Step:
                       else torch.from_numpy(w.block_mapping).to(device))
         self.ws = pa.workspace_for(self.q, self.k, self.tables, partition_size)
         self.launches_per_step = self._count_launches()
-        self.graph = None
-        self.ev = None
 
     def _count_launches(self):
         n = 1                                           # decode (append fused in)
@@ -273,7 +280,7 @@ class Step:
         return n
 
     def run(self, ev_pair=None):
-        """Enqueue one step on the current stream; ev_pair brackets the decode."""
+        """Enqueue one step on the current stream; ev_pair brackets the decode call."""
         pa = self.pa
         if self.pairs is not None:
             pa.copy_blocks(self.k, self.v, self.pairs)
@@ -290,40 +297,6 @@ class Step:
         if ev_pair is not None:
             ev_pair[1].record()
 
-    def capture(self, steps_per_graph: int):
-        """Capture `steps_per_graph` steps twice: `graph` runs them back to
-        back, `graph_ev` with an event pair around each decode call.
-
-        External events become event-record nodes of a graph, so each replay
-        of `graph_ev` timestamps every decode.  A record node between two
-        kernels also cuts the programmatic dependency between them (the next
-        step's decode could otherwise be scheduled while this step's merge
-        drains), so the timed steps replay `graph`, save for one replay of
-        `graph_ev` at the end."""
-        import torch
-        self.ev = [(timing_event(), timing_event()) for _ in range(steps_per_graph)]
-        s = torch.cuda.Stream(self.dev)
-        s.wait_stream(torch.cuda.current_stream(self.dev))
-        with torch.cuda.stream(s):
-            for _ in range(2):
-                self.run()
-        torch.cuda.current_stream(self.dev).wait_stream(s)
-        torch.cuda.synchronize(self.dev)
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            for i in range(steps_per_graph):
-                self.run()
-        self.graph = g
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            for i in range(steps_per_graph):
-                self.run(self.ev[i])
-        self.graph_ev = g
-
-    def decode_ms(self):
-        """Mean decode duration (ms) over the events of the last graph replay."""
-        return float(np.mean([a.elapsed_time(b) for a, b in self.ev]))
-
 
 def timing_event():
     import torch
@@ -331,6 +304,25 @@ def timing_event():
         return torch.cuda.Event(enable_timing=True, external=True)
     except TypeError:                      # torch without external events
         return None
+
+
+def capture(fns, device):
+    """A CUDA graph of the enqueued work of `fns`, called in order (after two
+    eager warm-up passes on a side stream)."""
+    import torch
+    s = torch.cuda.Stream(device)
+    s.wait_stream(torch.cuda.current_stream(device))
+    with torch.cuda.stream(s):
+        for _ in range(2):
+            for f in fns:
+                f()
+    torch.cuda.current_stream(device).wait_stream(s)
+    torch.cuda.synchronize(device)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for f in fns:
+            f()
+    return g
 
 
 def pick_steps_per_graph(steps: int, cap: int = 32) -> int:
@@ -350,47 +342,117 @@ def pool_utilisation(w):
             "table_tokens": int(w.seq_lens.sum())}
 
 
-def cpu_baseline(w, budget_s: float = 12.0, threads: int = 0):
-    """The fp64 oracle on a bounded sample: whole sequences in order, repeated
-    until ~budget_s of CPU work, on `threads` host threads (0: all cores);
-    returns (GB/s of KV processed, sample text, cores, {sequence: oracle
-    output row} of the first pass)."""
+# ---------------------------------------------------------------------------
+# the oracle's timed step (cpu_baseline and --impl reference use the same one)
+# ---------------------------------------------------------------------------
+def oracle_pool_after_step(w):
+    """Host copies of the pool after the step's copy_blocks and
+    reshape_and_cache, applied by the oracle (not timed: the timed oracle step
+    is the decode, which is where the step's work is)."""
     import oracle
-    oracle.build()
-    threads = threads or oracle.num_threads()
     k, v = w.k_cache.copy(), w.v_cache.copy()
-    t0 = time.perf_counter()
     if w.block_mapping is not None and len(w.block_mapping):
         oracle.copy_blocks(k, v, w.block_mapping)
     if w.slot_mapping is not None:
         oracle.reshape_and_cache(k, v, w.k_new, w.v_new, w.slot_mapping)
-    per_seq = 2 * w.num_kv_heads * w.head_dim * 2
-    done_bytes, seqs, reps = 0, 0, 0
-    chunk = max(1, threads // 2)
-    rows = {}
-    while True:
-        for s0 in range(0, w.num_seqs, chunk):
-            sel = list(range(s0, min(w.num_seqs, s0 + chunk)))
-            out = oracle.decode(w.q, k, v, w.block_tables, w.seq_lens, w.scale, w.dtype,
-                                seqs=sel, threads=threads)
-            if reps == 0:
-                for s in sel:
-                    rows[s] = out[s]
-            done_bytes += int(sum(int(w.seq_lens[s]) for s in sel)) * per_seq
-            seqs += len(sel)
-            if time.perf_counter() - t0 > budget_s:
+    return k, v
+
+
+def oracle_step_budget(steps: int, warmup: int) -> float:
+    """Seconds one oracle step may take: the whole --steps/--warmup run of the
+    reference arm then ends within about two minutes."""
+    return min(2.0, 120.0 / max(1, steps + warmup))
+
+
+def oracle_sample(w, k, v, budget_s: float):
+    """The oracle's step on the host cores: one fp64 decode call over the
+    first n sequences of the workload (every host thread), n the largest prefix
+    whose call fits `budget_s` (timed: doubling, then bisection); when one
+    sequence alone exceeds it, a prefix of that sequence's tokens.
+
+    Returns (run, bytes per step, threads, text); run() performs one step and
+    returns the oracle's rows {sequence: fp64 [Hq, D]}."""
+    import oracle
+    oracle.build()
+    threads = oracle.num_threads()
+    per_tok = 2 * w.num_kv_heads * w.head_dim * 2
+    lens = w.seq_lens.copy()
+
+    def call(n):
+        sel = list(range(n))
+        out = oracle.decode(w.q, k, v, w.block_tables, lens, w.scale, w.dtype, seqs=sel,
+                            threads=threads)
+        return {s: out[s] for s in sel}
+
+    def timed(n):
+        t0 = time.perf_counter()
+        call(n)
+        return time.perf_counter() - t0
+
+    call(1)                                              # first call: library and pages
+    one = timed(1)
+    if one > budget_s:
+        lens[0] = max(1, int(int(w.seq_lens[0]) * budget_s / one))
+        n = 1
+        what = f"the first {int(lens[0])} tokens of sequence 0"
+    else:
+        lo, hi = 1, 1
+        while hi < w.num_seqs:
+            hi = min(w.num_seqs, 2 * hi)
+            if timed(hi) > budget_s:
                 break
-        else:
-            reps += 1
-            if time.perf_counter() - t0 < budget_s:
-                continue
-        break
+            lo = hi
+        while hi - lo > 1:
+            mid = (lo + hi) // 2
+            if timed(mid) > budget_s:
+                hi = mid
+            else:
+                lo = mid
+        n = lo
+        what = ("all %d sequences" % n if n == w.num_seqs
+                else f"sequences 0..{n - 1} of {w.num_seqs}")
+    nbytes = int(sum(int(lens[s]) for s in range(n))) * per_tok
+    text = (f"fp64 oracle decode of {what} per step, one call on {threads} host threads "
+            f"(copy_blocks / reshape_and_cache applied once beforehand, untimed)")
+    return (lambda: call(n)), nbytes, threads, text
+
+
+def cpu_baseline(w, steps: int, warmup: int, budget_s: float = 10.0):
+    """The oracle's step (oracle_sample, sized exactly as --impl reference
+    sizes it for the same --steps/--warmup) repeated for ~budget_s."""
+    k, v = oracle_pool_after_step(w)
+    run, nbytes, threads, text = oracle_sample(w, k, v, oracle_step_budget(steps, warmup))
+    run()
+    reps = 0
+    t0 = time.perf_counter()
+    while True:
+        run()
+        reps += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
     dt = time.perf_counter() - t0
-    sample = (f"fp64 oracle step (copy/reshape once, then decode of {seqs} sequences in order, "
-              f"{reps} full passes) in {dt:.1f} s")
-    return done_bytes / dt / 1e9, sample, threads, rows
+    return {"value": nbytes * reps / dt / 1e9, "unit": "GB/s", "cores": threads,
+            "kind": "oracle", "sample": f"{text}; {reps} steps in {dt:.1f} s"}
 
 
+def parity_vs_oracle(w, out):
+    """The timed step's output (every sequence) against the oracle's step."""
+    import oracle
+    oracle.build()
+    k, v = oracle_pool_after_step(w)
+    t0 = time.perf_counter()
+    ref = oracle.decode(w.q, k, v, w.block_tables, w.seq_lens, w.scale, w.dtype)
+    dt = time.perf_counter() - t0
+    got = out.float().cpu().numpy().astype(np.float64)
+    err = float(np.abs(got - ref).max())
+    tol = 4e-3 if w.dtype == "f16" else 1.6e-2
+    return {"max_abs_err": err, "sequences": int(w.num_seqs), "tolerance": tol,
+            "ok": bool(np.isfinite(got).all() and err <= tol), "oracle_s": dt}
+
+
+# ---------------------------------------------------------------------------
+# pipelined end-to-end steps through the public API
+# ---------------------------------------------------------------------------
 def pipelined_e2e(inputs, out, bind, step, steps: int, device, before=None):
     """End-to-end steps through the public API with host buffers, pipelined
     the way a serving loop runs them.
@@ -498,6 +560,208 @@ def e2e_measure(st, steps: int, device, flush=None):
     return ms, h2d, d2h
 
 
+# ---------------------------------------------------------------------------
+# one decode workload, measured
+# ---------------------------------------------------------------------------
+def time_decode(st, w, args, device, big: bool, use_graph: bool):
+    """Device time of K steps, and the mean duration of one decode call.
+
+    big (K/V per step above twice L2): K steps run back to back, as a CUDA
+    graph of `spg` steps replayed K/spg times with no event node inside it
+    (an event-record node between two kernels would cut their programmatic
+    dependency), CUDA events around the replays.  After the timed region one
+    more replay of a second graph, with an event pair around every decode
+    call, gives the call durations the roofline uses.
+    Otherwise: L2 flushed (2 x L2 write) before every step; each step timed
+    alone with events around it and around its decode call.
+    Returns (elapsed ms over K steps, mean call ms, timing text)."""
+    import torch
+    K = args.steps
+    if big and use_graph:
+        spg = pick_steps_per_graph(K)
+        g = capture([st.run] * spg, device)
+        ev = [(timing_event(), timing_event()) for _ in range(spg)]
+        g_ev = capture([lambda e=e: st.run(e) for e in ev], device)
+        for _ in range(max(1, -(-args.warmup // spg))):
+            g.replay()
+        torch.cuda.synchronize(device)
+        barrier(device)
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for _ in range(K // spg):
+            g.replay()
+        t1.record()
+        torch.cuda.synchronize(device)
+        elapsed = t0.elapsed_time(t1)
+        g_ev.replay()
+        torch.cuda.synchronize(device)
+        call_ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
+        text = (f"CUDA graph of {spg} steps back to back (no event nodes), replayed {K // spg} "
+                f"times, CUDA events around the replays; call durations from one more replay "
+                f"of the same steps with an event pair around each decode call, after the "
+                f"timed region")
+        return elapsed, call_ms, text
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    if big:
+        for _ in range(args.warmup):
+            st.run()
+        torch.cuda.synchronize(device)
+        barrier(device)
+        t0.record()
+        for _ in range(K):
+            st.run()
+        t1.record()
+        torch.cuda.synchronize(device)
+        elapsed = t0.elapsed_time(t1)
+        calls = []
+        for _ in range(min(K, 32)):
+            st.run(e)
+            torch.cuda.synchronize(device)
+            calls.append(e[0].elapsed_time(e[1]))
+        return elapsed, float(np.mean(calls)), "eager steps back to back, CUDA events around them"
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=device)
+    for _ in range(args.warmup):
+        flush.zero_()
+        st.run()
+    torch.cuda.synchronize(device)
+    barrier(device)
+    elapsed, calls = 0.0, []
+    for _ in range(K):
+        flush.zero_()
+        t0.record()
+        st.run(e)
+        t1.record()
+        torch.cuda.synchronize(device)
+        elapsed += t0.elapsed_time(t1)
+        calls.append(e[0].elapsed_time(e[1]))
+    return (elapsed, float(np.mean(calls)),
+            "L2 flushed (2 x 129 MB write) before every step; each step timed alone with "
+            "CUDA events")
+
+
+def l2_carryover(w, st, args, device):
+    """Steps alternating between two copies of the workload in separate
+    buffers, so that no step finds the previous step's K/V in L2.  Returns the
+    alternating step time, to set against the repeated step's."""
+    import torch
+    st2 = Step(w, device, st.ps)
+    spg = 16
+    g = capture([st.run, st2.run] * (spg // 2), device)
+    for _ in range(max(1, -(-args.warmup // spg))):
+        g.replay()
+    torch.cuda.synchronize(device)
+    reps = max(1, args.steps // spg)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(reps):
+        g.replay()
+    t1.record()
+    torch.cuda.synchronize(device)
+    ms = t0.elapsed_time(t1) / (reps * spg)
+    del st2, g
+    return ms, reps * spg
+
+
+def measure_decode(name: str, args, device, rank: int, world: int, partition=None,
+                   headline: bool = False) -> dict:
+    """One decode workload on this rank's GPU: device-resident rate, end-to-end
+    rate through the public API, the decode call's roofline, the timed step's
+    output against the oracle (rank 0, N=1) and the clocks seen."""
+    import torch
+    import paged_kv_cache_260_gb300 as pa
+    ps = DEFAULT_PARTITION[name] if partition is None else partition
+    w = make_workload(name, rank)
+    st = Step(w, device, ps)
+    kv_bytes = w.kv_read_bytes()
+    # blocks that sequences share (parallel sampling) need leaving HBM once
+    # per step: the L2 decision and the HBM roofline count them once
+    unique_bytes = w.unique_kv_read_bytes()
+    big = unique_bytes > 2 * L2_BYTES
+    use_graph = timing_event() is not None and not args.no_graph
+    pa.get_device_error()
+    with ClockSampler(physical_gpu_index(dist_env()[2])) as clk:
+        elapsed, call_ms, timing_text = time_decode(st, w, args, device, big, use_graph)
+        barrier(device)
+    assert pa.get_device_error() == 0, f"{name}: a kernel recorded an error in the timed region"
+    t_max = dist_max(elapsed, device)
+    ms_per_step = t_max / args.steps
+    total_bytes = dist_sum(kv_bytes, device)
+    value = total_bytes / (ms_per_step * 1e-3) / 1e9
+    e2e_ms, h2d, d2h = e2e_measure(
+        st, max(20, min(args.steps, 300)), device,
+        None if big else torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=device))
+    e2e_ms = dist_max(e2e_ms, device)
+    peak, peak_src = measured_hbm_peak()
+    achieved = unique_bytes / (call_ms * 1e-3) / 1e9
+    carry = None
+    if headline and big and use_graph and not args.no_l2_check:
+        alt_ms, alt_steps = l2_carryover(w, st, args, device)
+        carry = {"ms_per_step_alternating": alt_ms, "steps": alt_steps,
+                 "ms_per_step_repeated": ms_per_step,
+                 "ratio": alt_ms / ms_per_step,
+                 "how": "the same steps alternating between two copies of the workload in "
+                        "separate buffers (no step finds the previous step's K/V in L2), "
+                        "against the same step repeated"}
+    parity = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        parity = parity_vs_oracle(w, st.out)
+    shared = unique_bytes != kv_bytes
+    res = {
+        "value": value,
+        "unit": "GB/s",
+        "ms_per_step": ms_per_step,
+        "pct_of_hbm_peak": 100.0 * unique_bytes / (ms_per_step * 1e-3) / 1e9 / peak,
+        "unique_gbps": dist_sum(unique_bytes, device) / (ms_per_step * 1e-3) / 1e9,
+        "seqs_per_s": dist_sum(w.num_seqs, device) / (ms_per_step * 1e-3),
+        "dtype": w.dtype,
+        "config": {
+            "workload": DESCRIPTION[name],
+            "name": name,
+            "num_seqs": w.num_seqs, "num_heads": w.num_heads, "num_kv_heads": w.num_kv_heads,
+            "head_dim": w.head_dim, "block_size": 16, "partition_size": ps,
+            "kv_bytes_per_step": kv_bytes,
+            "unique_kv_bytes_per_step": unique_bytes,
+            "step": ("copy_blocks + " if w.block_mapping is not None else "")
+                    + ("decode with reshape_and_cache fused (pa_decode_append)"
+                       if w.slot_mapping is not None else "decode") + " + merge",
+            "l2": ("inputs larger than L2 (K/V read per step %.0f MB vs 129 MB L2)"
+                   % (unique_bytes / 1e6) if big else
+                   "L2 flushed (2 x 129 MB write) before every step"),
+            "timing": timing_text,
+            "parallelism": "replicas" if world > 1 else "single GPU",
+        },
+        "e2e": {"value": total_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "roofline": {"bound": "hbm",
+                     "kernel": "decode_mma_kernel + merge kernel(s): one pa_decode / "
+                               "pa_decode_append call",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak,
+                     "peak_source": (peak_src + " (MEASURED_PEAKS.json hbm_gbs, copy burst)"
+                                     if peak_src == "measured" else "fallback 6.8 TB/s"),
+                     "algorithmic_bytes_per_launch": unique_bytes,
+                     "bytes_basis": ("unique blocks: a block that several sequences share "
+                                     "counts once" if shared else
+                                     "K and V of every live token and kv head"),
+                     "call_ms": call_ms,
+                     "traffic": ncu_traffic(name)},
+        "parity_vs_oracle": parity,
+        "pool_utilisation": pool_utilisation(w),
+        "gpu_launches": st.launches_per_step * args.steps,
+        "clocks": clk.summary(),
+    }
+    if shared:
+        res["logical_kv_gbps"] = value
+    if carry is not None:
+        res["l2_carryover"] = carry
+    res["_w"] = w
+    return res
+
+
+NESTED = ("long", "mha7b", "parsamp", "tiny")
+
+
 def run_ours(args):
     import torch
     rank, world = dist_init("nccl" if torch.cuda.is_available() else "gloo")
@@ -509,140 +773,38 @@ def run_ours(args):
     import paged_kv_cache_260_gb300 as pa
     pa.load()
 
-    ps = DEFAULT_PARTITION[args.workload] if args.partition is None else args.partition
-    w = make_workload(args.workload, rank)
-    st = Step(w, device, ps)
-    kv_bytes = w.kv_read_bytes()
-    # blocks shared between sequences (parallel sampling) are read once per
-    # step from HBM at best; the L2 decision and the HBM figure use them once
-    unique_bytes = w.unique_kv_read_bytes()
-    l2_ok = unique_bytes > 2 * L2_BYTES
-    spg = pick_steps_per_graph(args.steps)
-    use_graph = timing_event() is not None and not args.no_graph
-    if use_graph:
-        st.ev = None
-        st.capture(spg)
-        replays = args.steps // spg
-        for _ in range(max(1, -(-args.warmup // spg))):
-            st.graph.replay()
-        st.graph_ev.replay()
-    else:
-        ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-        for _ in range(args.warmup):
-            st.run()
-    torch.cuda.synchronize(device)
-    assert pa.get_device_error() == 0, "a kernel recorded an error during warm-up"
-
-    flush = None if l2_ok else torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=device)
-    dec_ms = []
-    with ClockSampler(physical_gpu_index(local)) as clk:
-        barrier(device)
-        t0 = torch.cuda.Event(enable_timing=True)
-        t1 = torch.cuda.Event(enable_timing=True)
-        if flush is None:
-            t0.record()
-            if use_graph:
-                # the last replay is the graph with an event pair around each
-                # call, whose timestamps give the roofline its call durations
-                for _ in range(replays - 1):
-                    st.graph.replay()
-                st.graph_ev.replay()
-            else:
-                for _ in range(args.steps):
-                    st.run(ev)
-            t1.record()
-            torch.cuda.synchronize(device)
-            elapsed = t0.elapsed_time(t1)
-            dec_ms.append(st.decode_ms() if use_graph else ev[0].elapsed_time(ev[1]))
-        else:
-            # small working set: flush L2 before every step, time the steps only
-            elapsed = 0.0
-            ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-            for _ in range(args.steps):
-                flush.zero_()
-                t0.record()
-                st.run(ev)
-                t1.record()
-                torch.cuda.synchronize(device)
-                elapsed += t0.elapsed_time(t1)
-                dec_ms.append(ev[0].elapsed_time(ev[1]))
-        barrier(device)
-    assert pa.get_device_error() == 0, "a kernel recorded an error in the timed region"
-    t_max = dist_max(elapsed, device)
-    ms_per_step = t_max / args.steps
-    total_bytes = dist_sum(kv_bytes, device)
-    total_seqs = dist_sum(w.num_seqs, device)
-    value = total_bytes / (ms_per_step * 1e-3) / 1e9
-    dec = float(np.mean(dec_ms))
-
-    e2e_ms, h2d, d2h = e2e_measure(st, max(20, min(args.steps, 300)), device, flush)
-    e2e_ms = dist_max(e2e_ms, device)
-    peak, peak_src = measured_hbm_peak()
-    achieved = kv_bytes / (dec * 1e-3) / 1e9
-    traffic = ncu_traffic(args.workload)
+    head_name = args.workload or "gqa8b"
+    head = measure_decode(head_name, args, device, rank, world, args.partition, headline=True)
+    w = head.pop("_w")
     cpu = None
-    parity = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, sample, cores, rows = cpu_baseline(w)
-        cpu = {"value": v, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample}
-        if args.workload == "tiny":
-            v1, sample1, _, _ = cpu_baseline(w, budget_s=3.0, threads=1)
-            cpu["single_core"] = {"value": v1, "unit": "GB/s", "cores": 1, "sample": sample1}
-        # the timed step's own output against the oracle rows the sample computed
-        got = st.out.float().cpu().numpy().astype(np.float64)
-        err = max(float(np.abs(got[s] - r).max()) for s, r in rows.items())
-        parity = {"max_abs_err": err, "sequences": len(rows),
-                  "tolerance": 4e-3 if w.dtype == "f16" else 1.6e-2, "ok": err <= (4e-3 if w.dtype == "f16" else 1.6e-2)}
+        cpu = cpu_baseline(w, args.steps, args.warmup)
+    nested = {}
+    if args.workload is None and not args.only_headline:
+        for name in NESTED:
+            r = measure_decode(name, args, device, rank, world)
+            r.pop("_w")
+            nested[name] = r
     if rank != 0:
         return
     line = {
         "metric": METRIC,
-        "value": value,
+        "value": head["value"],
         "unit": "GB/s",
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": ms_per_step,
+        "ms_per_step": head["ms_per_step"],
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": w.dtype,
         "data": "synthetic (seeded N(0,1) q/K/V, random block permutation)",
-        "pct_of_hbm_peak": 100.0 * value / world / peak,
-        "unique_gbps": dist_sum(unique_bytes, device) / (ms_per_step * 1e-3) / 1e9,
-        "seqs_per_s": total_seqs / (ms_per_step * 1e-3),
-        "config": {
-            "workload": DESCRIPTION[args.workload],
-            "name": args.workload,
-            "num_seqs": w.num_seqs, "num_heads": w.num_heads, "num_kv_heads": w.num_kv_heads,
-            "head_dim": w.head_dim, "block_size": 16, "partition_size": ps,
-            "kv_bytes_per_step": kv_bytes,
-            "unique_kv_bytes_per_step": unique_bytes,
-            "step": ("copy_blocks + " if w.block_mapping is not None else "")
-                    + ("decode with reshape_and_cache fused (pa_decode_append)"
-                       if w.slot_mapping is not None else "decode") + " + merge",
-            "l2": ("inputs larger than L2 (KV read per step %.0f MB vs 129 MB L2)" % (unique_bytes / 1e6)
-                   if l2_ok else "L2 flushed (258 MB write) before every step; steps timed alone"),
-            "timing": ("CUDA graph of %d steps back to back, replayed %d times, CUDA events around "
-                       "the replays; the last replay has an event pair around each call, which "
-                       "gives the roofline its call duration" % (spg, args.steps // spg)
-                       if use_graph and l2_ok else "CUDA events per step"),
-            "parallelism": "replicas" if world > 1 else "single GPU",
-        },
-        "e2e": {"value": total_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
-                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "roofline": {"bound": "hbm", "kernel": "decode_mma_kernel + merge kernel(s) (one pa_decode / pa_decode_append call)",
-                     "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs, copy burst)"
-                     if peak_src == "measured" else "fallback 6.8 TB/s",
-                     "algorithmic_bytes_per_launch": kv_bytes, "decode_ms": dec,
-                     "traffic": traffic},
-        "cpu_baseline": cpu,
-        "parity_vs_oracle": parity,
-        "pool_utilisation": pool_utilisation(w),
-        "gpu_launches": st.launches_per_step * args.steps,
-        "clocks": clk.summary(),
     }
+    line.update({k: v for k, v in head.items() if k not in ("value", "unit", "ms_per_step", "dtype")})
+    line["cpu_baseline"] = cpu
+    if nested:
+        line["workloads"] = nested
     print(json.dumps(line), flush=True)
 
 
@@ -755,27 +917,78 @@ def prefill_flops(w, rows=None):
     return 4 * w.head_dim * w.num_heads * total
 
 
-def prefill_cpu_baseline(w, rows=32):
-    """The fp64 oracle on the last `rows` rows of every chunk (a prefill whose
-    chunks are those rows, over the same contexts)."""
-    import oracle
-    oracle.build()
-    threads = min(oracle.num_threads(), w.num_seqs)
-    idx = []
-    qs = [0]
+def prefill_oracle_rows(w, rows):
+    """The query rows of a prefill sample: the last `rows` rows of every chunk
+    (a prefill whose chunks are those rows, over the same contexts).
+    Returns (row indices, query starts of the sample)."""
+    idx, qs = [], [0]
     for s in range(w.num_seqs):
         a, b = int(w.query_start[s]), int(w.query_start[s + 1])
         r = min(rows, b - a)
         idx.extend(range(b - r, b))
         qs.append(qs[-1] + r)
-    q = np.ascontiguousarray(w.q[idx])
+    return idx, np.array(qs, np.int32)
+
+
+def prefill_oracle_sample(w, budget_s: float):
+    """The oracle's prefill step on the host cores: the fp64 oracle on the last
+    r rows of every chunk, r the most rows whose call fits `budget_s` (one
+    row timed first).  cpu_baseline and --impl reference use this same step.
+    Returns (run, flops per step, threads, text, row indices)."""
+    import oracle
+    oracle.build()
+    threads = min(oracle.num_threads(), w.num_seqs)
+
+    def make(rows):
+        idx, qs = prefill_oracle_rows(w, rows)
+        q = np.ascontiguousarray(w.q[idx])
+        return (lambda: oracle.prefill(q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, qs,
+                                       w.scale, w.dtype, threads=threads)), idx
+
+    run1, _ = make(1)
+    run1()
     t0 = time.perf_counter()
-    ref = oracle.prefill(q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens,
-                         np.array(qs, np.int32), w.scale, w.dtype, threads=threads)
+    run1()
+    one = max(1e-4, time.perf_counter() - t0)
+    max_chunk = int(np.diff(w.query_start).max())
+    rows = int(max(1, min(max_chunk, budget_s / one)))
+    run, idx = make(rows)
+    text = (f"fp64 oracle prefill of the last {rows} rows of each of the {w.num_seqs} chunks "
+            f"per step ({len(idx)} rows x {w.num_heads} heads), {threads} host threads")
+    return run, prefill_flops(w, rows), threads, text, idx
+
+
+def prefill_cpu_baseline(w, steps: int, warmup: int, budget_s: float = 10.0):
+    """The oracle's prefill step (prefill_oracle_sample, sized as --impl
+    reference sizes it) repeated for ~budget_s."""
+    run, flops, threads, text, _ = prefill_oracle_sample(
+        w, max(0.05, min(2.0, 90.0 / max(1, steps + warmup))))
+    reps = 0
+    t0 = time.perf_counter()
+    while True:
+        run()
+        reps += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
     dt = time.perf_counter() - t0
-    sample = (f"fp64 oracle prefill of the last {rows} rows of each of the {w.num_seqs} chunks "
-              f"({len(idx)} rows x {w.num_heads} heads) in {dt:.1f} s")
-    return prefill_flops(w, rows) / dt / 1e12, sample, threads, (idx, ref)
+    return {"value": flops * reps / dt / 1e12, "unit": "TFLOP/s", "cores": threads,
+            "kind": "oracle", "sample": f"{text}; {reps} steps in {dt:.1f} s"}
+
+
+def prefill_parity(w, out, rows=32):
+    """The last `rows` rows of every chunk of the timed prefill's output
+    against the oracle's."""
+    import oracle
+    oracle.build()
+    idx, qs = prefill_oracle_rows(w, rows)
+    ref = oracle.prefill(np.ascontiguousarray(w.q[idx]), w.k_cache, w.v_cache, w.block_tables,
+                         w.seq_lens, qs, w.scale, w.dtype,
+                         threads=min(oracle.num_threads(), w.num_seqs))
+    got = out.float().cpu().numpy().astype(np.float64)[idx]
+    err = float(np.abs(got - ref).max())
+    tol = 4e-3 if w.dtype == "f16" else 1.6e-2
+    return {"max_abs_err": err, "rows": len(idx), "tolerance": tol,
+            "ok": bool(np.isfinite(got).all() and err <= tol)}
 
 
 def run_prefill(args):
@@ -854,12 +1067,8 @@ def run_prefill(args):
     cpu = None
     parity = None
     if not args.no_cpu_baseline:
-        cv, sample, cores, (idx, ref) = prefill_cpu_baseline(w)
-        cpu = {"value": cv, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample}
-        got = out.float().cpu().numpy().astype(np.float64)[idx]
-        err = float(np.abs(got - ref).max())
-        tol = 4e-3 if w.dtype == "f16" else 1.6e-2
-        parity = {"max_abs_err": err, "rows": len(idx), "tolerance": tol, "ok": err <= tol}
+        cpu = prefill_cpu_baseline(w, args.steps, args.warmup)
+        parity = prefill_parity(w, out)
     print(json.dumps({
         "metric": PREFILL_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": 1,
         "steps": steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
@@ -883,117 +1092,55 @@ def run_prefill(args):
 
 
 def run_reference(args):
-    """The oracle as the reference arm: W untimed and K timed steps, each a
-    bounded sample of the workload (its first sequences in order, or a prefix
-    of the first sequence when one sequence is more than a step's share),
-    sized so that the whole run takes about two minutes."""
+    """The oracle as the reference arm: W untimed and K timed steps of the
+    oracle's step (oracle_sample: one fp64 decode call over the first n
+    sequences, sized so that the whole run takes about two minutes), the same
+    step cpu_baseline times in our arm's line."""
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    import oracle
-    oracle.build()
-    w = make_workload(args.workload, 0)
-    per_seq = 2 * w.num_kv_heads * w.head_dim * 2
-    budget = 120.0 / max(1, args.steps + args.warmup)   # seconds per step
-    # small samples run on one thread: starting threads would dominate them
-    threads = 1 if budget < 0.05 else oracle.num_threads()
-
-    def run(sel, lens):
-        oracle.decode(w.q, w.k_cache, w.v_cache, w.block_tables, lens, w.scale, w.dtype,
-                      seqs=sel, threads=threads)
-
-    lens = w.seq_lens.copy()
-
-    def timed(n):
-        t0 = time.perf_counter()
-        run(list(range(n)), lens)
-        return time.perf_counter() - t0
-
-    # the largest prefix of sequences whose sample fits a step's share
-    # (timed, since lengths differ): doubling, then bisection
-    run([0], lens)                                       # first call: library and pages
-    one = timed(1)
-    if one > budget:
-        lens[0] = max(1, int(int(w.seq_lens[0]) * budget / one))
-        n = 1
-        sample = f"fp64 oracle decode of the first {int(lens[0])} tokens of sequence 0 per step"
-    else:
-        lo, hi = 1, 1
-        while hi < w.num_seqs:
-            hi = min(w.num_seqs, 2 * hi)
-            if timed(hi) > budget:
-                break
-            lo = hi
-        while hi - lo > 1:
-            mid = (lo + hi) // 2
-            if timed(mid) > budget:
-                hi = mid
-            else:
-                lo = mid
-        n = lo
-        sample = f"fp64 oracle decode of sequences 0..{n - 1} of the workload per step"
-    sel = list(range(n))
+    w = make_workload(args.workload or "gqa8b", 0)
+    k, v = oracle_pool_after_step(w)
+    run, nbytes, threads, text = oracle_sample(w, k, v,
+                                               oracle_step_budget(args.steps, args.warmup))
     for _ in range(args.warmup):
-        run(sel, lens)
+        run()
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        run(sel, lens)
+        run()
     dt = time.perf_counter() - t0
-    b = sum(int(lens[s]) for s in sel) * per_seq
-    value = b * args.steps / dt / 1e9
+    value = nbytes * args.steps / dt / 1e9
+    name = args.workload or "gqa8b"
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": DESCRIPTION[args.workload], "name": args.workload},
+        "config": {"workload": DESCRIPTION[name], "name": name},
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
-                         "sample": sample},
+                         "sample": text},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
 
 
 def run_reference_prefill(args):
     """The oracle as the reference arm of the prefill line: W untimed and K
-    timed steps, each the fp64 oracle on the last r rows of every chunk, r
-    sized so that the whole run takes about 90 s."""
+    timed steps of the oracle's prefill step (prefill_oracle_sample), sized so
+    that the whole run takes about 90 s."""
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    import oracle
     import synth
-    oracle.build()
     w = synth.by_name(args.workload)
-    threads = min(oracle.num_threads(), w.num_seqs)
-    budget = max(0.05, 90.0 / max(1, args.steps + args.warmup))   # seconds per step
-
-    def sample(rows):
-        idx, qs = [], [0]
-        for s in range(w.num_seqs):
-            a, b = int(w.query_start[s]), int(w.query_start[s + 1])
-            r = min(rows, b - a)
-            idx.extend(range(b - r, b))
-            qs.append(qs[-1] + r)
-        q = np.ascontiguousarray(w.q[idx])
-        qs = np.array(qs, np.int32)
-        return lambda: oracle.prefill(q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, qs,
-                                      w.scale, w.dtype, threads=threads)
-
-    t0 = time.perf_counter()
-    sample(1)()
-    one = max(1e-4, time.perf_counter() - t0)
-    max_chunk = int(np.diff(w.query_start).max())
-    rows = int(max(1, min(max_chunk, budget / one)))
-    step = sample(rows)
+    run, flops, threads, text, _ = prefill_oracle_sample(
+        w, max(0.05, min(2.0, 90.0 / max(1, args.steps + args.warmup))))
     for _ in range(args.warmup):
-        step()
+        run()
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        step()
+        run()
     dt = time.perf_counter() - t0
-    value = prefill_flops(w, rows) * args.steps / dt / 1e12
-    text = (f"fp64 oracle prefill of the last {rows} rows of each of the {w.num_seqs} chunks "
-            f"per step")
+    value = flops * args.steps / dt / 1e12
     print(json.dumps({
         "impl": "reference", "metric": PREFILL_METRIC, "value": value, "unit": "TFLOP/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -1010,20 +1157,25 @@ def run_reference_prefill(args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
-    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=list(DESCRIPTION) + ["swap", "prefill", "prefill_long"],
-                    default="gqa8b")
+                    default=None,
+                    help="one workload alone (default: the GQA batch-128 headline, with the "
+                         "other decode workloads nested in the same line)")
     ap.add_argument("--partition", type=int, default=None,
                     help="-1 no split, 0 balanced split, >0 fixed partition tokens")
     ap.add_argument("--no-graph", action="store_true")
-    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true",
+                    help="skip the oracle legs (cpu_baseline and parity)")
+    ap.add_argument("--no-l2-check", action="store_true")
+    ap.add_argument("--only-headline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
-        if args.workload.startswith("prefill"):
+        if args.workload and args.workload.startswith("prefill"):
             run_reference_prefill(args)
         elif args.workload == "swap":
             print(json.dumps({"impl": "reference", "unavailable": "swap_blocks moves bytes "
@@ -1032,7 +1184,7 @@ def main(argv=None):
             run_reference(args)
     elif args.workload == "swap":
         run_swap(args)
-    elif args.workload.startswith("prefill"):
+    elif args.workload and args.workload.startswith("prefill"):
         run_prefill(args)
     else:
         run_ours(args)

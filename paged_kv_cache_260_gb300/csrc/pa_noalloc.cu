@@ -11,6 +11,7 @@
 //
 // The array is loaded with the library's device code: every GPU that loads
 // the library holds kNoAllocScratchBytes of it until the process exits.
+#include <atomic>
 #include <mutex>
 #include <stdint.h>
 
@@ -27,23 +28,30 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 
 constexpr int kMaxDevices = 64;
 std::mutex g_noalloc_mutex;
-void *g_noalloc_ptr[kMaxDevices];   // device address of the array, per device
+std::atomic<void *> g_noalloc_ptr[kMaxDevices];   // device address of the array, per device
 
-// One-time set-up per device, with that device current: the array's name is
-// only a host-side stand-in, so look up its real device address.
+// The array's device address on the current device.  The array's name is
+// only a host-side stand-in, so the first call on a device looks the real
+// address up (with that device current) under a lock; later calls read the
+// cached pointer without one.
 int scratch_address(void **out)
 {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    if (cudaGetDevice(&dev) != cudaSuccess)
         return PA_ERR_CUDA;
-    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-    if (!g_noalloc_ptr[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p)
-            return PA_ERR_CUDA;
-        g_noalloc_ptr[dev] = p;
+    if (dev < 0 || dev >= kMaxDevices)
+        return PA_ERR_UNSUPPORTED;
+    void *p = g_noalloc_ptr[dev].load(std::memory_order_acquire);
+    if (!p) {
+        std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+        p = g_noalloc_ptr[dev].load(std::memory_order_relaxed);
+        if (!p) {
+            if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p)
+                return PA_ERR_CUDA;
+            g_noalloc_ptr[dev].store(p, std::memory_order_release);
+        }
     }
-    *out = g_noalloc_ptr[dev];
+    *out = p;
     return PA_OK;
 }
 
@@ -57,10 +65,9 @@ extern "C" int pa_decode_noalloc(void *out, const void *q, const void *k_cache,
                                  int max_blocks_per_seq, int num_blocks, float scale, int dtype,
                                  void *stream)
 {
-    if (num_seqs == 0)
-        return PA_OK;
     // The balanced split's scratch never needs clearing: every call writes
     // each worker's cut descriptor and every partial row before reading it.
+    // An empty batch needs no scratch; pa_decode still checks its arguments.
     const size_t need = pa_decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim,
                                                  max_blocks_per_seq, 0);
     if (need > pa::kNoAllocScratchBytes)
