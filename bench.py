@@ -528,36 +528,52 @@ def pipelined_e2e(inputs, out, bind, step, steps: int, device, before=None):
     return a.elapsed_time(z) / steps, h2d, d2h, outs_h[(count[0] - 1) % 2].clone()
 
 
-def e2e_measure(st, steps: int, device, flush=None):
+def e2e_measure(st, steps: int, device, rotate_pools: bool = False):
     """The decode step end to end (pipelined_e2e): q, tables, lengths, the new
     tokens, their slots and the copy-on-write pairs come in from one packed
-    pinned host buffer, the output goes back.  `flush`, when given, is
-    zeroed ahead of every step, as the device-resident timing does for
-    working sets that L2 could hold.  The last step's host output must equal
-    the device-resident step's, bit for bit.  Returns (ms per step, h2d
-    bytes, d2h bytes)."""
+    pinned host buffer, the output goes back.  With `rotate_pools` (working
+    sets that L2 could hold) the steps cycle through copies of the pool whose
+    sizes add up to at least twice L2, so that no step finds the K/V it reads
+    left in L2 by an earlier step -- the end-to-end counterpart of the L2
+    flush before every device-timed step, without a flush inside the timed
+    region.  The last step's host output must equal the device-resident
+    step's, bit for bit.  Returns (ms per step, h2d bytes, d2h bytes, pool
+    copies)."""
     import torch
     names = [n for n in ["q", "tables", "lens", "k_new", "v_new", "slots", "pairs"]
              if getattr(st, n) is not None]
     saved = [getattr(st, n) for n in names]
     saved_out = st.out
+    saved_pool = (st.k, st.v)
+    pools = [saved_pool]
+    if rotate_pools:
+        pool_bytes = 2 * st.k.numel() * st.k.element_size()
+        copies = min(64, max(2, -(-2 * L2_BYTES // pool_bytes)))
+        pools += [(st.k.clone(), st.v.clone()) for _ in range(copies - 1)]
+    turn = [0]
 
     def bind(views, out_buf):
         for n, v in zip(names, views):
             setattr(st, n, v)
         st.out = out_buf
+        st.k, st.v = pools[turn[0] % len(pools)]
+        turn[0] += 1
 
     try:
-        ms, h2d, d2h, last = pipelined_e2e(saved, saved_out, bind, st.run, steps, device,
-                                           before=None if flush is None else flush.zero_)
+        ms, h2d, d2h, last = pipelined_e2e(saved, saved_out, bind, st.run, steps, device)
     finally:
-        bind(saved, saved_out)
+        for n, v in zip(names, saved):
+            setattr(st, n, v)
+        st.out = saved_out
+        st.k, st.v = saved_pool
+    copies = len(pools)
+    del pools
     st.run()
     torch.cuda.synchronize(device)
     if not torch.equal(st.out.cpu(), last):
         raise RuntimeError("the pipelined end-to-end step's output differs from the "
                            "device-resident step's")
-    return ms, h2d, d2h
+    return ms, h2d, d2h, copies
 
 
 # ---------------------------------------------------------------------------
@@ -621,23 +637,37 @@ def time_decode(st, w, args, device, big: bool, use_graph: bool):
             calls.append(e[0].elapsed_time(e[1]))
         return elapsed, float(np.mean(calls)), "eager steps back to back, CUDA events around them"
     flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=device)
+    # a step timed alone would otherwise wait for the host between launches:
+    # each step is one CUDA-graph replay (or, without graphs, eager launches)
+    if use_graph:
+        e = (timing_event(), timing_event())      # recorded inside a graph: external
+        g1 = capture([st.run], device)
+        g1_ev = capture([lambda: st.run(e)], device)
+        one, one_ev = g1.replay, g1_ev.replay
+    else:
+        one, one_ev = st.run, (lambda: st.run(e))
     for _ in range(args.warmup):
         flush.zero_()
-        st.run()
+        one()
     torch.cuda.synchronize(device)
     barrier(device)
     elapsed, calls = 0.0, []
     for _ in range(K):
         flush.zero_()
         t0.record()
-        st.run(e)
+        one()
         t1.record()
         torch.cuda.synchronize(device)
         elapsed += t0.elapsed_time(t1)
+    for _ in range(min(K, 32)):
+        flush.zero_()
+        one_ev()
+        torch.cuda.synchronize(device)
         calls.append(e[0].elapsed_time(e[1]))
     return (elapsed, float(np.mean(calls)),
             "L2 flushed (2 x 129 MB write) before every step; each step timed alone with "
-            "CUDA events")
+            "CUDA events" + (", replayed as a CUDA graph of the step" if use_graph else "")
+            + "; call durations from separate replays with an event pair around the decode call")
 
 
 def l2_carryover(w, st, args, device):
@@ -688,9 +718,8 @@ def measure_decode(name: str, args, device, rank: int, world: int, partition=Non
     ms_per_step = t_max / args.steps
     total_bytes = dist_sum(kv_bytes, device)
     value = total_bytes / (ms_per_step * 1e-3) / 1e9
-    e2e_ms, h2d, d2h = e2e_measure(
-        st, max(20, min(args.steps, 300)), device,
-        None if big else torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=device))
+    e2e_ms, h2d, d2h, copies = e2e_measure(st, max(20, min(args.steps, 300)), device,
+                                           rotate_pools=not big)
     e2e_ms = dist_max(e2e_ms, device)
     peak, peak_src = measured_hbm_peak()
     achieved = unique_bytes / (call_ms * 1e-3) / 1e9
@@ -732,7 +761,10 @@ def measure_decode(name: str, args, device, rank: int, world: int, partition=Non
             "parallelism": "replicas" if world > 1 else "single GPU",
         },
         "e2e": {"value": total_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
-                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "l2": ("inputs larger than L2" if big else
+                       f"steps cycle through {copies} copies of the pool (>= 2 x L2 in all), "
+                       f"no flush in the timed region")},
         "roofline": {"bound": "hbm",
                      "kernel": "decode_mma_kernel + merge kernel(s): one pa_decode / "
                                "pa_decode_append call",

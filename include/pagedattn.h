@@ -22,7 +22,7 @@
  *    physical block block_tables[s][t / block_size] at offset
  *    t % block_size; slot numbers are block * block_size + offset.
  *  - block_size must be 16; head_dim 64 or 128; num_heads a multiple of
- *    num_kv_heads with a group G = num_heads / num_kv_heads of 1..8.  Query
+ *    num_kv_heads with a group G = num_heads / num_kv_heads of 1..16.  Query
  *    head h reads kv head h / G (grouped-query attention: several query heads
  *    share one K/V head, ICML tutorial notes, section "Attention 简化与 KV Cache
  *    优化").
@@ -71,9 +71,13 @@ int pa_version(void);
 const char *pa_status_string(int status);
 
 /*
- * Bytes of device workspace pa_decode needs for these sizes (0 when none).
- * partition_size selects the split-K mode exactly as in pa_decode.  The value
- * depends on the current device's SM count for partition_size == 0.
+ * Library plumbing, no passage of the pages behind it: bytes of device
+ * workspace pa_decode needs for these sizes (0 when none).  partition_size
+ * selects the split-K mode exactly as in pa_decode.  The value depends on the
+ * current device's SM count for the split modes.  It takes max_blocks_per_seq
+ * (the block-table row length, which bounds every sequence's length) rather
+ * than a maximum sequence length, because that is the figure pa_decode itself
+ * receives.
  */
 size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads,
                                 int head_dim, int max_blocks_per_seq,
@@ -123,7 +127,12 @@ size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads,
  *
  * workspace: device buffer of at least pa_decode_workspace_size(...) bytes,
  * 256-byte aligned, caller-owned; its contents need no initialisation.  Calls
- * that share a workspace must be ordered on one stream.
+ * that share a workspace must be ordered on one stream.  The split modes
+ * always need one; with no split (-1) a workspace is needed only for batches
+ * of more than 2048 sequences, whose per-sequence lengths and tile prefix a
+ * one-block kernel builds there first (smaller batches keep them in shared
+ * memory).  A batch has no size limit beyond 32-bit tile indices
+ * (num_seqs * max_blocks_per_seq * num_kv_heads < 2^31).
  */
 int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
               const int32_t *block_tables, const int32_t *seq_lens,
@@ -167,9 +176,12 @@ int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache
  *
  * workspace (optional, 256-byte aligned, caller-owned, no initialisation
  * needed): at least pa_prefill_workspace_size(...) bytes.  With it a small
- * planning kernel first sorts the (sequence, query tile) work by its length,
- * longest first, so the grid ends on short work (the greedy longest-first
- * schedule); without it (NULL) the work runs in a fixed order.  Results are
+ * planning kernel first orders the (sequence, query tile) work: longest
+ * first when the batch's K/V fits in L2, so the grid ends on short work (the
+ * greedy longest-first schedule); otherwise sequence by sequence, each
+ * sequence's kv heads one after the other with all of its query tiles, so
+ * that the blocks running together share one head's K/V through L2.
+ * Without it (NULL) the work runs in a fixed order.  Results are
  * bit-identical either way.  Calls sharing a workspace must be ordered on
  * one stream.  PA_ERR_WORKSPACE if it is too small or misaligned.
  */
@@ -317,8 +329,9 @@ int pa_gather_kv(void *k_out, void *v_out, const void *k_cache, const void *v_ca
                  int max_blocks_per_seq, int num_blocks, int dtype, void *stream);
 
 /*
- * Check the tables a decode would read: counts, into *bad_count (a device
- * uint32 the caller zeroes), the entries block_tables[s][b] with
+ * Library plumbing, no passage of the pages behind it.  Check the tables a
+ * decode would read: counts, into *bad_count (a device uint32 the caller
+ * zeroes), the entries block_tables[s][b] with
  * b < ceil(seq_lens[s]/16) outside [0, num_blocks), plus the sequences whose
  * length is outside [0, max_blocks_per_seq*16].
  */
@@ -335,9 +348,13 @@ int pa_validate_tables(const int32_t *block_tables, const int32_t *seq_lens,
 int pa_selftest_bounded_wait(int limit_us, void *stream);
 
 /*
- * Synchronise `stream`, return in *bits the PA_DEVERR_* bits kernels on the
- * current device have recorded since the last clear, and clear them when
- * `clear` is non-zero.  Returns PA_ERR_DEVICE when bits is non-zero.
+ * Library plumbing, no passage of the pages behind it.  Synchronise `stream`,
+ * return in *bits the PA_DEVERR_* bits kernels on the current device have
+ * recorded since the last clear, and clear them when `clear` is non-zero.
+ * Returns PA_ERR_DEVICE when bits is non-zero.  An expired bounded wait is
+ * one of those bits (PA_DEVERR_TIMEOUT) rather than a status of its own: the
+ * kernel that gave up has long returned when the host asks, and it may have
+ * recorded other bits too.
  */
 int pa_get_device_error(void *stream, uint32_t *bits, int clear);
 

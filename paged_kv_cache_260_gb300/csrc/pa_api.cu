@@ -234,7 +234,9 @@ int check_common(int num_kv_heads, int head_dim, int block_size, int num_blocks,
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? PA_OK : PA_ERR_CUDA; }
 
 struct WorkspaceLayout {
-    size_t m_off, l_off, o_off, sm_off, sl_off, so_off, desc_off, total;
+    size_t m_off, l_off, o_off, sm_off, sl_off, so_off, desc_off, pre_off, lens_off, share_off,
+        total;
+    bool seq_global;
 };
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -244,31 +246,44 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 //   (x head_dim for o) -- the documented layout;
 //   both split modes: m, l, o of two slots per worker and query head of the
 //   group (a worker's first and last pieces are the only ones that can be
-//   cut), then one cut descriptor per worker.
+//   cut), then one cut descriptor per worker;
+//   any mode, batches above kSeqsInSmem: the unit prefix [num_seqs + 1] and
+//   the clamped lengths [num_seqs], int32, and the first-block-shared flags
+//   [num_seqs] plus one "any flag set" byte, built by the prep kernel.
 WorkspaceLayout workspace_layout(int mode, int num_seqs, int num_heads, int num_kv_heads,
                                  int head_dim, int p_max, int workers)
 {
     WorkspaceLayout w{};
-    if (mode == kModeWhole)
-        return w;
-    const int group = num_heads / num_kv_heads;
-    const size_t prow = mode == kModeFixed ? (size_t)num_seqs * num_heads * p_max : 0;
-    const size_t srow = 2 * (size_t)workers * group;
     size_t at = 0;
-    w.m_off = at;
-    at = round_up(at + sizeof(float) * prow, 256);
-    w.l_off = at;
-    at = round_up(at + sizeof(float) * prow, 256);
-    w.o_off = at;
-    at = round_up(at + sizeof(float) * prow * head_dim, 256);
-    w.sm_off = at;
-    at = round_up(at + sizeof(float) * srow, 256);
-    w.sl_off = at;
-    at = round_up(at + sizeof(float) * srow, 256);
-    w.so_off = at;
-    at = round_up(at + sizeof(float) * srow * head_dim, 256);
-    w.desc_off = at;
-    w.total = round_up(at + sizeof(CutDesc) * workers, 256);
+    if (mode != kModeWhole) {
+        const int group = num_heads / num_kv_heads;
+        const size_t prow = mode == kModeFixed ? (size_t)num_seqs * num_heads * p_max : 0;
+        const size_t srow = 2 * (size_t)workers * group;
+        w.m_off = at;
+        at = round_up(at + sizeof(float) * prow, 256);
+        w.l_off = at;
+        at = round_up(at + sizeof(float) * prow, 256);
+        w.o_off = at;
+        at = round_up(at + sizeof(float) * prow * head_dim, 256);
+        w.sm_off = at;
+        at = round_up(at + sizeof(float) * srow, 256);
+        w.sl_off = at;
+        at = round_up(at + sizeof(float) * srow, 256);
+        w.so_off = at;
+        at = round_up(at + sizeof(float) * srow * head_dim, 256);
+        w.desc_off = at;
+        at = round_up(at + sizeof(CutDesc) * workers, 256);
+    }
+    if (num_seqs > kSeqsInSmem) {
+        w.seq_global = true;
+        w.pre_off = at;
+        at = round_up(at + sizeof(int32_t) * ((size_t)num_seqs + 1), 256);
+        w.lens_off = at;
+        at = round_up(at + sizeof(int32_t) * (size_t)num_seqs, 256);
+        w.share_off = at;
+        at = round_up(at + (size_t)num_seqs + 1, 256);
+    }
+    w.total = at;
     return w;
 }
 
@@ -352,7 +367,7 @@ static int decode_impl(void *out, const void *q, const void *k_cache, const void
     if (num_heads % num_kv_heads)
         return PA_ERR_INVALID_ARG;
     const int group = num_heads / num_kv_heads;
-    if (group > 8 || num_seqs > kMaxSeqs)
+    if (group > kMaxGroup)
         return PA_ERR_UNSUPPORTED;
     if (num_seqs == 0)
         return PA_OK;
@@ -372,8 +387,13 @@ static int decode_impl(void *out, const void *q, const void *k_cache, const void
         return rc;
 
     KernelSet ks{};
-    const bool found = dtype == PA_DTYPE_F16 ? decode_kernels_f16(head_dim, group, &ks)
-                                             : decode_kernels_bf16(head_dim, group, &ks);
+    bool found;
+    if (group <= 8)
+        found = dtype == PA_DTYPE_F16 ? decode_kernels_f16(head_dim, &ks)
+                                      : decode_kernels_bf16(head_dim, &ks);
+    else
+        found = dtype == PA_DTYPE_F16 ? decode_kernels_f16_g16(head_dim, &ks)
+                                      : decode_kernels_bf16_g16(head_dim, &ks);
     if (!found)
         return PA_ERR_UNSUPPORTED;
     DeviceState *ds;
@@ -382,25 +402,18 @@ static int decode_impl(void *out, const void *q, const void *k_cache, const void
         return rc;
     int dev = 0;
     cudaGetDevice(&dev);
-    // the wide variant unless the per-sequence arrays leave it too little
-    // shared memory (static shared memory counts against the limit too)
-    int var = 0;
+    // per-sequence arrays in shared memory up to kSeqsInSmem sequences, else
+    // in the workspace (static shared memory counts against the limit too)
+    const bool seq_global = num_seqs > kSeqsInSmem;
     size_t limit = 0;
-    size_t smem = decode_smem_bytes(ks.smem_fixed[0], num_seqs);
-    rc = dynamic_smem_limit(ks.decode[0], dev, ds->smem_optin, &limit);
+    const size_t smem = seq_global ? ks.smem_fixed : decode_smem_bytes(ks.smem_fixed, num_seqs);
+    rc = dynamic_smem_limit(ks.decode, dev, ds->smem_optin, &limit);
     if (rc != PA_OK)
         return rc;
-    if (smem > limit) {
-        var = 1;
-        smem = decode_smem_bytes(ks.smem_fixed[1], num_seqs);
-        rc = dynamic_smem_limit(ks.decode[1], dev, ds->smem_optin, &limit);
-        if (rc != PA_OK)
-            return rc;
-    }
     if (smem > limit)
         return PA_ERR_UNSUPPORTED;
-    const void *decode_fn = ks.decode[var];
-    const int warps = ks.warps[var];
+    const void *decode_fn = ks.decode;
+    const int warps = ks.warps;
     // Blocks per SM, looked up for the shared memory rounded up to 2 KiB
     // (within the kernel's limit): a serving loop's batch size changes every
     // step, and the rounding keeps the cache of occupancy results to ~100
@@ -448,7 +461,13 @@ static int decode_impl(void *out, const void *q, const void *k_cache, const void
         p.ws_sm = reinterpret_cast<float *>(ws + wl.sm_off);
         p.ws_sl = reinterpret_cast<float *>(ws + wl.sl_off);
         p.ws_so = reinterpret_cast<float *>(ws + wl.so_off);
-        p.ws_desc = reinterpret_cast<CutDesc *>(ws + wl.desc_off);
+        if (mode != kModeWhole)
+            p.ws_desc = reinterpret_cast<CutDesc *>(ws + wl.desc_off);
+        if (wl.seq_global) {
+            p.ws_pre = reinterpret_cast<int32_t *>(ws + wl.pre_off);
+            p.ws_lens = reinterpret_cast<int32_t *>(ws + wl.lens_off);
+            p.ws_share = reinterpret_cast<uint8_t *>(ws + wl.share_off);
+        }
     }
     p.err = ds->err;
     p.num_seqs = num_seqs;
@@ -475,6 +494,12 @@ static int decode_impl(void *out, const void *q, const void *k_cache, const void
     // touch no global memory before that kernel has completed.
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     void *args[] = {&p, &tmk, &tmv};
+    if (wl.seq_global) {
+        void *pargs[] = {&p};
+        rc = launch_dependent(ks.prep, dim3(1), dim3(kPrepThreads), 0, st, pargs);
+        if (rc != PA_OK)
+            return rc;
+    }
     rc = launch_dependent(decode_fn, dim3(grid), dim3(warps * 32), smem, st, args);
     if (rc != PA_OK || mode == kModeWhole)
         return rc;
@@ -525,15 +550,16 @@ static long long prefill_q_ranks(int max_query_len, int num_heads, int num_kv_he
     return (max_query_len + tokens_per_block - 1) / tokens_per_block;
 }
 
-// Work-order workspace: the pair count, then one word per (sequence, query
-// tile) pair.
+// Work-order workspace: the pair count and the order's kind (two ints, 16
+// bytes), one word per (sequence, query tile) pair, then each sequence's
+// first pair and pair count (int32 each).
 size_t pa_prefill_workspace_size(int num_seqs, int max_query_len, int num_heads,
                                  int num_kv_heads)
 {
     const long long q_ranks = prefill_q_ranks(max_query_len, num_heads, num_kv_heads);
     if (num_seqs <= 0 || q_ranks <= 0)
         return 0;
-    return round_up(16 + 4 * (size_t)num_seqs * (size_t)q_ranks, 256);
+    return round_up(16 + 4 * (size_t)num_seqs * (size_t)q_ranks + 8 * (size_t)num_seqs, 256);
 }
 
 int pa_prefill(void *out, const void *q, const void *k_cache, const void *v_cache,
@@ -616,15 +642,22 @@ int pa_prefill(void *out, const void *q, const void *k_cache, const void *v_cach
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (planned) {
         int *count = static_cast<int *>(workspace);
+        int *by_seq = count + 1;
         uint32_t *plan = reinterpret_cast<uint32_t *>(static_cast<char *>(workspace) + 16);
+        int32_t *seq_start = reinterpret_cast<int32_t *>(plan + (size_t)num_seqs * q_ranks);
+        int32_t *seq_nq = seq_start + num_seqs;
         p.plan = plan;
         p.plan_count = count;
+        p.plan_by_seq = by_seq;
+        p.plan_seq_start = seq_start;
+        p.plan_seq_nq = seq_nq;
         int tpb = kPrefillTiles * (kPrefillRows / group), bn = kPrefillKeys;
         // K and V bytes a token holds over all kv heads, and the L2 size: the
         // plan keeps each sequence's tiles together when the batch's K/V
         // does not fit in L2
         long long kv_bytes_per_token = 2LL * num_kv_heads * head_dim * 2, l2_bytes = ds->l2_bytes;
-        void *pargs[] = {&p, &tpb, &bn, &plan, &count, &kv_bytes_per_token, &l2_bytes};
+        void *pargs[] = {&p,        &tpb,     &bn,       &plan,  &count, &kv_bytes_per_token,
+                         &l2_bytes, &by_seq, &seq_start, &seq_nq};
         rc = cuda_status(cudaLaunchKernel(kk.plan_fn, dim3(1), dim3(1024), pargs, 0, st));
         if (rc != PA_OK)
             return rc;

@@ -1,9 +1,10 @@
-// pa_decode_bf16.cu -- bf16 instantiations of the decode and merge kernels.
+// pa_decode_bf16.cu -- bf16 instantiations of the decode and merge kernels,
+// groups of 1..8 query heads per kv head.
 #include "pa_decode_mma.cuh"
 
 namespace pa {
-bool decode_kernels_bf16(int head_dim, int group, KernelSet *ks)
+bool decode_kernels_bf16(int head_dim, KernelSet *ks)
 {
-    return kernels_for<__nv_bfloat16>(head_dim, group, ks);
+    return kernels_for_nt<__nv_bfloat16, 1>(head_dim, ks);
 }
 }  // namespace pa

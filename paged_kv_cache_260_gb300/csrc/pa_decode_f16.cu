@@ -1,9 +1,10 @@
-// pa_decode_f16.cu -- fp16 instantiations of the decode and merge kernels.
+// pa_decode_f16.cu -- f16 instantiations of the decode and merge kernels,
+// groups of 1..8 query heads per kv head.
 #include "pa_decode_mma.cuh"
 
 namespace pa {
-bool decode_kernels_f16(int head_dim, int group, KernelSet *ks)
+bool decode_kernels_f16(int head_dim, KernelSet *ks)
 {
-    return kernels_for<__half>(head_dim, group, ks);
+    return kernels_for_nt<__half, 1>(head_dim, ks);
 }
 }  // namespace pa

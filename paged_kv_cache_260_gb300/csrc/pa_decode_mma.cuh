@@ -23,15 +23,20 @@
 //    never synchronise with each other.  A run that lies in one worker's share
 //    is written straight from registers; the pieces of a cut run go to
 //    per-worker slots and a separate merge kernel combines them.
-//  * One warp serves the whole query group of a kv head (G <= 8), so each K/V
-//    byte leaves HBM once per decode.  Per tile, on the tensor cores:
+//  * One warp serves the whole query group of a kv head (G <= 16), so each
+//    K/V byte leaves HBM once per decode.  Per tile, on the tensor cores:
 //        S[16 tokens x 8 heads] = K[16 x D] . Q^T[D x 8]       (K = A operand)
 //        O^T[D x 8 heads]      += V^T[D x 16] . P^T[16 x 8]    (V = A operand)
-//    with mma.sync m16n8k16 and fp32 accumulation.  The group is padded to 8
-//    columns.  P (the softmax weights, in [0, 1]) is rounded to the input
-//    type for the second product and transposed in registers (movmatrix), so
-//    every lane owns the same two heads in S and in O: the online-softmax
-//    rescale needs no data exchange between lanes.
+//    with mma.sync m16n8k16 and fp32 accumulation, once per 8-column tile of
+//    query heads (one tile for G <= 8, two for G <= 16; each K or V fragment
+//    loaded from shared memory serves both).  The group is padded to a
+//    multiple of 8 columns.  P (the softmax weights, in [0, 1]) is rounded to
+//    the input type for the second product and transposed in registers
+//    (movmatrix), so every lane owns the same heads in S and in O: the
+//    online-softmax rescale needs no data exchange between lanes.
+//  * Large batches (more than kSeqsInSmem sequences) keep the per-sequence
+//    lengths and unit prefix in the workspace, built once by a one-block
+//    kernel, instead of in every block's shared memory.
 #pragma once
 
 #include <cuda.h>
@@ -42,21 +47,22 @@
 
 namespace pa {
 
-template <int D>
+template <int D, int NT>
 struct MmaShape {
     static_assert(D == 64 || D == 128, "head_dim");
+    static_assert(NT == 1 || NT == 2, "query columns: 8 or 16");
     static constexpr int NB = D / 64;                         // 64-column boxes per tile
     static constexpr int BOX = kBlockSize * 128;              // bytes of one box (16 rows x 128 B)
     static constexpr int TILE = NB * BOX;                     // bytes of K (or V) per tile
     static constexpr int KSTEPS = D / 16;                     // QK: k-steps; PV: m-tiles
-    static constexpr int QB_MAX = 8 * D * 2;                  // q group, up to 8 heads
+    static constexpr int QB_MAX = 8 * NT * D * 2;             // q group, up to 8 * NT heads
     static constexpr int QSLOT = (QB_MAX + 1023) / 1024 * 1024;
     static constexpr int STAGE = 2 * TILE + QSLOT;            // multiple of 1024 (swizzle atom)
 };
 
-template <int D, int W, int S>
+template <int D, int NT, int W, int S>
 struct MmaLayout {
-    using Sh = MmaShape<D>;
+    using Sh = MmaShape<D, NT>;
     static constexpr size_t stages = (size_t)W * S * Sh::STAGE;
     static constexpr size_t bars = (size_t)W * S * 8;
     // +1024: the dynamic shared memory base is aligned up to the swizzle atom
@@ -85,55 +91,64 @@ __device__ __forceinline__ size_t slot_row(int G, int slot, int g)
     return (size_t)slot * G + g;
 }
 
-template <typename T, int D, int W, int S>
-__global__ void __launch_bounds__(W * 32)
-decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
-                  const __grid_constant__ CUtensorMap tmv)
+// Whether this thread's strided share of the flags holds a set one.
+__device__ __forceinline__ bool share_any_of(const uint8_t *share, int n, int tid, int nth)
 {
-    using Sh = MmaShape<D>;
-    using Lay = MmaLayout<D, W, S>;
+    bool any = false;
+    for (int s = tid; s < n; s += nth)
+        any |= share[s] != 0;
+    return any;
+}
+
+// Large batches: the per-sequence arrays (clamped lengths, unit prefix,
+// first-block-shared flags) are built once into the workspace by this
+// one-block kernel, instead of by every decode block into its shared memory;
+// share[num_seqs] is left set when any flag is.
+template <int NTH>
+__global__ void __launch_bounds__(NTH) decode_prep_kernel(const DecodeParams p)
+{
+    // the decode that follows may be scheduled now; it waits for this grid
+    grid_dependents_launch();
+    grid_dependency_wait();
+    build_prefix<NTH>(p, p.ws_pre, p.ws_lens, p.ws_share);
+    const bool any = __syncthreads_or(share_any_of(p.ws_share, p.num_seqs, threadIdx.x, NTH));
+    if (threadIdx.x == 0)
+        p.ws_share[p.num_seqs] = any ? 1 : 0;
+}
+
+// L2 policy for a tile that another sequence's table also names (a block
+// shared by parallel samples): normal priority, so that tiles read once
+// (evict-first) leave L2 before it and the siblings' reads find it there.
+__device__ __forceinline__ uint64_t l2_evict_normal_policy()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// One warp's whole walk: its pieces, tile by tile, and their results.
+// SHARE: some sequence of the batch shares its first block with a
+// neighbour; only then are the neighbours' table entries looked up per tile
+// (the check costs the unshared loop a few per cent even when it never
+// fires, so the kernel holds two copies of the loop and picks one per block).
+template <typename T, int D, int NT, int W, int S, bool SHARE>
+__device__ __forceinline__ void decode_worker(const DecodeParams &p, const CUtensorMap &tmk,
+                                              const CUtensorMap &tmv, unsigned char *smem,
+                                              uint64_t *bars, const int32_t *pre,
+                                              const int32_t *lens, const uint8_t *share)
+{
+    using Sh = MmaShape<D, NT>;
     using E = Elem<T>;
     using M = Mma<T>;
     constexpr int KS = Sh::KSTEPS;
     constexpr uint32_t FULL = 0xffffffffu;
-
-    extern __shared__ unsigned char smem_raw[];
-    const uint32_t raw_addr = smem_addr(smem_raw);
-    unsigned char *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Lay::stages);
-    int32_t *pre = reinterpret_cast<int32_t *>(bars + W * S);
-    int32_t *lens = pre + p.num_seqs + 1;
-
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int n = p.num_seqs, Hkv = p.num_kv_heads, Hq = p.num_heads;
     const int G = Hq / Hkv;
     const int worker = blockIdx.x * W + warp;
 
-    if (lane == 0) {
-        for (int st = 0; st < S; ++st)
-            mbar_init(smem_addr(&bars[warp * S + st]), 1);
-        mbar_init_fence();
-    }
-    // the merge kernels that follow may be scheduled now; they wait for us
-    grid_dependents_launch();
-    for (int i = tid * 32; i < n; i += W * 32 * 32)
-        prefetch_l2(p.seq_lens + i);
-    // no global memory is read or written before the preceding kernel has
-    // completed (the prefetch above only warms L2)
-    grid_dependency_wait();
-    build_prefix<W * 32>(p, pre, lens);
-    __syncthreads();
-
-    // sequences without tokens get zeros (no piece ever covers them)
-    for (int s = blockIdx.x; s < n; s += gridDim.x) {
-        if (lens[s] == 0) {
-            T *o = reinterpret_cast<T *>(p.out) + (size_t)s * Hq * D;
-            for (int e = tid; e < Hq * D; e += W * 32)
-                o[e] = E::from_f(0.f);
-        }
-    }
-
-    const uint64_t pol = l2_evict_first_policy();
+    const uint64_t pol_once = l2_evict_first_policy();
+    const uint64_t pol_shared = SHARE ? l2_evict_normal_policy() : pol_once;
     const uint32_t bar0 = smem_addr(&bars[warp * S]);
     unsigned char *wst = smem + (size_t)warp * S * Sh::STAGE;
     const uint32_t wst_addr = smem_addr(wst);
@@ -145,6 +160,9 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
     Walker cons = prod;
     int ptile = prod.valid ? prod.tb : 0;
     bool pfirst = true, pdone = !prod.valid;
+    // the producer's sequence shares its first block with a neighbour (read
+    // once per piece, not per tile)
+    bool pseq_share = SHARE && prod.valid && share[prod.s];
     auto advance = [&]() {
         while (!pdone && ptile >= prod.te) {
             prod.next();
@@ -153,13 +171,36 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
             else {
                 ptile = prod.tb;
                 pfirst = true;
+                if constexpr (SHARE)
+                    pseq_share = share[prod.s];
             }
         }
     };
     advance();
-    int pphys = 0;
-    if (!pdone && lane == 0)
-        pphys = __ldg(p.block_tables + (size_t)prod.s * p.max_blocks + ptile);
+    // Physical block of the next tile and, for a sequence whose first block
+    // a neighbour shares, the blocks the neighbours' tables name at the same
+    // position (-1: none).  A block that a neighbour also names is shared
+    // (parallel samples) and read again soon.  The loads are issued a tile
+    // ahead and compared only when the tile is issued, so their latency hides
+    // behind the current tile's math.
+    int pphys = 0, pnb0 = -1, pnb1 = -1;
+    auto lookup = [&]() {
+        if (pdone || lane != 0)
+            return;
+        const int32_t *row = p.block_tables + (size_t)prod.s * p.max_blocks;
+        pphys = __ldg(row + ptile);
+        if constexpr (SHARE) {
+            pnb0 = pnb1 = -1;
+            if (!pseq_share)
+                return;
+            const int lo_tok = ptile * kBlockSize;
+            if (prod.s > 0 && lens[prod.s - 1] > lo_tok)
+                pnb0 = __ldg(row - p.max_blocks + ptile);
+            if (prod.s + 1 < n && lens[prod.s + 1] > lo_tok)
+                pnb1 = __ldg(row + p.max_blocks + ptile);
+        }
+    };
+    lookup();
     int issued = 0;
     auto produce = [&](int st) {
         if (pdone)
@@ -173,6 +214,9 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
             const int row = (phys * Hkv + prod.h) * kBlockSize;
             const uint32_t bar = bar0 + st * 8;
             const uint32_t dst = wst_addr + st * Sh::STAGE;
+            uint64_t pol = pol_once;
+            if constexpr (SHARE)
+                pol = (pnb0 == pphys) | (pnb1 == pphys) ? pol_shared : pol_once;
             mbar_arrive_expect_tx(bar, 2 * Sh::TILE + (pfirst ? qb_bytes : 0));
 #pragma unroll
             for (int b = 0; b < Sh::NB; ++b) {
@@ -187,8 +231,7 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
         pfirst = false;
         ++ptile;
         advance();
-        if (!pdone && lane == 0)
-            pphys = __ldg(p.block_tables + (size_t)prod.s * p.max_blocks + ptile);
+        lookup();
         ++issued;
     };
 #pragma unroll 1
@@ -196,29 +239,33 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
         produce(st);
 
     // ---- per-lane fragment geometry ----
+    // Query columns come in NT tiles of 8 heads; in each, lane owns heads
+    // 8j + 2qd and 8j + 2qd + 1 in S and in O.
     const int r = lane >> 2;          // S: token row (and +8); O: head_dim row (and +8)
-    const int qd = lane & 3;          // S and O: heads 2*qd, 2*qd + 1
-    const int h0 = 2 * qd, h1 = h0 + 1;
+    const int qd = lane & 3;
     const int mi = lane >> 3, rr = lane & 7;   // ldmatrix: matrix index, row within it
     const int krow = ((mi & 1) << 3) + rr, kcs = mi >> 1;   // K (A operand, row-major)
     const int vrow = ((mi >> 1) << 3) + rr, vcs = mi & 1;   // V (A operand via .trans)
 
-    uint32_t qf[KS][2];               // B fragments of Q^T for the current piece
-    float o[KS][4];                   // O^T accumulators: (row, h0) (row, h1) (row+8, h0) (row+8, h1)
-    float m0, m1, l0, l1;             // running max (base 2) and partial sums, heads h0, h1
+    uint32_t qf[NT][KS][2];           // B fragments of Q^T for the current piece
+    float o[NT][KS][4];               // O^T accumulators: (row, h0) (row, h1) (row+8, h0) (row+8, h1)
+    float m[NT][2], l[NT][2];         // running max (base 2) and partial sums, heads h0, h1
     int it = 0;
     bool aborted = false;
     int abort_it = 0;
     CutDesc desc{0, 0, 0, 0, 0, 0, 0, 0};
 
     while (cons.valid) {
-        m0 = m1 = -INFINITY;
-        l0 = l1 = 0.f;
 #pragma unroll
-        for (int mt = 0; mt < KS; ++mt)
+        for (int j = 0; j < NT; ++j) {
+            m[j][0] = m[j][1] = -INFINITY;
+            l[j][0] = l[j][1] = 0.f;
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
-                o[mt][c] = 0.f;
+            for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    o[j][mt][c] = 0.f;
+        }
         const int L = lens[cons.s];
         bool need_q = true;
 
@@ -261,11 +308,15 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
             const uint32_t vst = kst + Sh::TILE;
             if (need_q) {
                 const unsigned char *qs = wst + (size_t)st * Sh::STAGE + 2 * Sh::TILE;
-                const uint32_t *qrow = reinterpret_cast<const uint32_t *>(qs + (size_t)r * D * 2);
 #pragma unroll
-                for (int ks = 0; ks < KS; ++ks) {
-                    qf[ks][0] = r < G ? qrow[(16 * ks + 2 * qd) / 2] : 0u;
-                    qf[ks][1] = r < G ? qrow[(16 * ks + 8 + 2 * qd) / 2] : 0u;
+                for (int j = 0; j < NT; ++j) {
+                    const int hq = 8 * j + r;     // B column: query head of the group
+                    const uint32_t *qrow = reinterpret_cast<const uint32_t *>(qs + (size_t)hq * D * 2);
+#pragma unroll
+                    for (int ks = 0; ks < KS; ++ks) {
+                        qf[j][ks][0] = hq < G ? qrow[(16 * ks + 2 * qd) / 2] : 0u;
+                        qf[j][ks][1] = hq < G ? qrow[(16 * ks + 8 + 2 * qd) / 2] : 0u;
+                    }
                 }
                 need_q = false;
             }
@@ -286,54 +337,66 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
                 __syncwarp();
             }
 
-            // S = K . Q^T  (two accumulators to shorten the dependency chain)
-            float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+            // S = K . Q^T  (two accumulators per column tile to shorten the
+            // dependency chain; each K fragment serves every column tile)
+            float sa[NT][4], sb[NT][4];
+#pragma unroll
+            for (int j = 0; j < NT; ++j)
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    sa[j][c] = sb[j][c] = 0.f;
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {
                 uint32_t a[4];
                 ldsm_x4(kst + (ks >> 2) * Sh::BOX + swz(krow, 2 * (ks & 3) + kcs), a[0], a[1], a[2], a[3]);
-                M::run((ks & 1) ? sb : sa, a, qf[ks][0], qf[ks][1]);
+#pragma unroll
+                for (int j = 0; j < NT; ++j)
+                    M::run((ks & 1) ? sb[j] : sa[j], a, qf[j][ks][0], qf[j][ks][1]);
             }
-            float x0 = (sa[0] + sb[0]) * p.scale_log2;   // token r,   head h0
-            float x1 = (sa[1] + sb[1]) * p.scale_log2;   // token r,   head h1
-            float x2 = (sa[2] + sb[2]) * p.scale_log2;   // token r+8, head h0
-            float x3 = (sa[3] + sb[3]) * p.scale_log2;   // token r+8, head h1
             const bool masked = nvalid < kBlockSize;
-            if (masked) {
-                // slots past the end may hold anything, NaN included
-                if (r >= nvalid)
-                    x0 = x1 = -INFINITY;
-                if (r + 8 >= nvalid)
-                    x2 = x3 = -INFINITY;
-            }
-            float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+            uint32_t pb[NT][2];
 #pragma unroll
-            for (int off = 4; off < 32; off <<= 1) {
-                mx0 = fmaxf(mx0, __shfl_xor_sync(FULL, mx0, off));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(FULL, mx1, off));
-            }
-            if (__any_sync(FULL, (mx0 > m0) | (mx1 > m1))) {
-                const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
-                const float a0 = exp2f(m0 - n0), a1 = exp2f(m1 - n1);
-                m0 = n0;
-                m1 = n1;
-                l0 *= a0;
-                l1 *= a1;
-#pragma unroll
-                for (int mt = 0; mt < KS; ++mt) {
-                    o[mt][0] *= a0;
-                    o[mt][1] *= a1;
-                    o[mt][2] *= a0;
-                    o[mt][3] *= a1;
+            for (int j = 0; j < NT; ++j) {
+                float x0 = (sa[j][0] + sb[j][0]) * p.scale_log2;   // token r,   head h0
+                float x1 = (sa[j][1] + sb[j][1]) * p.scale_log2;   // token r,   head h1
+                float x2 = (sa[j][2] + sb[j][2]) * p.scale_log2;   // token r+8, head h0
+                float x3 = (sa[j][3] + sb[j][3]) * p.scale_log2;   // token r+8, head h1
+                if (masked) {
+                    // slots past the end may hold anything, NaN included
+                    if (r >= nvalid)
+                        x0 = x1 = -INFINITY;
+                    if (r + 8 >= nvalid)
+                        x2 = x3 = -INFINITY;
                 }
+                float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1) {
+                    mx0 = fmaxf(mx0, __shfl_xor_sync(FULL, mx0, off));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(FULL, mx1, off));
+                }
+                if (__any_sync(FULL, (mx0 > m[j][0]) | (mx1 > m[j][1]))) {
+                    const float n0 = fmaxf(m[j][0], mx0), n1 = fmaxf(m[j][1], mx1);
+                    const float a0 = exp2f(m[j][0] - n0), a1 = exp2f(m[j][1] - n1);
+                    m[j][0] = n0;
+                    m[j][1] = n1;
+                    l[j][0] *= a0;
+                    l[j][1] *= a1;
+#pragma unroll
+                    for (int mt = 0; mt < KS; ++mt) {
+                        o[j][mt][0] *= a0;
+                        o[j][mt][1] *= a1;
+                        o[j][mt][2] *= a0;
+                        o[j][mt][3] *= a1;
+                    }
+                }
+                const float p0 = exp2f(x0 - m[j][0]), p1 = exp2f(x1 - m[j][1]);
+                const float p2 = exp2f(x2 - m[j][0]), p3 = exp2f(x3 - m[j][1]);
+                l[j][0] += p0 + p2;
+                l[j][1] += p1 + p3;
+                // P^T as the B operand: rows of P (tokens) become columns
+                pb[j][0] = movmatrix_trans(M::pack(p0, p1));
+                pb[j][1] = movmatrix_trans(M::pack(p2, p3));
             }
-            const float p0 = exp2f(x0 - m0), p1 = exp2f(x1 - m1);
-            const float p2 = exp2f(x2 - m0), p3 = exp2f(x3 - m1);
-            l0 += p0 + p2;
-            l1 += p1 + p3;
-            // P^T as the B operand: rows of P (tokens) become columns
-            const uint32_t pb0 = movmatrix_trans(M::pack(p0, p1));
-            const uint32_t pb1 = movmatrix_trans(M::pack(p2, p3));
 
             // O^T += V^T . P^T ; value rows past the end are zeroed (0 * NaN is NaN)
             uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
@@ -351,7 +414,9 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
                 a[1] &= mlo;
                 a[2] &= mhi;
                 a[3] &= mhi;
-                M::run(o[mt], a, pb0, pb1);
+#pragma unroll
+                for (int j = 0; j < NT; ++j)
+                    M::run(o[j][mt], a, pb[j][0], pb[j][1]);
             }
             __syncwarp();
             if (!aborted)
@@ -360,59 +425,66 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
         }
 
         // ---- end of piece: write this warp's result ----
-#pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-            l0 += __shfl_xor_sync(FULL, l0, off);
-            l1 += __shfl_xor_sync(FULL, l1, off);
-        }
-        const float inv0 = 1.f / l0, inv1 = 1.f / l1;
         const int s = cons.s, h = cons.h;
-        if (cons.whole_run()) {
-            T *out = reinterpret_cast<T *>(p.out) + ((size_t)s * Hq + h * G) * D;
+        const bool whole = cons.whole_run();
+        const bool wp = !whole && cons.whole_part();
+        const int slot = 2 * worker + (cons.first ? 0 : 1);
 #pragma unroll
-            for (int mt = 0; mt < KS; ++mt) {
-                const int d0 = 16 * mt + r;
-                if (h0 < G) {
-                    out[h0 * D + d0] = E::from_f(o[mt][0] * inv0);
-                    out[h0 * D + d0 + 8] = E::from_f(o[mt][2] * inv0);
-                }
-                if (h1 < G) {
-                    out[h1 * D + d0] = E::from_f(o[mt][1] * inv1);
-                    out[h1 * D + d0 + 8] = E::from_f(o[mt][3] * inv1);
-                }
-            }
-        } else {
-            // a partition (fixed mode) goes to its documented row; a cut piece
-            // to this worker's first or last slot
-            const bool wp = cons.whole_part();
-            const int slot = 2 * worker + (cons.first ? 0 : 1);
-            float *pm = wp ? p.ws_m : p.ws_sm;
-            float *pl = wp ? p.ws_l : p.ws_sl;
-            float *po = wp ? p.ws_o : p.ws_so;
-            const size_t row0 = wp ? part_row(p, G, s, h, cons.part, h0) : slot_row(G, slot, h0);
-            const size_t row1 = wp ? part_row(p, G, s, h, cons.part, h1) : slot_row(G, slot, h1);
+        for (int j = 0; j < NT; ++j) {
 #pragma unroll
-            for (int mt = 0; mt < KS; ++mt) {
-                const int d0 = 16 * mt + r;
-                if (h0 < G) {
-                    po[row0 * D + d0] = o[mt][0] * inv0;
-                    po[row0 * D + d0 + 8] = o[mt][2] * inv0;
+            for (int off = 4; off < 32; off <<= 1) {
+                l[j][0] += __shfl_xor_sync(FULL, l[j][0], off);
+                l[j][1] += __shfl_xor_sync(FULL, l[j][1], off);
+            }
+            const float inv0 = 1.f / l[j][0], inv1 = 1.f / l[j][1];
+            const int h0 = 8 * j + 2 * qd, h1 = h0 + 1;
+            if (whole) {
+                T *out = reinterpret_cast<T *>(p.out) + ((size_t)s * Hq + h * G) * D;
+#pragma unroll
+                for (int mt = 0; mt < KS; ++mt) {
+                    const int d0 = 16 * mt + r;
+                    if (h0 < G) {
+                        out[h0 * D + d0] = E::from_f(o[j][mt][0] * inv0);
+                        out[h0 * D + d0 + 8] = E::from_f(o[j][mt][2] * inv0);
+                    }
+                    if (h1 < G) {
+                        out[h1 * D + d0] = E::from_f(o[j][mt][1] * inv1);
+                        out[h1 * D + d0 + 8] = E::from_f(o[j][mt][3] * inv1);
+                    }
                 }
-                if (h1 < G) {
-                    po[row1 * D + d0] = o[mt][1] * inv1;
-                    po[row1 * D + d0 + 8] = o[mt][3] * inv1;
+            } else {
+                // a partition (fixed mode) goes to its documented row; a cut
+                // piece to this worker's first or last slot
+                float *pm = wp ? p.ws_m : p.ws_sm;
+                float *pl = wp ? p.ws_l : p.ws_sl;
+                float *po = wp ? p.ws_o : p.ws_so;
+                const size_t row0 = wp ? part_row(p, G, s, h, cons.part, h0) : slot_row(G, slot, h0);
+                const size_t row1 = wp ? part_row(p, G, s, h, cons.part, h1) : slot_row(G, slot, h1);
+#pragma unroll
+                for (int mt = 0; mt < KS; ++mt) {
+                    const int d0 = 16 * mt + r;
+                    if (h0 < G) {
+                        po[row0 * D + d0] = o[j][mt][0] * inv0;
+                        po[row0 * D + d0 + 8] = o[j][mt][2] * inv0;
+                    }
+                    if (h1 < G) {
+                        po[row1 * D + d0] = o[j][mt][1] * inv1;
+                        po[row1 * D + d0 + 8] = o[j][mt][3] * inv1;
+                    }
+                }
+                if (r == 0) {
+                    if (h0 < G) {
+                        pm[row0] = m[j][0] * kLn2;
+                        pl[row0] = l[j][0];
+                    }
+                    if (h1 < G) {
+                        pm[row1] = m[j][1] * kLn2;
+                        pl[row1] = l[j][1];
+                    }
                 }
             }
-            if (r == 0) {
-                if (h0 < G) {
-                    pm[row0] = m0 * kLn2;
-                    pl[row0] = l0;
-                }
-                if (h1 < G) {
-                    pm[row1] = m1 * kLn2;
-                    pl[row1] = l1;
-                }
-            }
+        }
+        if (!whole) {
             // the unit (run, or partition in fixed mode) this piece belongs to
             const int u0 = cons.F + (p.mode == kModeFixed ? cons.part * cons.pt : 0);
             const int nu = p.mode == kModeFixed ? min(cons.pt, cons.nt - cons.part * cons.pt) : cons.nt;
@@ -440,6 +512,81 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
     }
 }
 
+template <typename T, int D, int NT, int W, int S>
+__global__ void __launch_bounds__(W * 32)
+decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
+                  const __grid_constant__ CUtensorMap tmv)
+{
+    using Sh = MmaShape<D, NT>;
+    using Lay = MmaLayout<D, NT, W, S>;
+    using E = Elem<T>;
+    using M = Mma<T>;
+    constexpr int KS = Sh::KSTEPS;
+    constexpr uint32_t FULL = 0xffffffffu;
+
+    extern __shared__ unsigned char smem_raw[];
+    const uint32_t raw_addr = smem_addr(smem_raw);
+    unsigned char *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Lay::stages);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int n = p.num_seqs, Hkv = p.num_kv_heads, Hq = p.num_heads;
+    const int G = Hq / Hkv;
+    const int worker = blockIdx.x * W + warp;
+    const bool seq_global = p.ws_pre != nullptr;
+
+    if (lane == 0) {
+        for (int st = 0; st < S; ++st)
+            mbar_init(smem_addr(&bars[warp * S + st]), 1);
+        mbar_init_fence();
+    }
+    // the merge kernels that follow may be scheduled now; they wait for us
+    grid_dependents_launch();
+    if (!seq_global)
+        for (int i = tid * 32; i < n; i += W * 32 * 32)
+            prefetch_l2(p.seq_lens + i);
+    // no global memory is read or written before the preceding kernel has
+    // completed (the prefetch above only warms L2)
+    grid_dependency_wait();
+    const int32_t *pre, *lens;
+    const uint8_t *share;
+    bool any_share = false;
+    if (seq_global) {
+        // built by decode_prep_kernel, the grid this one waited for
+        pre = p.ws_pre;
+        lens = p.ws_lens;
+        share = p.ws_share;
+    } else {
+        int32_t *spre = reinterpret_cast<int32_t *>(bars + W * S);
+        int32_t *slens = spre + n + 1;
+        uint8_t *sshare = reinterpret_cast<uint8_t *>(slens + n);
+        build_prefix<W * 32>(p, spre, slens, sshare);
+        pre = spre;
+        lens = slens;
+        share = sshare;
+    }
+    // whether any sequence shares its first block (the prep kernel leaves
+    // the answer after the flags); the barrier also publishes the arrays
+    if (seq_global)
+        any_share = __syncthreads_or(tid == 0 && share[n] != 0);
+    else
+        any_share = __syncthreads_or(share_any_of(share, n, tid, W * 32));
+
+    // sequences without tokens get zeros (no piece ever covers them)
+    for (int s = blockIdx.x; s < n; s += gridDim.x) {
+        if (lens[s] == 0) {
+            T *o = reinterpret_cast<T *>(p.out) + (size_t)s * Hq * D;
+            for (int e = tid; e < Hq * D; e += W * 32)
+                o[e] = E::from_f(0.f);
+        }
+    }
+
+    if (any_share)
+        decode_worker<T, D, NT, W, S, true>(p, tmk, tmv, smem, bars, pre, lens, share);
+    else
+        decode_worker<T, D, NT, W, S, false>(p, tmk, tmv, smem, bars, pre, lens, share);
+}
+
 // ---------------------------------------------------------------------------
 // Log-sum-exp merge of partial results (m_p, l_p, o_p):
 //     M = max_p m_p,  w_p = l_p exp(m_p - M),  out = sum_p w_p o_p / sum_p w_p
@@ -451,7 +598,7 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
 // output (a run) or, in fixed mode, the partition's documented row.
 // ---------------------------------------------------------------------------
 template <typename T, int D>
-__global__ void __launch_bounds__(256) merge_cut_kernel(const DecodeParams p)
+__global__ void __launch_bounds__(512) merge_cut_kernel(const DecodeParams p)
 {
     constexpr int V = D / 32;
     constexpr int CH = 8;
@@ -622,33 +769,31 @@ __global__ void __launch_bounds__(512) merge_part_kernel(const DecodeParams p)
     }
 }
 
-template <typename T, int D>
+template <typename T, int D, int NT>
 inline void fill_kernel_set(KernelSet *ks)
 {
-    // wide: one thread block per SM of WW independent warps; compact: 4 warps
+    // one thread block per SM of W independent warps, two copy stages each:
+    // as many warps as fit in shared memory with the per-sequence arrays of
+    // kSeqsInSmem sequences (a 16-column query slot costs two warps at D=128)
     constexpr int S = 2;
-    constexpr int WW = D == 128 ? 10 : 12;
-    ks->decode[0] = reinterpret_cast<const void *>(&decode_mma_kernel<T, D, WW, S>);
-    ks->warps[0] = WW;
-    ks->smem_fixed[0] = MmaLayout<D, WW, S>::fixed;
-    ks->decode[1] = reinterpret_cast<const void *>(&decode_mma_kernel<T, D, 4, S>);
-    ks->warps[1] = 4;
-    ks->smem_fixed[1] = MmaLayout<D, 4, S>::fixed;
+    constexpr int W = D == 128 ? (NT == 1 ? 10 : 8) : 12;
+    ks->decode = reinterpret_cast<const void *>(&decode_mma_kernel<T, D, NT, W, S>);
+    ks->warps = W;
+    ks->smem_fixed = MmaLayout<D, NT, W, S>::fixed;
+    ks->prep = reinterpret_cast<const void *>(&decode_prep_kernel<kPrepThreads>);
     ks->merge_cut = reinterpret_cast<const void *>(&merge_cut_kernel<T, D>);
     ks->merge_part = reinterpret_cast<const void *>(&merge_part_kernel<T, D>);
 }
 
-template <typename T>
-inline bool kernels_for(int head_dim, int group, KernelSet *ks)
+template <typename T, int NT>
+inline bool kernels_for_nt(int head_dim, KernelSet *ks)
 {
-    if (group < 1 || group > 8)
-        return false;
     if (head_dim == 128) {
-        fill_kernel_set<T, 128>(ks);
+        fill_kernel_set<T, 128, NT>(ks);
         return true;
     }
     if (head_dim == 64) {
-        fill_kernel_set<T, 64>(ks);
+        fill_kernel_set<T, 64, NT>(ks);
         return true;
     }
     return false;

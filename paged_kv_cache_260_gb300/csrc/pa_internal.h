@@ -34,6 +34,9 @@ struct DecodeParams {
     float *ws_sl;
     float *ws_so;
     CutDesc *ws_desc;      // per worker: the cut unit that starts in its range
+    int32_t *ws_pre;       // large batches: unit prefix [num_seqs + 1] in the workspace, or null
+    int32_t *ws_lens;      //   clamped lengths [num_seqs] (null: all three in shared memory)
+    uint8_t *ws_share;     //   and first-block-shared flags [num_seqs]
     uint32_t *err;         // device error bits (PA_DEVERR_*)
     int num_seqs;
     int num_heads;
@@ -48,29 +51,36 @@ struct DecodeParams {
     float scale_log2;      // scale * log2(e): scores are kept in base 2
 };
 
-// Kernels of one (dtype, head_dim) instantiation.  decode[0] is the wide
-// variant (one block of many warps per SM); decode[1] a compact one used when
-// the per-sequence arrays of a large batch leave too little shared memory.
+// Kernels of one (dtype, head_dim, query columns) instantiation.
 struct KernelSet {
-    const void *decode[2];
-    int warps[2];            // warps (workers) per decode thread block
-    size_t smem_fixed[2];    // dynamic shared memory excluding the per-sequence arrays
+    const void *decode;      // one thread block per SM of `warps` independent warps
+    int warps;
+    size_t smem_fixed;       // dynamic shared memory excluding the per-sequence arrays
+    const void *prep;        // large batches: builds the per-sequence arrays in the workspace
     const void *merge_cut;   // combines the pieces of cut units
     const void *merge_part;  // fixed mode: merges partitions into the output
 };
 
 // Per-sequence shared-memory arrays of the decode kernel: unit prefix
-// [num_seqs + 1] and clamped lengths [num_seqs], int32 each.
+// [num_seqs + 1] and clamped lengths [num_seqs], int32 each, then one
+// first-block-shared flag byte per sequence.
 inline size_t decode_smem_bytes(size_t smem_fixed, int num_seqs)
 {
-    return smem_fixed + sizeof(int32_t) * (2 * (size_t)num_seqs + 1);
+    return smem_fixed + sizeof(int32_t) * (2 * (size_t)num_seqs + 1) + (size_t)num_seqs;
 }
 
-constexpr int kMaxSeqs = 8192;        // per-sequence arrays live in shared memory
+// Batches up to this size keep the per-sequence arrays in each decode block's
+// shared memory (every variant fits them under the 227 KiB limit); larger
+// ones have them built once in the workspace by the prep kernel.
+constexpr int kSeqsInSmem = 2048;
+constexpr int kPrepThreads = 1024;
 constexpr int kMaxWarpsPerSM = 16;    // decode workers <= SMs * this (workspace sizing)
 constexpr int kMinTiles = 2;          // split modes: least tiles per worker (warp)
+constexpr int kMaxGroup = 16;         // query heads per kv head: two 8-column tiles
 
-bool decode_kernels_f16(int head_dim, int group, KernelSet *ks);
-bool decode_kernels_bf16(int head_dim, int group, KernelSet *ks);
+bool decode_kernels_f16(int head_dim, KernelSet *ks);       // groups 1..8
+bool decode_kernels_bf16(int head_dim, KernelSet *ks);
+bool decode_kernels_f16_g16(int head_dim, KernelSet *ks);   // groups 9..16
+bool decode_kernels_bf16_g16(int head_dim, KernelSet *ks);
 
 }  // namespace pa

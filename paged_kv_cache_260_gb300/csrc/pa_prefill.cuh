@@ -91,6 +91,30 @@ struct PrefillShape {
     static_assert(SMEM <= 227 * 1024, "one block per SM");
 };
 
+// The (sequence, query tile, kv head) of block b under the work order;
+// false past the end of the order.
+__device__ __forceinline__ bool plan_block(const PrefillParams &p, int b, int &s, int &tile,
+                                           int &h)
+{
+    const int Hkv = p.num_kv_heads;
+    const int k = b / Hkv;
+    if (k >= *p.plan_count)
+        return false;
+    uint32_t e = p.plan[k];
+    if (*p.plan_by_seq) {
+        const int s0 = (int)(e >> 16);
+        const int st = p.plan_seq_start[s0], nq = p.plan_seq_nq[s0];
+        const int local = b - Hkv * st;
+        h = local / nq;
+        e = p.plan[st + local % nq];
+    } else {
+        h = b % Hkv;
+    }
+    s = (int)(e >> 16);
+    tile = (int)(e & 0xffffu);
+    return true;
+}
+
 template <typename T, int D>
 __global__ void __launch_bounds__(PrefillShape<D>::THREADS)
 prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk,
@@ -124,19 +148,15 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
     const int Hkv = p.num_kv_heads, Hq = p.num_heads, G = Hq / Hkv;
     const int TPG = Sh::BM / G;                   // chunk tokens per group
     const int TPB = Sh::NG * TPG;                 // chunk tokens per block
-    const int h = blockIdx.x % Hkv;
+    int h = blockIdx.x % Hkv;
 
     // ---- the block's rows and key range (uniform over the block) ----------
     // no global memory is read before the preceding kernel (the plan) is done
     grid_dependency_wait();
     int s, rank = 0, tile = 0;
     if (p.plan) {
-        const int k = blockIdx.x / Hkv;
-        if (k >= *p.plan_count)
+        if (!plan_block(p, blockIdx.x, s, tile, h))
             return;
-        const uint32_t e = p.plan[k];
-        s = (int)(e >> 16);
-        tile = (int)(e & 0xffffu);
     } else {
         const int per_rank = p.num_seqs * Hkv;
         rank = blockIdx.x / per_rank;
@@ -325,12 +345,10 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
         // while this block's query rows load: warm L2 with those of the
         // block one wave later (its pair and kv head from the work order)
         if (p.plan) {
-            const int nb = (int)blockIdx.x + p.wave;
-            if (nb / Hkv < *p.plan_count) {
-                const uint32_t e = p.plan[nb / Hkv];
-                const int s2 = (int)(e >> 16), h2 = nb % Hkv;
+            int s2, tile2, h2;
+            if (plan_block(p, (int)blockIdx.x + p.wave, s2, tile2, h2)) {
                 const int qs2 = __ldg(p.query_start + s2);
-                const int t02 = (int)(e & 0xffffu) * TPB;
+                const int t02 = tile2 * TPB;
                 const int ntok = min(TPB, __ldg(p.query_start + s2 + 1) - qs2 - t02);
                 const int lines = G * D * 2 / 128;  // 128-byte lines of a token's G heads
                 const T *qg = reinterpret_cast<const T *>(p.q);
@@ -597,17 +615,20 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
 
 // ---------------------------------------------------------------------------
 // Work order of a prefill, one block.  The hardware hands thread blocks to
-// SMs in index order as SMs free up, and block b computes pair plan[b / Hkv]
-// for kv head b % Hkv, so the order decides both the schedule and what the
-// blocks running at the same time share:
+// SMs in index order as SMs free up, so the order decides both the schedule
+// and what the blocks running at the same time share (plan_block maps a
+// block to its work):
 //  * the (sequence, query tile) pairs sorted by their key-tile count,
-//    heaviest first (a counting sort on the count): the greedy
-//    longest-first schedule, ending on the lightest pairs.  Used when the
-//    batch's K/V fits in L2, so any blocks may run side by side;
+//    heaviest first (a counting sort on the count), block b taking pair
+//    plan[b / Hkv] for kv head b % Hkv: the greedy longest-first schedule,
+//    ending on the lightest pairs.  Used when the batch's K/V fits in L2, so
+//    any blocks may run side by side;
 //  * otherwise sequence by sequence, the sequences ordered by their heaviest
-//    tile and each sequence's tiles heaviest first.  The blocks running at
-//    one time then work on few sequences and stream the same K/V prefix, so
-//    L2 serves most of it instead of DRAM.
+//    tile and each sequence's tiles heaviest first; a sequence's blocks take
+//    its kv heads one after the other, each with all of its query tiles.
+//    The blocks running at one time then stream the K/V of a few kv heads of
+//    one sequence, together, so L2 serves the re-reads and each head's K/V
+//    leaves DRAM about once.
 // Pairs of one count keep no particular order (their results do not depend
 // on it).
 // ---------------------------------------------------------------------------
@@ -615,7 +636,8 @@ constexpr int kPlanBuckets = 2048;   // key-tile counts above this share the top
 
 __global__ void __launch_bounds__(1024)
 prefill_plan_kernel(const PrefillParams p, int tpb, int bn, uint32_t *plan, int *count,
-                    long long kv_bytes_per_token, long long l2_bytes)
+                    long long kv_bytes_per_token, long long l2_bytes, int *by_seq,
+                    int32_t *seq_start, int32_t *seq_nq)
 {
     __shared__ int hist_tile[kPlanBuckets];  // pairs per key-tile count
     __shared__ int hist_seq[kPlanBuckets];   // pairs of the sequences whose heaviest tile has it
@@ -682,6 +704,8 @@ prefill_plan_kernel(const PrefillParams p, int tpb, int bn, uint32_t *plan, int 
         atomicAdd(&tokens, my_tokens);
     __syncthreads();
     const bool by_sequence = (long long)tokens * kv_bytes_per_token > l2_bytes;
+    if (tid == 0)
+        *by_seq = by_sequence ? 1 : 0;
     int *hist = by_sequence ? hist_seq : hist_tile;
     // start of each bucket in descending order of the count: thread t owns
     // buckets B-1-2t and B-2-2t; warp scans, then a scan of the warp totals
@@ -726,6 +750,8 @@ prefill_plan_kernel(const PrefillParams p, int tpb, int bn, uint32_t *plan, int 
         if (by_sequence) {
             if (nq > first) {
                 int at = atomicAdd(&hist_seq[bucket(L, c, nq - 1)], nq - first);
+                seq_start[s] = at;
+                seq_nq[s] = nq - first;
                 for (int t = nq - 1; t >= first; --t)
                     plan[at++] = ((uint32_t)s << 16) | (uint32_t)t;
             }

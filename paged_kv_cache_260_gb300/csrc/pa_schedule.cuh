@@ -169,8 +169,13 @@ __device__ __forceinline__ int seq_units(int L, int mode)
 }
 
 // Clamp the lengths into shared memory and build the exclusive unit prefix.
+// Also flag each sequence whose first block is named by a neighbouring
+// sequence's table too (share[s] = 1): sequences forked from one prompt
+// (parallel samples) share their prompt's blocks and sit next to each other
+// in the batch.  Only flagged sequences pay for per-tile sharing checks.
 template <int NT>
-__device__ __forceinline__ void build_prefix(const DecodeParams &p, int32_t *pre, int32_t *lens)
+__device__ __forceinline__ void build_prefix(const DecodeParams &p, int32_t *pre, int32_t *lens,
+                                             uint8_t *share)
 {
     constexpr int NW = NT / 32;
     __shared__ int warp_sum[NW];
@@ -179,15 +184,23 @@ __device__ __forceinline__ void build_prefix(const DecodeParams &p, int32_t *pre
     const int per = (n + NT - 1) / NT;
     const int lo = min(n, tid * per), hi = min(n, lo + per);
     const int maxlen = p.max_blocks * kBlockSize;
+    const size_t mb = (size_t)p.max_blocks;
     int sum = 0;
     bool bad = false;
     for (int s = lo; s < hi; ++s) {
+        // every load below is in bounds whatever the lengths hold
         int L = __ldg(p.seq_lens + s);
+        const int Lp = s > 0 ? __ldg(p.seq_lens + s - 1) : 0;
+        const int Ln = s + 1 < n ? __ldg(p.seq_lens + s + 1) : 0;
+        const int b0 = __ldg(p.block_tables + s * mb);
+        const int bp = s > 0 ? __ldg(p.block_tables + (s - 1) * mb) : -1;
+        const int bn = s + 1 < n ? __ldg(p.block_tables + (s + 1) * mb) : -1;
         if (L < 0 || L > maxlen) {
             bad = true;
             L = L < 0 ? 0 : maxlen;
         }
         lens[s] = L;
+        share[s] = (uint8_t)(L > 0 && ((Lp > 0 && bp == b0) || (Ln > 0 && bn == b0)));
         sum += seq_units(L, p.mode);
     }
     if (bad && blockIdx.x == 0)

@@ -65,7 +65,8 @@ def test_decode_rejects_bad_scalars(lib):
     assert _decode(lib, block_size=32) == 2
     assert _decode(lib, dtype=7) == 2
     assert _decode(lib, num_heads=7) == 1              # not a multiple of kv heads
-    assert _decode(lib, num_heads=20) == 2             # group 10 > 8
+    assert _decode(lib, num_heads=34) == 2             # group 17 > 16
+    assert _decode(lib, num_heads=32) == 1             # group 16 is served: null pointers refused
     assert _decode(lib, scale=float("nan")) == 1
     assert _decode(lib, num_seqs=-1) == 1
     assert _decode(lib, num_seqs=0) == 0               # nothing to do
@@ -143,7 +144,8 @@ def test_prefill_rejects_bad_scalars(lib):
 def test_prefill_workspace_size(lib):
     lib.pa_prefill_workspace_size.restype = C.c_size_t
     # 32 q heads over 8 kv heads: 4 per group, 64 chunk tokens per block
-    assert lib.pa_prefill_workspace_size(8, 512, 32, 8) == 512          # 16 + 4*8*8 -> 512
-    assert lib.pa_prefill_workspace_size(100, 1000, 32, 8) == 6656      # 16 + 4*100*16 -> 6656
+    # 16 + 4 * seqs * query tiles + 8 * seqs, rounded up to 256
+    assert lib.pa_prefill_workspace_size(8, 512, 32, 8) == 512          # 16 + 256 + 64
+    assert lib.pa_prefill_workspace_size(100, 1000, 32, 8) == 7424      # 16 + 6400 + 800
     assert lib.pa_prefill_workspace_size(0, 512, 32, 8) == 0
     assert lib.pa_prefill_workspace_size(8, 512, 30, 8) == 0            # not a multiple

@@ -35,7 +35,11 @@ LENS = [0, 1, 2, 15, 16, 17, 31, 33, 100, 257, 700, 1029]
 @pytest.mark.parametrize("Hq,Hkv,D,dtype", [
     (8, 8, 64, "f16"), (8, 8, 128, "bf16"), (8, 4, 128, "f16"), (12, 4, 64, "bf16"),
     (16, 4, 128, "bf16"), (10, 2, 128, "f16"), (12, 2, 64, "f16"), (14, 2, 128, "bf16"),
-    (16, 2, 128, "f16"), (8, 1, 64, "bf16")])
+    (16, 2, 128, "f16"), (8, 1, 64, "bf16"),
+    # groups 9..16: the query columns take a second 8-column tile (MQA-like
+    # sharing of one kv head by many query heads)
+    (9, 1, 128, "f16"), (26, 2, 128, "bf16"), (15, 1, 64, "bf16"), (16, 1, 128, "bf16"),
+    (32, 2, 64, "f16")])
 def test_decode_ragged(pa, mode, Hq, Hkv, D, dtype):
     w = synth.build("ragged", len(LENS), Hq, Hkv, D, dtype, LENS, seed=100 + Hq + D, append=True,
                     poison=True)
@@ -203,18 +207,37 @@ def test_many_short_sequences(pa):
     check(pa, w, -1)
 
 
-@pytest.mark.parametrize("n", [1, 7, 100, 3300, 3307, 3308, 5000])
+@pytest.mark.parametrize("n", [1, 7, 100, 2047, 2048, 2049, 5000])
 def test_batch_sizes_across_kernel_variants(pa, n):
-    # The decode keeps each sequence's length and prefix in shared memory, so
-    # the block's footprint grows with the batch: at head_dim 128 it reaches
-    # the 227 KiB limit near 3,307 sequences, past which the compact 4-warp
-    # variant runs.  Batch sizes on both sides of that edge (where the
-    # footprint rounded up for the occupancy lookup would pass the limit)
-    # match the oracle.
+    # Up to 2048 sequences each decode block keeps the per-sequence lengths
+    # and unit prefix in its shared memory; larger batches have a one-block
+    # kernel build them once in the workspace.  Batch sizes on both sides of
+    # that edge match the oracle.
     rng = np.random.default_rng(n)
     lens = rng.integers(0, 48, size=n)
     w = synth.build("sizes", n, 16, 4, 128, "bf16", lens, seed=n, poison=True)
     check(pa, w, 0)
+
+
+@pytest.mark.parametrize("mode", [0, -1, 64])
+@pytest.mark.parametrize("Hq,Hkv,D,dtype", [(16, 1, 64, "f16"), (8, 2, 128, "bf16")])
+def test_twenty_thousand_ragged_sequences(pa, mode, Hq, Hkv, D, dtype):
+    # a continuous batch far above the shared-memory edge, at group 16 and 4,
+    # lengths 0..300 with NaN in every slot no live token holds
+    n = 20000
+    rng = np.random.default_rng(2000 + Hq)
+    lens = rng.integers(0, 301, size=n)
+    lens[rng.integers(0, n, size=50)] = 0
+    w = synth.build("b20k", n, Hq, Hkv, D, dtype, lens, seed=2001 + Hq, append=True, poison=True)
+    check(pa, w, mode)
+
+
+def test_group_above_sixteen_is_refused(pa):
+    w = synth.build("g17", 2, 17, 1, 64, "f16", [5, 9], seed=3)
+    dw = DevWorkload(w)
+    with pytest.raises(pa.PagedAttnError) as e:
+        pa.decode(dw.out, dw.q, dw.k, dw.v, dw.tables, dw.lens, w.scale)
+    assert e.value.status == 2                         # PA_ERR_UNSUPPORTED
 
 
 def test_bad_table_entry_is_flagged_not_faulting(pa):
