@@ -53,7 +53,7 @@ import numpy as np  # noqa: E402
 METRIC = "paged decode attn: effective KV-read HBM GB/s, % of GB300 peak; seqs/s"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
-DEFAULT_PARTITION = {"tiny": 0, "mha7b": 0, "gqa8b": 0, "long": 512, "parsamp": 0}
+DEFAULT_PARTITION = {"tiny": 0, "mha7b": 0, "gqa8b": 0, "long": 512, "parsamp": 0, "batch20k": 0}
 DESCRIPTION = {
     "tiny": "tiny decode: 4 seqs, 8/8 heads, head_dim 64, fp16, lens U[1,100], 64-block pool, +1 token",
     "mha7b": "MHA 7B-shaped decode: 64 seqs, 32/32 heads, head_dim 128, fp16, lens U[512,2048]",
@@ -63,6 +63,8 @@ DESCRIPTION = {
              "{32768,65536,98304,131072}, 512-token partitions + log-sum-exp merge"),
     "parsamp": ("parallel sampling: 16 prompts x 8 samples, 40/8 heads, head_dim 128, fp16, "
                 "1024 shared prompt tokens + U[0,256] + 1, 112 copy-on-write pairs per step"),
+    "batch20k": ("large continuous batch: 20000 seqs, 32/2 heads (group 16), head_dim 128, bf16, "
+                 "lens U[1,256], +1 token per seq; per-sequence arrays in the workspace"),
 }
 
 
@@ -129,7 +131,8 @@ def replica_seed(base_seed: int, rank: int) -> int:
 # ---------------------------------------------------------------------------
 def make_workload(name: str, seed_offset: int = 0):
     import synth
-    base = {"tiny": 1001, "mha7b": 1002, "gqa8b": 1003, "long": 1004, "parsamp": 1005}[name]
+    base = {"tiny": 1001, "mha7b": 1002, "gqa8b": 1003, "long": 1004, "parsamp": 1005,
+            "batch20k": 1008}[name]
     return synth.by_name(name, seed=replica_seed(base, seed_offset))
 
 
@@ -791,7 +794,7 @@ def measure_decode(name: str, args, device, rank: int, world: int, partition=Non
     return res
 
 
-NESTED = ("long", "mha7b", "parsamp", "tiny")
+NESTED = ("long", "mha7b", "parsamp", "tiny", "batch20k")
 
 
 def run_ours(args):

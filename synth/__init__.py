@@ -29,6 +29,8 @@ long        4      32/8     128  bf16   {32768, 65536, 98304, 131072},
                                          512-token split-K partitions
 parsamp     16x8   40/8     128  f16    1024 shared + U[0,256] + 1,
                                          copy-on-write of the last shared block
+batch20k    20000  32/2     128  bf16   U[1,256], +1 token (a large batch at
+                                         group 16; not one of the five)
 ==========  =====  =======  ===  =====  =======================================
 """
 from __future__ import annotations
@@ -405,6 +407,13 @@ def parsamp(poison=False, seed=1005, num_prompts=16, samples=8, prompt_len=1024,
     return w
 
 
+def batch20k(poison=False, seed=1008, num_seqs=20000):
+    """A large continuous batch: 20,000 sequences, 32 query / 2 kv heads
+    (group 16), head_dim 128, bf16, lengths U[1, 256], one new token each."""
+    lens = _len_rng(seed).integers(1, 256, size=num_seqs, endpoint=True)
+    return build("batch20k", num_seqs, 32, 2, 128, BF16, lens, seed, append=True, poison=poison)
+
+
 def build_prefill(name: str, num_heads: int, num_kv_heads: int, head_dim: int, dtype: str,
                   seq_lens, chunk_lens, seed: int, *, pool_factor: float = 1.25,
                   poison: bool = False, max_blocks: Optional[int] = None) -> Workload:
@@ -447,6 +456,7 @@ WORKLOADS = {
     "gqa8b": gqa8b,
     "long": long,
     "parsamp": parsamp,
+    "batch20k": batch20k,
     "prefill": prefill_chunks,
     "prefill_long": prefill_long,
 }
