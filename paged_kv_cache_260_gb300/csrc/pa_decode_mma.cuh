@@ -517,12 +517,8 @@ __global__ void __launch_bounds__(W * 32)
 decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
                   const __grid_constant__ CUtensorMap tmv)
 {
-    using Sh = MmaShape<D, NT>;
     using Lay = MmaLayout<D, NT, W, S>;
     using E = Elem<T>;
-    using M = Mma<T>;
-    constexpr int KS = Sh::KSTEPS;
-    constexpr uint32_t FULL = 0xffffffffu;
 
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
@@ -530,9 +526,7 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Lay::stages);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int n = p.num_seqs, Hkv = p.num_kv_heads, Hq = p.num_heads;
-    const int G = Hq / Hkv;
-    const int worker = blockIdx.x * W + warp;
+    const int n = p.num_seqs, Hq = p.num_heads;
     const bool seq_global = p.ws_pre != nullptr;
 
     if (lane == 0) {
