@@ -53,7 +53,8 @@ import numpy as np  # noqa: E402
 METRIC = "paged decode attn: effective KV-read HBM GB/s, % of GB300 peak; seqs/s"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
-DEFAULT_PARTITION = {"tiny": 0, "mha7b": 0, "gqa8b": 0, "long": 512, "parsamp": 0, "batch20k": 0}
+DEFAULT_PARTITION = {"tiny": 0, "mha7b": 0, "gqa8b": 0, "long": 512, "parsamp": 0, "batch20k": 0,
+                     "parsamp8k": 0}
 DESCRIPTION = {
     "tiny": "tiny decode: 4 seqs, 8/8 heads, head_dim 64, fp16, lens U[1,100], 64-block pool, +1 token",
     "mha7b": "MHA 7B-shaped decode: 64 seqs, 32/32 heads, head_dim 128, fp16, lens U[512,2048]",
@@ -65,7 +66,12 @@ DESCRIPTION = {
                 "1024 shared prompt tokens + U[0,256] + 1, 112 copy-on-write pairs per step"),
     "batch20k": ("large continuous batch: 20000 seqs, 32/2 heads (group 16), head_dim 128, bf16, "
                  "lens U[1,256], +1 token per seq; per-sequence arrays in the workspace"),
+    "parsamp8k": ("parallel sampling with a long prompt: 16 prompts x 8 samples, 40/8 heads, "
+                  "head_dim 128, fp16, 8192 shared prompt tokens + U[0,256] + 1, 112 "
+                  "copy-on-write pairs per step"),
 }
+# parallel-sampling workloads that run pa_decode_shared_prefix by default
+SHARED_DEFAULT = {"parsamp8k": True}
 
 
 # ---------------------------------------------------------------------------
@@ -132,7 +138,7 @@ def replica_seed(base_seed: int, rank: int) -> int:
 def make_workload(name: str, seed_offset: int = 0):
     import synth
     base = {"tiny": 1001, "mha7b": 1002, "gqa8b": 1003, "long": 1004, "parsamp": 1005,
-            "batch20k": 1008}[name]
+            "batch20k": 1008, "parsamp8k": 1009}[name]
     return synth.by_name(name, seed=replica_seed(base, seed_offset))
 
 
@@ -249,7 +255,7 @@ def physical_gpu_index(local_rank: int) -> int:
 class Step:
     """Device state of one replica and its decode step (graph-captured)."""
 
-    def __init__(self, w, device, partition_size):
+    def __init__(self, w, device, partition_size, shared=None):
         import torch
         import paged_kv_cache_260_gb300 as pa
         self.pa, self.w, self.dev, self.ps = pa, w, device, partition_size
@@ -270,12 +276,29 @@ class Step:
         self.slots = None if w.slot_mapping is None else torch.from_numpy(w.slot_mapping).to(device)
         self.pairs = (None if w.block_mapping is None or len(w.block_mapping) == 0
                       else torch.from_numpy(w.block_mapping).to(device))
-        self.ws = pa.workspace_for(self.q, self.k, self.tables, partition_size)
+        # parallel samples with a long shared prompt: the shared-prefix decode
+        # reads each prompt's shared blocks once per group of samples (with a
+        # short prompt its second decode pass costs more than it saves)
+        self.shared = (shared if shared is not None else SHARED_DEFAULT.get(w.name, False)) \
+            and "samples" in w.meta and partition_size == 0
+        if self.shared:
+            self.group = int(w.meta["samples"])
+            self.prefix_len = (-(-int(w.meta["prompt_len"]) // 16) - 1) * 16
+            n, hq, d = self.q.shape
+            nbytes = pa.decode_shared_prefix_workspace_size(n, self.group, self.prefix_len, hq,
+                                                            self.k.shape[1], d,
+                                                            self.tables.shape[1])
+            self.ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        else:
+            self.ws = pa.workspace_for(self.q, self.k, self.tables, partition_size)
         self.launches_per_step = self._count_launches()
 
     def _count_launches(self):
-        n = 1                                           # decode (append fused in)
-        n += int(self.pairs is not None)                # copy_blocks
+        n = int(self.pairs is not None)                 # copy_blocks
+        if self.shared:
+            # gather, prefix decode + merge, suffix decode + merge, final merge
+            return n + 6 + (2 if self.w.num_seqs > 2048 else 0)
+        n += 1                                          # decode (append fused in)
         if self.ps >= 0:
             n += 1                                      # merge of cut runs / partitions
         if self.ps > 0 and self.tables.shape[1] * 16 > self.ps:
@@ -289,7 +312,11 @@ class Step:
             pa.copy_blocks(self.k, self.v, self.pairs)
         if ev_pair is not None:
             ev_pair[0].record()
-        if self.slots is not None:
+        if self.shared:
+            pa.decode_shared_prefix(self.out, self.q, self.k, self.v, self.tables, self.lens,
+                                    self.group, self.prefix_len, self.w.scale, k_new=self.k_new,
+                                    v_new=self.v_new, slot_mapping=self.slots, workspace=self.ws)
+        elif self.slots is not None:
             # reshape_and_cache of the newest token fused into the decode launch
             pa.decode_append(self.out, self.q, self.k, self.v, self.tables, self.lens, self.k_new,
                              self.v_new, self.slots, self.w.scale, partition_size=self.ps,
@@ -705,7 +732,7 @@ def measure_decode(name: str, args, device, rank: int, world: int, partition=Non
     import paged_kv_cache_260_gb300 as pa
     ps = DEFAULT_PARTITION[name] if partition is None else partition
     w = make_workload(name, rank)
-    st = Step(w, device, ps)
+    st = Step(w, device, ps, shared={"auto": None, "on": True, "off": False}[args.shared_prefix])
     kv_bytes = w.kv_read_bytes()
     # blocks that sequences share (parallel sampling) need leaving HBM once
     # per step: the L2 decision and the HBM roofline count them once
@@ -739,6 +766,18 @@ def measure_decode(name: str, args, device, rank: int, world: int, partition=Non
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         parity = parity_vs_oracle(w, st.out)
     shared = unique_bytes != kv_bytes
+    other = None
+    if "samples" in w.meta and ps == 0 and not args.no_other_decode:
+        # the same step with the other decode of a parallel-sampling batch,
+        # timed the same way, for comparison
+        st_o = Step(w, device, ps, shared=not st.shared)
+        o_elapsed, o_call, _ = time_decode(st_o, w, args, device, big, use_graph)
+        other = {"ms_per_step": o_elapsed / args.steps, "call_ms": o_call,
+                 "value": kv_bytes / (o_elapsed / args.steps * 1e-3) / 1e9,
+                 "decode": ("pa_decode_shared_prefix (the shared prompt blocks read once per "
+                            "group)" if st_o.shared else
+                            "pa_decode_append (every sample reads the shared prompt blocks)")}
+        del st_o
     res = {
         "value": value,
         "unit": "GB/s",
@@ -755,7 +794,10 @@ def measure_decode(name: str, args, device, rank: int, world: int, partition=Non
             "kv_bytes_per_step": kv_bytes,
             "unique_kv_bytes_per_step": unique_bytes,
             "step": ("copy_blocks + " if w.block_mapping is not None else "")
-                    + ("decode with reshape_and_cache fused (pa_decode_append)"
+                    + ("shared-prefix decode (pa_decode_shared_prefix, groups of %d samples, "
+                       "%d shared tokens) with reshape_and_cache fused"
+                       % (st.group, st.prefix_len) if st.shared else
+                       "decode with reshape_and_cache fused (pa_decode_append)"
                        if w.slot_mapping is not None else "decode") + " + merge",
             "l2": ("inputs larger than L2 (K/V read per step %.0f MB vs 129 MB L2)"
                    % (unique_bytes / 1e6) if big else
@@ -769,8 +811,11 @@ def measure_decode(name: str, args, device, rank: int, world: int, partition=Non
                        f"steps cycle through {copies} copies of the pool (>= 2 x L2 in all), "
                        f"no flush in the timed region")},
         "roofline": {"bound": "hbm",
-                     "kernel": "decode_mma_kernel + merge kernel(s): one pa_decode / "
-                               "pa_decode_append call",
+                     "kernel": ("one pa_decode_shared_prefix call: gather, decode_mma_kernel + "
+                                "merge on the shared prefix, on the suffixes, final merge"
+                                if st.shared else
+                                "decode_mma_kernel + merge kernel(s): one pa_decode / "
+                                "pa_decode_append call"),
                      "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak,
                      "peak_source": (peak_src + " (MEASURED_PEAKS.json hbm_gbs, copy burst)"
@@ -788,13 +833,15 @@ def measure_decode(name: str, args, device, rank: int, world: int, partition=Non
     }
     if shared:
         res["logical_kv_gbps"] = value
+    if other is not None:
+        res["shared_prefix_decode" if not st.shared else "plain_decode"] = other
     if carry is not None:
         res["l2_carryover"] = carry
     res["_w"] = w
     return res
 
 
-NESTED = ("long", "mha7b", "parsamp", "tiny", "batch20k")
+NESTED = ("long", "mha7b", "parsamp", "tiny", "batch20k", "parsamp8k")
 
 
 def run_ours(args):
@@ -1205,6 +1252,11 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip the oracle legs (cpu_baseline and parity)")
     ap.add_argument("--no-l2-check", action="store_true")
+    ap.add_argument("--no-other-decode", action="store_true",
+                    help="parallel sampling: skip timing the other decode beside it")
+    ap.add_argument("--shared-prefix", choices=["auto", "on", "off"], default="auto",
+                    help="parallel sampling: pa_decode_shared_prefix (on) or pa_decode_append "
+                         "(off); auto: on for the long-prompt workload")
     ap.add_argument("--only-headline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:

@@ -221,6 +221,48 @@ int pa_decode_append(void *out, const void *q, void *k_cache, void *v_cache,
                      void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * One decode step of a batch whose sequences come in groups that share a
+ * prompt prefix: parallel samples of one prompt keep the prompt's blocks
+ * shared by reference (block sharing with copy-on-write, section
+ * 系统实现要点 and the page-sharing row of the OS-paging table in the vLLM
+ * reading notes).  The result equals pa_decode (or pa_decode_append when
+ * k_new, v_new and slot_mapping are given) up to rounding, but each group's
+ * shared prefix is read once for the whole group instead of once per
+ * sequence: the prefix is decoded as a batch of virtual sequences, each
+ * holding up to 16 query columns (sample, head) of one group and kv head
+ * and reading the group's first table; each sequence's own tokens past the
+ * prefix are a second decode; the two partial results of every (sequence,
+ * head) are combined with the log-sum-exp rule of the split-K merge.
+ *
+ *   group_size   sequences [g*group_size, (g+1)*group_size) form group g;
+ *                num_seqs must be a multiple of it
+ *   prefix_len   tokens of the shared prefix, a multiple of 16, > 0; the
+ *                first prefix_len/16 entries of the tables of a group's
+ *                sequences must name the same blocks (not checked: the prefix
+ *                is read through the group's first table), and every sequence
+ *                must be longer than prefix_len when tokens are appended (the
+ *                new token must lie past the shared prefix, as copy-on-write
+ *                guarantees)
+ *   k_new, v_new, slot_mapping  as in pa_decode_append, or all NULL
+ *   workspace    at least pa_decode_shared_prefix_workspace_size(...) bytes,
+ *                256-byte aligned, caller-owned, no initialisation needed
+ * Other arguments as pa_decode.  Launches: a gather of the virtual batch, the
+ * two decodes (each with its merge) and the final merge.  A sequence shorter
+ * than prefix_len sets PA_DEVERR_SEQLEN_RANGE.
+ */
+size_t pa_decode_shared_prefix_workspace_size(int num_seqs, int group_size, int prefix_len,
+                                              int num_heads, int num_kv_heads, int head_dim,
+                                              int max_blocks_per_seq);
+
+int pa_decode_shared_prefix(void *out, const void *q, void *k_cache, void *v_cache,
+                            const int32_t *block_tables, const int32_t *seq_lens,
+                            const void *k_new, const void *v_new, const int64_t *slot_mapping,
+                            int num_seqs, int group_size, int prefix_len, int num_heads,
+                            int num_kv_heads, int head_dim, int block_size,
+                            int max_blocks_per_seq, int num_blocks, float scale, int dtype,
+                            void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * pa_decode without a workspace argument, for callers that cannot allocate
  * device memory: an engine that gives (nearly) all free HBM to its KV block
  * pool at start-up and forbids allocations afterwards, a plugin whose host

@@ -18,7 +18,8 @@ import threading
 
 __all__ = [
     "PagedAttnError", "load", "version", "decode", "decode_workspace_size", "workspace_for",
-    "decode_noalloc", "decode_append", "prefill", "prefill_workspace_size",
+    "decode_noalloc", "decode_append", "decode_shared_prefix",
+    "decode_shared_prefix_workspace_size", "prefill", "prefill_workspace_size",
     "reshape_and_cache", "copy_blocks", "swap_blocks", "gather_kv", "validate_tables",
     "selftest_bounded_wait", "get_device_error",
     "PA_DTYPE_F16", "PA_DTYPE_BF16", "DEVERR", "STATUS",
@@ -67,6 +68,11 @@ def load(path: str = LIB_PATH):
         L.pa_decode_append.restype = i
         L.pa_decode_append.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i,
                                        f, i, i, vp, sz, vp]
+        L.pa_decode_shared_prefix_workspace_size.restype = sz
+        L.pa_decode_shared_prefix_workspace_size.argtypes = [i, i, i, i, i, i, i]
+        L.pa_decode_shared_prefix.restype = i
+        L.pa_decode_shared_prefix.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i,
+                                              i, i, i, i, f, i, vp, sz, vp]
         L.pa_decode_noalloc.restype = i
         L.pa_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, vp]
         L.pa_reshape_and_cache.restype = i
@@ -210,6 +216,41 @@ def decode_append(out, q, k_cache, v_cache, block_tables, seq_lens, k_new, v_new
                                  float(scale), _dtype_code(q), int(partition_size),
                                  _ptr(workspace), wbytes, _stream(stream))
     _check("pa_decode_append", rc)
+    return out
+
+
+def decode_shared_prefix_workspace_size(num_seqs, group_size, prefix_len, num_heads,
+                                        num_kv_heads, head_dim, max_blocks_per_seq) -> int:
+    return int(load().pa_decode_shared_prefix_workspace_size(
+        num_seqs, group_size, prefix_len, num_heads, num_kv_heads, head_dim, max_blocks_per_seq))
+
+
+def decode_shared_prefix(out, q, k_cache, v_cache, block_tables, seq_lens, group_size,
+                         prefix_len, scale, k_new=None, v_new=None, slot_mapping=None,
+                         workspace=None, stream=None):
+    """pa_decode_shared_prefix: decode (with the newest tokens appended when
+    k_new, v_new and slot_mapping are given) of a batch whose consecutive
+    groups of `group_size` sequences share their first `prefix_len` tokens'
+    blocks; the shared prefix is read once per group."""
+    n, hq, d = q.shape
+    nb, hkv, bs, d2 = k_cache.shape
+    _require(out.shape == q.shape and d2 == d and v_cache.shape == k_cache.shape, "shapes")
+    _require(block_tables.dim() == 2 and block_tables.shape[0] == n and seq_lens.shape == (n,),
+             "table shapes")
+    if k_new is not None:
+        _require(k_new.shape == (n, hkv, d) and v_new.shape == k_new.shape and
+                 slot_mapping.shape == (n,), "new-token shapes")
+    if workspace is None:
+        nbytes = decode_shared_prefix_workspace_size(n, group_size, prefix_len, hq, hkv, d,
+                                                     block_tables.shape[1])
+        workspace = _scratch(nbytes, q.device, stream) if nbytes else None
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load().pa_decode_shared_prefix(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(seq_lens),
+        _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), n, int(group_size), int(prefix_len), hq,
+        hkv, d, bs, block_tables.shape[1], nb, float(scale), _dtype_code(q), _ptr(workspace),
+        wbytes, _stream(stream))
+    _check("pa_decode_shared_prefix", rc)
     return out
 
 

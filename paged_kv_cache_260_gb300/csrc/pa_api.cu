@@ -12,6 +12,7 @@
 #include "pa_internal.h"
 #include "pa_prefill_abi.h"
 #include "pa_schedule.cuh"
+#include "pa_shared.h"
 #include "pagedattn.h"
 
 namespace pa {
@@ -352,12 +353,21 @@ size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, i
         .total;
 }
 
+// What a decode does beyond pa_decode: the fused append, partial outputs,
+// tokens skipped at the start of every sequence.
+struct DecodeExtra {
+    const void *k_new = nullptr, *v_new = nullptr;
+    const int64_t *slot_mapping = nullptr;
+    float *out_m = nullptr, *out_l = nullptr, *out_o = nullptr;
+    int len_offset = 0;
+};
+
 static int decode_impl(void *out, const void *q, const void *k_cache, const void *v_cache,
                        const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,
                        int num_heads, int num_kv_heads, int head_dim, int block_size,
                        int max_blocks_per_seq, int num_blocks, float scale, int dtype,
                        int partition_size, void *workspace, size_t workspace_bytes, void *stream,
-                       const void *k_new, const void *v_new, const int64_t *slot_mapping)
+                       const DecodeExtra &x)
 {
     int rc = check_common(num_kv_heads, head_dim, block_size, num_blocks, dtype);
     if (rc != PA_OK)
@@ -371,7 +381,7 @@ static int decode_impl(void *out, const void *q, const void *k_cache, const void
         return PA_ERR_UNSUPPORTED;
     if (num_seqs == 0)
         return PA_OK;
-    if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens)
+    if ((!out && !x.out_o) || !q || !k_cache || !v_cache || !block_tables || !seq_lens)
         return PA_ERR_INVALID_ARG;
     if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
         !aligned(block_tables, 4) || !aligned(seq_lens, 4))
@@ -450,9 +460,13 @@ static int decode_impl(void *out, const void *q, const void *k_cache, const void
     p.v_cache = v_cache;
     p.block_tables = block_tables;
     p.seq_lens = seq_lens;
-    p.k_new = k_new;
-    p.v_new = v_new;
-    p.slot_mapping = slot_mapping;
+    p.k_new = x.k_new;
+    p.v_new = x.v_new;
+    p.slot_mapping = x.slot_mapping;
+    p.out_m = x.out_m;
+    p.out_l = x.out_l;
+    p.out_o = x.out_o;
+    p.len_offset = x.len_offset;
     char *ws = static_cast<char *>(workspace);
     if (wl.total > 0) {
         p.ws_m = reinterpret_cast<float *>(ws + wl.m_off);
@@ -520,8 +534,7 @@ int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache
 {
     return decode_impl(out, q, k_cache, v_cache, block_tables, seq_lens, num_seqs, num_heads,
                        num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks, scale,
-                       dtype, partition_size, workspace, workspace_bytes, stream, nullptr, nullptr,
-                       nullptr);
+                       dtype, partition_size, workspace, workspace_bytes, stream, DecodeExtra{});
 }
 
 int pa_decode_append(void *out, const void *q, void *k_cache, void *v_cache,
@@ -534,10 +547,177 @@ int pa_decode_append(void *out, const void *q, void *k_cache, void *v_cache,
     if (num_seqs > 0 && (!k_new || !v_new || !slot_mapping || !aligned(k_new, 16) ||
                          !aligned(v_new, 16) || !aligned(slot_mapping, 8)))
         return PA_ERR_INVALID_ARG;
+    DecodeExtra x;
+    x.k_new = k_new;
+    x.v_new = v_new;
+    x.slot_mapping = slot_mapping;
     return decode_impl(out, q, k_cache, v_cache, block_tables, seq_lens, num_seqs, num_heads,
                        num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks, scale,
-                       dtype, partition_size, workspace, workspace_bytes, stream, k_new, v_new,
-                       slot_mapping);
+                       dtype, partition_size, workspace, workspace_bytes, stream, x);
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// pa_decode_shared_prefix: the shared prefix of each group decoded once, as
+// a batch of virtual sequences of up to 16 query columns, the suffixes as a
+// second decode, both with partial outputs, then one log-sum-exp merge.
+// ---------------------------------------------------------------------------
+namespace pa {
+namespace {
+
+struct SharedLayout {
+    size_t qv, tv, lv, pm, pl, po, sm, sl, so, dws, dws_bytes, total;
+    int nvb, cv, nvseq;
+};
+
+bool shared_layout(int num_seqs, int group_size, int prefix_len, int num_heads, int num_kv_heads,
+                   int head_dim, int max_blocks_per_seq, SharedLayout *L)
+{
+    if (num_seqs <= 0 || group_size <= 0 || num_seqs % group_size || prefix_len <= 0 ||
+        prefix_len % kBlockSize || num_heads <= 0 || num_kv_heads <= 0 ||
+        num_heads % num_kv_heads || max_blocks_per_seq <= 0 ||
+        prefix_len / kBlockSize > max_blocks_per_seq || (head_dim != 64 && head_dim != 128))
+        return false;
+    DeviceState *ds;
+    if (device_state(&ds) != PA_OK)
+        return false;
+    const int G = num_heads / num_kv_heads;
+    const long long cols = (long long)group_size * G;
+    L->cv = cols > 8 ? 16 : 8;
+    L->nvb = (int)((cols + L->cv - 1) / L->cv);
+    const long long nvs = (long long)(num_seqs / group_size) * L->nvb;
+    if (nvs >= (1LL << 30))
+        return false;
+    L->nvseq = (int)nvs;
+    const size_t P = (size_t)(prefix_len / kBlockSize);
+    const size_t vrows = (size_t)nvs * num_kv_heads * L->cv, srows = (size_t)num_seqs * num_heads;
+    size_t at = 0;
+    auto take = [&](size_t bytes) {
+        const size_t off = at;
+        at = round_up(at + bytes, 256);
+        return off;
+    };
+    L->qv = take(vrows * head_dim * 2);
+    L->tv = take((size_t)nvs * P * sizeof(int32_t));
+    L->lv = take((size_t)nvs * sizeof(int32_t));
+    L->pm = take(vrows * sizeof(float));
+    L->pl = take(vrows * sizeof(float));
+    L->po = take(vrows * head_dim * sizeof(float));
+    L->sm = take(srows * sizeof(float));
+    L->sl = take(srows * sizeof(float));
+    L->so = take(srows * head_dim * sizeof(float));
+    const int workers = ds->num_sms * kMaxWarpsPerSM;
+    const size_t d1 = workspace_layout(kModeBalanced, (int)nvs, num_kv_heads * L->cv, num_kv_heads,
+                                       head_dim, 1, workers).total;
+    const size_t d2 = workspace_layout(kModeBalanced, num_seqs, num_heads, num_kv_heads, head_dim,
+                                       1, workers).total;
+    L->dws_bytes = std::max(d1, d2);
+    L->dws = take(L->dws_bytes);
+    L->total = at;
+    return true;
+}
+
+}  // namespace
+}  // namespace pa
+
+extern "C" {
+
+size_t pa_decode_shared_prefix_workspace_size(int num_seqs, int group_size, int prefix_len,
+                                              int num_heads, int num_kv_heads, int head_dim,
+                                              int max_blocks_per_seq)
+{
+    SharedLayout L;
+    if (!shared_layout(num_seqs, group_size, prefix_len, num_heads, num_kv_heads, head_dim,
+                       max_blocks_per_seq, &L))
+        return 0;
+    return L.total;
+}
+
+int pa_decode_shared_prefix(void *out, const void *q, void *k_cache, void *v_cache,
+                            const int32_t *block_tables, const int32_t *seq_lens,
+                            const void *k_new, const void *v_new, const int64_t *slot_mapping,
+                            int num_seqs, int group_size, int prefix_len, int num_heads,
+                            int num_kv_heads, int head_dim, int block_size,
+                            int max_blocks_per_seq, int num_blocks, float scale, int dtype,
+                            void *workspace, size_t workspace_bytes, void *stream)
+{
+    int rc = check_common(num_kv_heads, head_dim, block_size, num_blocks, dtype);
+    if (rc != PA_OK)
+        return rc;
+    if (num_seqs < 0 || num_heads <= 0 || num_heads % num_kv_heads || !isfinite(scale))
+        return PA_ERR_INVALID_ARG;
+    if (num_heads / num_kv_heads > kMaxGroup)
+        return PA_ERR_UNSUPPORTED;
+    if (num_seqs == 0)
+        return PA_OK;
+    const bool append = k_new || v_new || slot_mapping;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens ||
+        (append && (!k_new || !v_new || !slot_mapping)))
+        return PA_ERR_INVALID_ARG;
+    if (!aligned(out, 16) || !aligned(q, 16) || !aligned(block_tables, 4) ||
+        (append && (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(slot_mapping, 8))))
+        return PA_ERR_INVALID_ARG;
+    SharedLayout L;
+    if (!shared_layout(num_seqs, group_size, prefix_len, num_heads, num_kv_heads, head_dim,
+                       max_blocks_per_seq, &L))
+        return PA_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < L.total || !aligned(workspace, 256))
+        return PA_ERR_WORKSPACE;
+    char *ws = static_cast<char *>(workspace);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int P = prefix_len / kBlockSize;
+
+    SharedParams sp{};
+    sp.q = q;
+    sp.block_tables = block_tables;
+    sp.num_seqs = num_seqs;
+    sp.group_size = group_size;
+    sp.prefix_tiles = P;
+    sp.num_heads = num_heads;
+    sp.num_kv_heads = num_kv_heads;
+    sp.head_dim = head_dim;
+    sp.max_blocks = max_blocks_per_seq;
+    sp.nvb = L.nvb;
+    sp.cv = L.cv;
+    sp.q_v = ws + L.qv;
+    sp.tables_v = reinterpret_cast<int32_t *>(ws + L.tv);
+    sp.lens_v = reinterpret_cast<int32_t *>(ws + L.lv);
+    sp.pm = reinterpret_cast<float *>(ws + L.pm);
+    sp.pl = reinterpret_cast<float *>(ws + L.pl);
+    sp.po = reinterpret_cast<float *>(ws + L.po);
+    sp.sm = reinterpret_cast<float *>(ws + L.sm);
+    sp.sl = reinterpret_cast<float *>(ws + L.sl);
+    sp.so = reinterpret_cast<float *>(ws + L.so);
+    sp.out = out;
+    rc = cuda_status(launch_shared_prep(sp, L.nvseq, st));
+    if (rc != PA_OK)
+        return rc;
+    // the prefix, once per group: virtual sequences of cv query columns each
+    DecodeExtra x1;
+    x1.out_m = reinterpret_cast<float *>(ws + L.pm);
+    x1.out_l = reinterpret_cast<float *>(ws + L.pl);
+    x1.out_o = reinterpret_cast<float *>(ws + L.po);
+    rc = decode_impl(nullptr, ws + L.qv, k_cache, v_cache, sp.tables_v, sp.lens_v, L.nvseq,
+                     num_kv_heads * L.cv, num_kv_heads, head_dim, block_size, P, num_blocks, scale,
+                     dtype, 0, ws + L.dws, L.dws_bytes, stream, x1);
+    if (rc != PA_OK)
+        return rc;
+    // every sequence's own tokens past the prefix (and the new token)
+    DecodeExtra x2;
+    x2.k_new = k_new;
+    x2.v_new = v_new;
+    x2.slot_mapping = slot_mapping;
+    x2.out_m = reinterpret_cast<float *>(ws + L.sm);
+    x2.out_l = reinterpret_cast<float *>(ws + L.sl);
+    x2.out_o = reinterpret_cast<float *>(ws + L.so);
+    x2.len_offset = prefix_len;
+    rc = decode_impl(nullptr, q, k_cache, v_cache, block_tables + P, seq_lens, num_seqs, num_heads,
+                     num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks, scale,
+                     dtype, 0, ws + L.dws, L.dws_bytes, stream, x2);
+    if (rc != PA_OK)
+        return rc;
+    return cuda_status(launch_shared_merge(sp, dtype == PA_DTYPE_BF16, st));
 }
 
 // Query tiles per (sequence, kv head) of a prefill grid, 0 on bad arguments.

@@ -438,7 +438,32 @@ __device__ __forceinline__ void decode_worker(const DecodeParams &p, const CUten
             }
             const float inv0 = 1.f / l[j][0], inv1 = 1.f / l[j][1];
             const int h0 = 8 * j + 2 * qd, h1 = h0 + 1;
-            if (whole) {
+            if (whole && p.out_o) {
+                // partial-output mode: m, l and the normalised result, fp32
+                const size_t row0 = (size_t)s * Hq + h * G + h0, row1 = row0 + 1;
+#pragma unroll
+                for (int mt = 0; mt < KS; ++mt) {
+                    const int d0 = 16 * mt + r;
+                    if (h0 < G) {
+                        p.out_o[row0 * D + d0] = o[j][mt][0] * inv0;
+                        p.out_o[row0 * D + d0 + 8] = o[j][mt][2] * inv0;
+                    }
+                    if (h1 < G) {
+                        p.out_o[row1 * D + d0] = o[j][mt][1] * inv1;
+                        p.out_o[row1 * D + d0 + 8] = o[j][mt][3] * inv1;
+                    }
+                }
+                if (r == 0) {
+                    if (h0 < G) {
+                        p.out_m[row0] = m[j][0] * kLn2;
+                        p.out_l[row0] = l[j][0];
+                    }
+                    if (h1 < G) {
+                        p.out_m[row1] = m[j][1] * kLn2;
+                        p.out_l[row1] = l[j][1];
+                    }
+                }
+            } else if (whole) {
                 T *out = reinterpret_cast<T *>(p.out) + ((size_t)s * Hq + h * G) * D;
 #pragma unroll
                 for (int mt = 0; mt < KS; ++mt) {
@@ -566,12 +591,22 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
     else
         any_share = __syncthreads_or(share_any_of(share, n, tid, W * 32));
 
-    // sequences without tokens get zeros (no piece ever covers them)
+    // sequences without tokens get zeros (no piece ever covers them); in
+    // partial-output mode an empty partial result (m = -inf, l = 0)
     for (int s = blockIdx.x; s < n; s += gridDim.x) {
         if (lens[s] == 0) {
-            T *o = reinterpret_cast<T *>(p.out) + (size_t)s * Hq * D;
-            for (int e = tid; e < Hq * D; e += W * 32)
-                o[e] = E::from_f(0.f);
+            if (p.out_o) {
+                for (int e = tid; e < Hq * D; e += W * 32)
+                    p.out_o[(size_t)s * Hq * D + e] = 0.f;
+                for (int e = tid; e < Hq; e += W * 32) {
+                    p.out_m[(size_t)s * Hq + e] = -INFINITY;
+                    p.out_l[(size_t)s * Hq + e] = 0.f;
+                }
+            } else {
+                T *o = reinterpret_cast<T *>(p.out) + (size_t)s * Hq * D;
+                for (int e = tid; e < Hq * D; e += W * 32)
+                    o[e] = E::from_f(0.f);
+            }
         }
     }
 
@@ -658,6 +693,16 @@ __global__ void __launch_bounds__(512) merge_cut_kernel(const DecodeParams p)
             p.ws_m[row] = Mx;
             p.ws_l[row] = Ws;
         }
+    } else if (p.out_o) {
+        const size_t row = (size_t)s * Hq + h * G + g;
+        float *dst = p.out_o + row * D + lane * V;
+#pragma unroll
+        for (int v = 0; v < V; ++v)
+            dst[v] = acc[v] * inv;
+        if (lane == 0) {
+            p.out_m[row] = Mx;
+            p.out_l[row] = Ws;
+        }
     } else {
         using M = Mma<T>;
         T *dst = reinterpret_cast<T *>(p.out) + ((size_t)s * Hq + h * G + g) * D + lane * V;
@@ -687,8 +732,8 @@ __global__ void __launch_bounds__(512) merge_part_kernel(const DecodeParams p)
     const int g = blockIdx.x % G, run = blockIdx.x / G;
     const int s = run / Hkv, h = run % Hkv;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    int L = __ldg(p.seq_lens + s);
-    L = max(0, min(L, p.max_blocks * kBlockSize));
+    int L = __ldg(p.seq_lens + s) - p.len_offset;
+    L = max(0, min(L, p.max_blocks * kBlockSize - p.len_offset));
     const int nt = (L + kBlockSize - 1) / kBlockSize;
     const int np = (nt + p.part_tiles - 1) / p.part_tiles;
     if (np <= 1)

@@ -37,6 +37,9 @@ struct DecodeParams {
     int32_t *ws_pre;       // large batches: unit prefix [num_seqs + 1] in the workspace, or null
     int32_t *ws_lens;      //   clamped lengths [num_seqs] (null: all three in shared memory)
     uint8_t *ws_share;     //   and first-block-shared flags [num_seqs]
+    float *out_m;          // partial-output mode (non-null): each (sequence, query head)'s
+    float *out_l;          //   m, l and normalised o go to row s * num_heads + h of these
+    float *out_o;          //   [num_seqs][num_heads](x head_dim) fp32 arrays instead of `out`
     uint32_t *err;         // device error bits (PA_DEVERR_*)
     int num_seqs;
     int num_heads;
@@ -49,6 +52,8 @@ struct DecodeParams {
     int min_tiles;         // least tiles given to one worker
     int workers;           // warps of the decode grid
     float scale_log2;      // scale * log2(e): scores are kept in base 2
+    int len_offset;        // tokens skipped at the start of every sequence (block_tables
+                           // already points past them); lengths count from there
 };
 
 // Kernels of one (dtype, head_dim, query columns) instantiation.

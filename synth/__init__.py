@@ -407,6 +407,14 @@ def parsamp(poison=False, seed=1005, num_prompts=16, samples=8, prompt_len=1024,
     return w
 
 
+def parsamp8k(poison=False, seed=1009):
+    """Parallel sampling with a long prompt: as parsamp, with 8192 prompt
+    tokens (8176 of them in blocks shared by the 8 samples of a prompt)."""
+    w = parsamp(poison=poison, seed=seed, prompt_len=8192)
+    w.name = "parsamp8k"
+    return w
+
+
 def batch20k(poison=False, seed=1008, num_seqs=20000):
     """A large continuous batch: 20,000 sequences, 32 query / 2 kv heads
     (group 16), head_dim 128, bf16, lengths U[1, 256], one new token each."""
@@ -457,6 +465,7 @@ WORKLOADS = {
     "long": long,
     "parsamp": parsamp,
     "batch20k": batch20k,
+    "parsamp8k": parsamp8k,
     "prefill": prefill_chunks,
     "prefill_long": prefill_long,
 }

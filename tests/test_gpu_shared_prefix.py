@@ -1,0 +1,121 @@
+"""GPU parity of pa_decode_shared_prefix against the fp64 oracle.
+
+Parallel samples of one prompt share the prompt's blocks (copy-on-write of
+the last, partly filled or written-to block).  The shared-prefix decode
+reads each group's shared blocks once, as virtual sequences of up to 16
+query columns, decodes every sample's own tokens separately and merges the
+two partial results.  Every case runs the whole step (copy_blocks, then the
+decode with the new tokens appended) on NaN-poisoned pools and compares
+with the oracle's step within the decode tolerance; the pools must come out
+bit-identical to the oracle's.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from gpu_util import TOL, DevWorkload, host_bits, max_err
+
+pytestmark = pytest.mark.gpu
+
+
+def shared_prefix_len(w):
+    """Tokens of the blocks every sample of a group names (the prompt's full
+    blocks before the copied last one)."""
+    pb = -(-w.meta["prompt_len"] // 16)
+    return (pb - 1) * 16
+
+
+def run(pa, w, append=True, prefix_len=None, group=None):
+    dw = DevWorkload(w)
+    pa.copy_blocks(dw.k, dw.v, dw.pairs)
+    out = torch.full_like(dw.q, float("nan"))
+    kw = dict(k_new=dw.k_new, v_new=dw.v_new, slot_mapping=dw.slots) if append else {}
+    if not append:
+        pa.reshape_and_cache(dw.k_new, dw.v_new, dw.k, dw.v, dw.slots)
+    pa.decode_shared_prefix(out, dw.q, dw.k, dw.v, dw.tables, dw.lens,
+                            group or w.meta["samples"],
+                            shared_prefix_len(w) if prefix_len is None else prefix_len,
+                            w.scale, **kw)
+    torch.cuda.synchronize()
+    return dw, out
+
+
+@pytest.mark.parametrize("append", [True, False])
+def test_parallel_sampling_config(pa, append):
+    # 16 prompts x 8 samples, 40/8 heads (40 query columns per group and kv
+    # head: three virtual sequences), 1024-token prompt: 1008 shared tokens
+    w = synth.parsamp(poison=True)
+    dw, out = run(pa, w, append)
+    assert pa.get_device_error() == 0
+    ref, k_ref, v_ref = oracle.step(w)
+    assert max_err(out, ref) <= TOL[w.dtype]
+    assert np.array_equal(host_bits(dw.k), k_ref) and np.array_equal(host_bits(dw.v), v_ref)
+
+
+# A prompt that ends inside a block is copied from the original every step,
+# so the samples' own tokens past the prompt in that block would not survive
+# the copy (the NaN poison of the original's empty slots would reach the
+# oracle): such prompts take no suffix here; block-aligned prompts do.
+@pytest.mark.parametrize("prompts,samples,prompt_len,hq,hkv,d,dtype", [
+    (2, 8, 40, 8, 2, 128, "f16"),      # unaligned prompt: 32 shared tokens, new token in the copy
+    (3, 2, 304, 32, 8, 128, "bf16"),   # 8 columns: one 8-column virtual sequence
+    (2, 3, 512, 16, 1, 64, "f16"),     # 48 columns, group 16, head_dim 64
+    (1, 16, 128, 8, 8, 64, "bf16"),    # MHA, 16 samples: 16 columns
+    (4, 5, 1008, 12, 4, 128, "f16"),   # 15 columns
+    (2, 4, 64, 64, 4, 128, "bf16"),    # group 16 x 4 samples = 64 columns
+    (2, 4, 200, 16, 4, 64, "bf16"),    # unaligned, head_dim 64
+])
+def test_shapes(pa, prompts, samples, prompt_len, hq, hkv, d, dtype):
+    suffix = None if prompt_len % 16 == 0 else [0] * (prompts * samples)
+    w = synth.parsamp(poison=True, num_prompts=prompts, samples=samples, prompt_len=prompt_len,
+                      max_suffix=70, num_heads=hq, num_kv_heads=hkv, head_dim=d, dtype=dtype,
+                      seed=prompts * 100 + samples, suffix_lens=suffix)
+    dw, out = run(pa, w)
+    assert pa.get_device_error() == 0
+    ref, k_ref, v_ref = oracle.step(w)
+    assert max_err(out, ref) <= TOL[w.dtype]
+    assert np.array_equal(host_bits(dw.k), k_ref)
+
+
+def test_shorter_shared_prefix_and_single_sample_groups(pa):
+    # any multiple of 16 up to the shared blocks is a valid prefix, and a
+    # group of one shares with nobody: both give the same result
+    w = synth.parsamp(poison=True, num_prompts=4, samples=4, prompt_len=208, max_suffix=40,
+                      num_heads=16, num_kv_heads=4, seed=9)
+    ref, _, _ = oracle.step(w)
+    for prefix_len, group in ((16, 4), (96, 4), (shared_prefix_len(w), 2), (64, 1)):
+        _, out = run(pa, w, prefix_len=prefix_len, group=group)
+        assert pa.get_device_error() == 0
+        assert max_err(out, ref) <= TOL[w.dtype], (prefix_len, group)
+
+
+def test_matches_plain_decode(pa):
+    w = synth.parsamp(poison=True, num_prompts=4, samples=8, prompt_len=512, max_suffix=100,
+                      seed=31)
+    dw, out = run(pa, w)
+    b = DevWorkload(w)
+    pa.copy_blocks(b.k, b.v, b.pairs)
+    pa.decode_append(b.out, b.q, b.k, b.v, b.tables, b.lens, b.k_new, b.v_new, b.slots, w.scale)
+    torch.cuda.synchronize()
+    assert float((out.float() - b.out.float()).abs().max()) <= TOL[w.dtype]
+    assert torch.equal(dw.k.view(torch.int16), b.k.view(torch.int16))
+
+
+def test_bad_arguments(pa):
+    w = synth.parsamp(num_prompts=2, samples=4, prompt_len=64, max_suffix=10)
+    dw = DevWorkload(w)
+    for group, prefix in ((3, 48), (4, 40), (4, 0), (0, 48)):
+        with pytest.raises(pa.PagedAttnError) as e:
+            pa.decode_shared_prefix(dw.out, dw.q, dw.k, dw.v, dw.tables, dw.lens, group, prefix,
+                                    w.scale)
+        assert e.value.status in (1, 3)
+
+
+def test_sequence_shorter_than_prefix_is_flagged(pa):
+    w = synth.parsamp(num_prompts=2, samples=4, prompt_len=64, max_suffix=10)
+    dw = DevWorkload(w)
+    dw.lens[1] = 20
+    pa.decode_shared_prefix(dw.out, dw.q, dw.k, dw.v, dw.tables, dw.lens, 4, 48, w.scale)
+    assert pa.get_device_error() & pa.DEVERR["SEQLEN_RANGE"]
