@@ -353,13 +353,11 @@ size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, i
         .total;
 }
 
-// What a decode does beyond pa_decode: the fused append, partial outputs,
-// tokens skipped at the start of every sequence.
+// What a decode does beyond pa_decode: the fused append, partial outputs.
 struct DecodeExtra {
     const void *k_new = nullptr, *v_new = nullptr;
     const int64_t *slot_mapping = nullptr;
     float *out_m = nullptr, *out_l = nullptr, *out_o = nullptr;
-    int len_offset = 0;
 };
 
 static int decode_impl(void *out, const void *q, const void *k_cache, const void *v_cache,
@@ -417,12 +415,15 @@ static int decode_impl(void *out, const void *q, const void *k_cache, const void
     const bool seq_global = num_seqs > kSeqsInSmem;
     size_t limit = 0;
     const size_t smem = seq_global ? ks.smem_fixed : decode_smem_bytes(ks.smem_fixed, num_seqs);
-    rc = dynamic_smem_limit(ks.decode, dev, ds->smem_optin, &limit);
+    rc = dynamic_smem_limit(x.out_o && ks.decode_partial ? ks.decode_partial : ks.decode, dev,
+                            ds->smem_optin, &limit);
     if (rc != PA_OK)
         return rc;
     if (smem > limit)
         return PA_ERR_UNSUPPORTED;
-    const void *decode_fn = ks.decode;
+    const void *decode_fn = x.out_o ? ks.decode_partial : ks.decode;
+    if (!decode_fn)
+        return PA_ERR_UNSUPPORTED;
     const int warps = ks.warps;
     // Blocks per SM, looked up for the shared memory rounded up to 2 KiB
     // (within the kernel's limit): a serving loop's batch size changes every
@@ -466,7 +467,6 @@ static int decode_impl(void *out, const void *q, const void *k_cache, const void
     p.out_m = x.out_m;
     p.out_l = x.out_l;
     p.out_o = x.out_o;
-    p.len_offset = x.len_offset;
     char *ws = static_cast<char *>(workspace);
     if (wl.total > 0) {
         p.ws_m = reinterpret_cast<float *>(ws + wl.m_off);
@@ -567,31 +567,38 @@ namespace pa {
 namespace {
 
 struct SharedLayout {
-    size_t qv, tv, lv, pm, pl, po, sm, sl, so, dws, dws_bytes, total;
-    int nvb, cv, nvseq;
+    size_t qv, tv, lv, kn, vn, sl, pm, pl, po, dws, dws_bytes, total;
+    int nvb, npre, nv, vmax_blocks;
 };
 
+constexpr int kSharedCols = 16;   // query columns of a virtual sequence per kv head
+
 bool shared_layout(int num_seqs, int group_size, int prefix_len, int num_heads, int num_kv_heads,
-                   int head_dim, int max_blocks_per_seq, SharedLayout *L)
+                   int head_dim, int max_blocks_per_seq, bool append, SharedLayout *L)
 {
     if (num_seqs <= 0 || group_size <= 0 || num_seqs % group_size || prefix_len <= 0 ||
         prefix_len % kBlockSize || num_heads <= 0 || num_kv_heads <= 0 ||
-        num_heads % num_kv_heads || max_blocks_per_seq <= 0 ||
-        prefix_len / kBlockSize > max_blocks_per_seq || (head_dim != 64 && head_dim != 128))
+        num_heads % num_kv_heads || num_heads / num_kv_heads > kMaxGroup ||
+        max_blocks_per_seq <= 0 || prefix_len / kBlockSize > max_blocks_per_seq ||
+        (head_dim != 64 && head_dim != 128))
         return false;
     DeviceState *ds;
     if (device_state(&ds) != PA_OK)
         return false;
     const int G = num_heads / num_kv_heads;
     const long long cols = (long long)group_size * G;
-    L->cv = cols > 8 ? 16 : 8;
-    L->nvb = (int)((cols + L->cv - 1) / L->cv);
-    const long long nvs = (long long)(num_seqs / group_size) * L->nvb;
-    if (nvs >= (1LL << 30))
+    L->nvb = (int)((cols + kSharedCols - 1) / kSharedCols);
+    const long long npre = (long long)(num_seqs / group_size) * L->nvb;
+    if (npre + num_seqs >= (1LL << 30))
         return false;
-    L->nvseq = (int)nvs;
-    const size_t P = (size_t)(prefix_len / kBlockSize);
-    const size_t vrows = (size_t)nvs * num_kv_heads * L->cv, srows = (size_t)num_seqs * num_heads;
+    L->npre = (int)npre;
+    L->nv = (int)npre + num_seqs;
+    const int P = prefix_len / kBlockSize;
+    L->vmax_blocks = std::max(P, max_blocks_per_seq - P);
+    if (L->vmax_blocks < 1)
+        L->vmax_blocks = 1;
+    const size_t nv = (size_t)L->nv;
+    const size_t vrows = nv * num_kv_heads * kSharedCols;
     size_t at = 0;
     auto take = [&](size_t bytes) {
         const size_t off = at;
@@ -599,20 +606,17 @@ bool shared_layout(int num_seqs, int group_size, int prefix_len, int num_heads, 
         return off;
     };
     L->qv = take(vrows * head_dim * 2);
-    L->tv = take((size_t)nvs * P * sizeof(int32_t));
-    L->lv = take((size_t)nvs * sizeof(int32_t));
+    L->tv = take(nv * L->vmax_blocks * sizeof(int32_t));
+    L->lv = take(nv * sizeof(int32_t));
+    L->kn = append ? take(nv * num_kv_heads * head_dim * 2) : 0;
+    L->vn = append ? take(nv * num_kv_heads * head_dim * 2) : 0;
+    L->sl = append ? take(nv * sizeof(int64_t)) : 0;
     L->pm = take(vrows * sizeof(float));
     L->pl = take(vrows * sizeof(float));
     L->po = take(vrows * head_dim * sizeof(float));
-    L->sm = take(srows * sizeof(float));
-    L->sl = take(srows * sizeof(float));
-    L->so = take(srows * head_dim * sizeof(float));
-    const int workers = ds->num_sms * kMaxWarpsPerSM;
-    const size_t d1 = workspace_layout(kModeBalanced, (int)nvs, num_kv_heads * L->cv, num_kv_heads,
-                                       head_dim, 1, workers).total;
-    const size_t d2 = workspace_layout(kModeBalanced, num_seqs, num_heads, num_kv_heads, head_dim,
-                                       1, workers).total;
-    L->dws_bytes = std::max(d1, d2);
+    L->dws_bytes = workspace_layout(kModeBalanced, L->nv, num_kv_heads * kSharedCols,
+                                    num_kv_heads, head_dim, 1, ds->num_sms * kMaxWarpsPerSM)
+                       .total;
     L->dws = take(L->dws_bytes);
     L->total = at;
     return true;
@@ -629,7 +633,7 @@ size_t pa_decode_shared_prefix_workspace_size(int num_seqs, int group_size, int 
 {
     SharedLayout L;
     if (!shared_layout(num_seqs, group_size, prefix_len, num_heads, num_kv_heads, head_dim,
-                       max_blocks_per_seq, &L))
+                       max_blocks_per_seq, true, &L))
         return 0;
     return L.total;
 }
@@ -656,65 +660,66 @@ int pa_decode_shared_prefix(void *out, const void *q, void *k_cache, void *v_cac
         (append && (!k_new || !v_new || !slot_mapping)))
         return PA_ERR_INVALID_ARG;
     if (!aligned(out, 16) || !aligned(q, 16) || !aligned(block_tables, 4) ||
+        !aligned(seq_lens, 4) ||
         (append && (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(slot_mapping, 8))))
         return PA_ERR_INVALID_ARG;
     SharedLayout L;
     if (!shared_layout(num_seqs, group_size, prefix_len, num_heads, num_kv_heads, head_dim,
-                       max_blocks_per_seq, &L))
+                       max_blocks_per_seq, append, &L))
         return PA_ERR_INVALID_ARG;
     if (!workspace || workspace_bytes < L.total || !aligned(workspace, 256))
         return PA_ERR_WORKSPACE;
+    DeviceState *ds;
+    rc = device_state(&ds);
+    if (rc != PA_OK)
+        return rc;
     char *ws = static_cast<char *>(workspace);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const int P = prefix_len / kBlockSize;
 
     SharedParams sp{};
     sp.q = q;
     sp.block_tables = block_tables;
+    sp.seq_lens = seq_lens;
+    sp.k_new = k_new;
+    sp.v_new = v_new;
+    sp.slot_mapping = slot_mapping;
     sp.num_seqs = num_seqs;
     sp.group_size = group_size;
-    sp.prefix_tiles = P;
+    sp.prefix_tiles = prefix_len / kBlockSize;
     sp.num_heads = num_heads;
     sp.num_kv_heads = num_kv_heads;
     sp.head_dim = head_dim;
     sp.max_blocks = max_blocks_per_seq;
     sp.nvb = L.nvb;
-    sp.cv = L.cv;
+    sp.npre = L.npre;
+    sp.vmax_blocks = L.vmax_blocks;
     sp.q_v = ws + L.qv;
     sp.tables_v = reinterpret_cast<int32_t *>(ws + L.tv);
     sp.lens_v = reinterpret_cast<int32_t *>(ws + L.lv);
+    sp.k_new_v = append ? ws + L.kn : nullptr;
+    sp.v_new_v = append ? ws + L.vn : nullptr;
+    sp.slots_v = append ? reinterpret_cast<int64_t *>(ws + L.sl) : nullptr;
+    sp.err = ds->err;
     sp.pm = reinterpret_cast<float *>(ws + L.pm);
     sp.pl = reinterpret_cast<float *>(ws + L.pl);
     sp.po = reinterpret_cast<float *>(ws + L.po);
-    sp.sm = reinterpret_cast<float *>(ws + L.sm);
-    sp.sl = reinterpret_cast<float *>(ws + L.sl);
-    sp.so = reinterpret_cast<float *>(ws + L.so);
     sp.out = out;
-    rc = cuda_status(launch_shared_prep(sp, L.nvseq, st));
+    rc = cuda_status(launch_shared_prep(sp, L.nv, st));
     if (rc != PA_OK)
         return rc;
-    // the prefix, once per group: virtual sequences of cv query columns each
-    DecodeExtra x1;
-    x1.out_m = reinterpret_cast<float *>(ws + L.pm);
-    x1.out_l = reinterpret_cast<float *>(ws + L.pl);
-    x1.out_o = reinterpret_cast<float *>(ws + L.po);
-    rc = decode_impl(nullptr, ws + L.qv, k_cache, v_cache, sp.tables_v, sp.lens_v, L.nvseq,
-                     num_kv_heads * L.cv, num_kv_heads, head_dim, block_size, P, num_blocks, scale,
-                     dtype, 0, ws + L.dws, L.dws_bytes, stream, x1);
-    if (rc != PA_OK)
-        return rc;
-    // every sequence's own tokens past the prefix (and the new token)
-    DecodeExtra x2;
-    x2.k_new = k_new;
-    x2.v_new = v_new;
-    x2.slot_mapping = slot_mapping;
-    x2.out_m = reinterpret_cast<float *>(ws + L.sm);
-    x2.out_l = reinterpret_cast<float *>(ws + L.sl);
-    x2.out_o = reinterpret_cast<float *>(ws + L.so);
-    x2.len_offset = prefix_len;
-    rc = decode_impl(nullptr, q, k_cache, v_cache, block_tables + P, seq_lens, num_seqs, num_heads,
-                     num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks, scale,
-                     dtype, 0, ws + L.dws, L.dws_bytes, stream, x2);
+    // one decode over the virtual batch: the groups' prefixes (16 columns of
+    // samples x heads each) and every sequence's own tokens past the prefix
+    DecodeExtra x;
+    x.k_new = sp.k_new_v;
+    x.v_new = sp.v_new_v;
+    x.slot_mapping = sp.slots_v;
+    x.out_m = reinterpret_cast<float *>(ws + L.pm);
+    x.out_l = reinterpret_cast<float *>(ws + L.pl);
+    x.out_o = reinterpret_cast<float *>(ws + L.po);
+    rc = decode_impl(nullptr, sp.q_v, k_cache, v_cache, sp.tables_v, sp.lens_v, L.nv,
+                     num_kv_heads * kSharedCols, num_kv_heads, head_dim, block_size,
+                     L.vmax_blocks, num_blocks, scale, dtype, 0, ws + L.dws, L.dws_bytes, stream,
+                     x);
     if (rc != PA_OK)
         return rc;
     return cuda_status(launch_shared_merge(sp, dtype == PA_DTYPE_BF16, st));

@@ -131,7 +131,7 @@ __device__ __forceinline__ uint64_t l2_evict_normal_policy()
 // neighbour; only then are the neighbours' table entries looked up per tile
 // (the check costs the unshared loop a few per cent even when it never
 // fires, so the kernel holds two copies of the loop and picks one per block).
-template <typename T, int D, int NT, int W, int S, bool SHARE>
+template <typename T, int D, int NT, int W, int S, bool SHARE, bool PARTIAL>
 __device__ __forceinline__ void decode_worker(const DecodeParams &p, const CUtensorMap &tmk,
                                               const CUtensorMap &tmv, unsigned char *smem,
                                               uint64_t *bars, const int32_t *pre,
@@ -438,7 +438,7 @@ __device__ __forceinline__ void decode_worker(const DecodeParams &p, const CUten
             }
             const float inv0 = 1.f / l[j][0], inv1 = 1.f / l[j][1];
             const int h0 = 8 * j + 2 * qd, h1 = h0 + 1;
-            if (whole && p.out_o) {
+            if (PARTIAL && whole) {
                 // partial-output mode: m, l and the normalised result, fp32
                 const size_t row0 = (size_t)s * Hq + h * G + h0, row1 = row0 + 1;
 #pragma unroll
@@ -537,7 +537,7 @@ __device__ __forceinline__ void decode_worker(const DecodeParams &p, const CUten
     }
 }
 
-template <typename T, int D, int NT, int W, int S>
+template <typename T, int D, int NT, int W, int S, bool PARTIAL>
 __global__ void __launch_bounds__(W * 32)
 decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
                   const __grid_constant__ CUtensorMap tmv)
@@ -595,7 +595,7 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
     // partial-output mode an empty partial result (m = -inf, l = 0)
     for (int s = blockIdx.x; s < n; s += gridDim.x) {
         if (lens[s] == 0) {
-            if (p.out_o) {
+            if (PARTIAL) {
                 for (int e = tid; e < Hq * D; e += W * 32)
                     p.out_o[(size_t)s * Hq * D + e] = 0.f;
                 for (int e = tid; e < Hq; e += W * 32) {
@@ -611,9 +611,9 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
     }
 
     if (any_share)
-        decode_worker<T, D, NT, W, S, true>(p, tmk, tmv, smem, bars, pre, lens, share);
+        decode_worker<T, D, NT, W, S, true, PARTIAL>(p, tmk, tmv, smem, bars, pre, lens, share);
     else
-        decode_worker<T, D, NT, W, S, false>(p, tmk, tmv, smem, bars, pre, lens, share);
+        decode_worker<T, D, NT, W, S, false, PARTIAL>(p, tmk, tmv, smem, bars, pre, lens, share);
 }
 
 // ---------------------------------------------------------------------------
@@ -732,8 +732,8 @@ __global__ void __launch_bounds__(512) merge_part_kernel(const DecodeParams p)
     const int g = blockIdx.x % G, run = blockIdx.x / G;
     const int s = run / Hkv, h = run % Hkv;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    int L = __ldg(p.seq_lens + s) - p.len_offset;
-    L = max(0, min(L, p.max_blocks * kBlockSize - p.len_offset));
+    int L = __ldg(p.seq_lens + s);
+    L = max(0, min(L, p.max_blocks * kBlockSize));
     const int nt = (L + kBlockSize - 1) / kBlockSize;
     const int np = (nt + p.part_tiles - 1) / p.part_tiles;
     if (np <= 1)
@@ -816,7 +816,11 @@ inline void fill_kernel_set(KernelSet *ks)
     // kSeqsInSmem sequences (a 16-column query slot costs two warps at D=128)
     constexpr int S = 2;
     constexpr int W = D == 128 ? (NT == 1 ? 10 : 8) : 12;
-    ks->decode = reinterpret_cast<const void *>(&decode_mma_kernel<T, D, NT, W, S>);
+    ks->decode = reinterpret_cast<const void *>(&decode_mma_kernel<T, D, NT, W, S, false>);
+    // partial outputs (the shared-prefix decode's virtual batch, 16 columns)
+    ks->decode_partial =
+        NT == 2 ? reinterpret_cast<const void *>(&decode_mma_kernel<T, D, NT, W, S, NT == 2>)
+                : nullptr;
     ks->warps = W;
     ks->smem_fixed = MmaLayout<D, NT, W, S>::fixed;
     ks->prep = reinterpret_cast<const void *>(&decode_prep_kernel<kPrepThreads>);

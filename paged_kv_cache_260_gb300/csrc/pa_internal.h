@@ -52,13 +52,12 @@ struct DecodeParams {
     int min_tiles;         // least tiles given to one worker
     int workers;           // warps of the decode grid
     float scale_log2;      // scale * log2(e): scores are kept in base 2
-    int len_offset;        // tokens skipped at the start of every sequence (block_tables
-                           // already points past them); lengths count from there
 };
 
 // Kernels of one (dtype, head_dim, query columns) instantiation.
 struct KernelSet {
     const void *decode;      // one thread block per SM of `warps` independent warps
+    const void *decode_partial;  // the same writing fp32 partial results (16 columns only)
     int warps;
     size_t smem_fixed;       // dynamic shared memory excluding the per-sequence arrays
     const void *prep;        // large batches: builds the per-sequence arrays in the workspace

@@ -183,17 +183,15 @@ __device__ __forceinline__ void build_prefix(const DecodeParams &p, int32_t *pre
     const int n = p.num_seqs;
     const int per = (n + NT - 1) / NT;
     const int lo = min(n, tid * per), hi = min(n, lo + per);
-    // lengths count from len_offset (tokens skipped, their blocks excluded
-    // from the table rows the kernel sees)
-    const int maxlen = p.max_blocks * kBlockSize - p.len_offset;
+    const int maxlen = p.max_blocks * kBlockSize;
     const size_t mb = (size_t)p.max_blocks;
     int sum = 0;
     bool bad = false;
     for (int s = lo; s < hi; ++s) {
         // every load below is in bounds whatever the lengths hold
-        int L = __ldg(p.seq_lens + s) - p.len_offset;
-        const int Lp = s > 0 ? __ldg(p.seq_lens + s - 1) - p.len_offset : 0;
-        const int Ln = s + 1 < n ? __ldg(p.seq_lens + s + 1) - p.len_offset : 0;
+        int L = __ldg(p.seq_lens + s);
+        const int Lp = s > 0 ? __ldg(p.seq_lens + s - 1) : 0;
+        const int Ln = s + 1 < n ? __ldg(p.seq_lens + s + 1) : 0;
         const int b0 = __ldg(p.block_tables + s * mb);
         const int bp = s > 0 ? __ldg(p.block_tables + (s - 1) * mb) : -1;
         const int bn = s + 1 < n ? __ldg(p.block_tables + (s + 1) * mb) : -1;
