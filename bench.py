@@ -21,7 +21,9 @@ Prints ONE JSON line (rank 0):
              neighbouring steps' compute, as a serving loop runs
   roofline   one decode call (decode + merge kernels) against the measured
              HBM peak, on the bytes that must leave HBM (a block shared by
-             several sequences counts once)
+             several sequences counts once); the call's duration is the
+             timed region's average where a step is that call alone, else
+             the mean of event pairs around single calls
   cpu_baseline  the fp64 oracle's step on the host cores, sized and timed
              the same way as ``--impl reference``
   parity_vs_oracle  the timed step's output, every sequence, against the
@@ -617,10 +619,11 @@ def time_decode(st, w, args, device, big: bool, use_graph: bool):
     (an event-record node between two kernels would cut their programmatic
     dependency), CUDA events around the replays.  After the timed region one
     more replay of a second graph, with an event pair around every decode
-    call, gives the call durations the roofline uses.
+    call, gives the durations of single calls.
     Otherwise: L2 flushed (2 x L2 write) before every step; each step timed
     alone with events around it and around its decode call.
-    Returns (elapsed ms over K steps, mean call ms, timing text)."""
+    Returns (elapsed ms over K steps, mean ms of a single call between its
+    own events, timing text)."""
     import torch
     K = args.steps
     if big and use_graph:
@@ -752,6 +755,15 @@ def measure_decode(name: str, args, device, rank: int, world: int, partition=Non
                                            rotate_pools=not big)
     e2e_ms = dist_max(e2e_ms, device)
     peak, peak_src = measured_hbm_peak()
+    # The roofline's duration of one decode call: where a step is that call
+    # alone and steps run back to back, the timed region's average (the
+    # region's events over its calls); otherwise the mean of the event pairs
+    # around single calls, which also keep a call from overlapping the one
+    # before it.
+    call_isolated = call_ms
+    region_avg = big and st.pairs is None
+    if region_avg:
+        call_ms = t_max / args.steps
     achieved = unique_bytes / (call_ms * 1e-3) / 1e9
     carry = None
     if headline and big and use_graph and not args.no_l2_check:
@@ -825,6 +837,10 @@ def measure_decode(name: str, args, device, rank: int, world: int, partition=Non
                                      "counts once" if shared else
                                      "K and V of every live token and kv head"),
                      "call_ms": call_ms,
+                     "call_ms_from": ("the timed region: its CUDA events over the decode "
+                                      "calls it ran back to back" if region_avg else
+                                      "an event pair around each decode call"),
+                     "call_ms_isolated": call_isolated,
                      "traffic": ncu_traffic(name)},
         "parity_vs_oracle": parity,
         "pool_utilisation": pool_utilisation(w),
