@@ -73,7 +73,7 @@ DESCRIPTION = {
                   "copy-on-write pairs per step"),
 }
 # parallel-sampling workloads that run pa_decode_shared_prefix by default
-SHARED_DEFAULT = {"parsamp8k": True}
+SHARED_DEFAULT = {"parsamp": True, "parsamp8k": True}
 
 
 # ---------------------------------------------------------------------------
@@ -298,8 +298,9 @@ class Step:
     def _count_launches(self):
         n = int(self.pairs is not None)                 # copy_blocks
         if self.shared:
-            # gather, prefix decode + merge, suffix decode + merge, final merge
-            return n + 6 + (2 if self.w.num_seqs > 2048 else 0)
+            # prefix attention, suffix lengths, suffix decode + merge, final
+            # merge (and the decode's per-sequence arrays above 2048 sequences)
+            return n + 5 + (1 if self.w.num_seqs > 2048 else 0)
         n += 1                                          # decode (append fused in)
         if self.ps >= 0:
             n += 1                                      # merge of cut runs / partitions
@@ -823,8 +824,10 @@ def measure_decode(name: str, args, device, rank: int, world: int, partition=Non
                        f"steps cycle through {copies} copies of the pool (>= 2 x L2 in all), "
                        f"no flush in the timed region")},
         "roofline": {"bound": "hbm",
-                     "kernel": ("one pa_decode_shared_prefix call: gather, decode_mma_kernel + "
-                                "merge on the shared prefix, on the suffixes, final merge"
+                     "kernel": ("one pa_decode_shared_prefix call: prefix_attn_kernel (each "
+                                "shared prefix block read once for all of its group's query "
+                                "columns), the suffix decode (decode_mma_kernel + merge), the "
+                                "final merge"
                                 if st.shared else
                                 "decode_mma_kernel + merge kernel(s): one pa_decode / "
                                 "pa_decode_append call"),

@@ -228,12 +228,14 @@ int pa_decode_append(void *out, const void *q, void *k_cache, void *v_cache,
  * reading notes).  The result equals pa_decode (or pa_decode_append when
  * k_new, v_new and slot_mapping are given) up to rounding, but each group's
  * shared prefix is read once for the whole group instead of once per
- * sequence: the prefix is decoded as a batch of virtual sequences, each
- * holding 16 query columns (sample, head) of one group and kv head and
- * reading the group's first table; each sequence's own tokens past the
- * prefix are further virtual sequences of the same decode launch; the two
- * partial results of every (sequence, head) are combined with the
- * log-sum-exp rule of the split-K merge.
+ * sequence: every query column (sample, head) of a group and kv head
+ * attends over the prefix together with the others, the prefix's tiles
+ * read once through the group's first table (in blocks of up to 64 columns,
+ * a long prefix in key chunks); each sequence's own tokens past the prefix
+ * are decoded in one decode launch (the tables from the first block past
+ * the prefix on, lengths less prefix_len); the partial results
+ * of every (sequence, head) are combined with the log-sum-exp rule of the
+ * split-K merge.
  *
  *   group_size   sequences [g*group_size, (g+1)*group_size) form group g;
  *                num_seqs must be a multiple of it
@@ -247,11 +249,10 @@ int pa_decode_append(void *out, const void *q, void *k_cache, void *v_cache,
  *   k_new, v_new, slot_mapping  as in pa_decode_append, or all NULL
  *   workspace    at least pa_decode_shared_prefix_workspace_size(...) bytes,
  *                256-byte aligned, caller-owned, no initialisation needed
- * Other arguments as pa_decode.  Launches: a gather of the virtual batch,
- * the decode (with its merge) and the final merge, all programmatic
- * dependent launches.  A sequence shorter than prefix_len sets
- * PA_DEVERR_SEQLEN_RANGE.  The workspace size covers the append; without it
- * less is used.
+ * Other arguments as pa_decode.  Launches: the prefix attention, the suffix
+ * lengths, the suffix decode (with its merge) and the final merge, all
+ * programmatic dependent launches.  A sequence shorter than prefix_len sets
+ * PA_DEVERR_SEQLEN_RANGE.
  */
 size_t pa_decode_shared_prefix_workspace_size(int num_seqs, int group_size, int prefix_len,
                                               int num_heads, int num_kv_heads, int head_dim,

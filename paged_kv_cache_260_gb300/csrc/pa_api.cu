@@ -559,22 +559,29 @@ int pa_decode_append(void *out, const void *q, void *k_cache, void *v_cache,
 }  // extern "C"
 
 // ---------------------------------------------------------------------------
-// pa_decode_shared_prefix: the shared prefix of each group decoded once, as
-// a batch of virtual sequences of up to 16 query columns, the suffixes as a
-// second decode, both with partial outputs, then one log-sum-exp merge.
+// pa_decode_shared_prefix: each group's shared prefix attended by all of the
+// group's query columns at once (prefix_attn_kernel, every prefix tile read
+// once, in key chunks), the suffixes as one decode over the sequences' own
+// tables past the prefix, both with partial outputs, then one log-sum-exp
+// merge.
 // ---------------------------------------------------------------------------
 namespace pa {
 namespace {
 
 struct SharedLayout {
-    size_t qv, tv, lv, kn, vn, sl, pm, pl, po, dws, dws_bytes, total;
-    int nvb, npre, nv, vmax_blocks;
+    size_t lv, pm, pl, po, xm, xl, xo, dws, dws_bytes, total;
+    int cols, col_blocks, chunk_tiles, nchunks;
 };
 
-constexpr int kSharedCols = 16;   // query columns of a virtual sequence per kv head
+// Key chunks of a prefix of P tiles: enough (group, kv head, column block,
+// chunk) thread blocks for about eight per SM (three run at a time), while
+// every chunk keeps at least kMinChunkTiles tiles (each chunk adds a partial
+// per column to write and merge).
+constexpr int kMinChunkTiles = 16;
+
 
 bool shared_layout(int num_seqs, int group_size, int prefix_len, int num_heads, int num_kv_heads,
-                   int head_dim, int max_blocks_per_seq, bool append, SharedLayout *L)
+                   int head_dim, int max_blocks_per_seq, SharedLayout *L)
 {
     if (num_seqs <= 0 || group_size <= 0 || num_seqs % group_size || prefix_len <= 0 ||
         prefix_len % kBlockSize || num_heads <= 0 || num_kv_heads <= 0 ||
@@ -587,35 +594,36 @@ bool shared_layout(int num_seqs, int group_size, int prefix_len, int num_heads, 
         return false;
     const int G = num_heads / num_kv_heads;
     const long long cols = (long long)group_size * G;
-    L->nvb = (int)((cols + kSharedCols - 1) / kSharedCols);
-    const long long npre = (long long)(num_seqs / group_size) * L->nvb;
-    if (npre + num_seqs >= (1LL << 30))
+    const long long npairs = (long long)(num_seqs / group_size) * num_kv_heads;
+    if (cols >= (1LL << 20) || num_seqs >= (1 << 30))
         return false;
-    L->npre = (int)npre;
-    L->nv = (int)npre + num_seqs;
+    L->cols = (int)cols;
+    L->col_blocks = (int)((cols + kPrefixCols - 1) / kPrefixCols);
     const int P = prefix_len / kBlockSize;
-    L->vmax_blocks = std::max(P, max_blocks_per_seq - P);
-    if (L->vmax_blocks < 1)
-        L->vmax_blocks = 1;
-    const size_t nv = (size_t)L->nv;
-    const size_t vrows = nv * num_kv_heads * kSharedCols;
+    const long long units = npairs * L->col_blocks;
+    long long k = (8LL * ds->num_sms + units - 1) / units;
+    k = std::max(1LL, std::min(k, (long long)std::max(1, P / kMinChunkTiles)));
+    L->chunk_tiles = (int)((P + k - 1) / k);
+    L->nchunks = (P + L->chunk_tiles - 1) / L->chunk_tiles;
+    if (units * L->nchunks >= (1LL << 31))
+        return false;
+    const size_t rows = (size_t)num_seqs * num_heads;           // suffix partials
+    const size_t xrows = (size_t)L->nchunks * npairs * cols;    // prefix partials
     size_t at = 0;
     auto take = [&](size_t bytes) {
         const size_t off = at;
         at = round_up(at + bytes, 256);
         return off;
     };
-    L->qv = take(vrows * head_dim * 2);
-    L->tv = take(nv * L->vmax_blocks * sizeof(int32_t));
-    L->lv = take(nv * sizeof(int32_t));
-    L->kn = append ? take(nv * num_kv_heads * head_dim * 2) : 0;
-    L->vn = append ? take(nv * num_kv_heads * head_dim * 2) : 0;
-    L->sl = append ? take(nv * sizeof(int64_t)) : 0;
-    L->pm = take(vrows * sizeof(float));
-    L->pl = take(vrows * sizeof(float));
-    L->po = take(vrows * head_dim * sizeof(float));
-    L->dws_bytes = workspace_layout(kModeBalanced, L->nv, num_kv_heads * kSharedCols,
-                                    num_kv_heads, head_dim, 1, ds->num_sms * kMaxWarpsPerSM)
+    L->lv = take((size_t)num_seqs * sizeof(int32_t));
+    L->pm = take(rows * sizeof(float));
+    L->pl = take(rows * sizeof(float));
+    L->po = take(rows * head_dim * sizeof(float));
+    L->xm = take(xrows * sizeof(float));
+    L->xl = take(xrows * sizeof(float));
+    L->xo = take(xrows * head_dim * sizeof(float));
+    L->dws_bytes = workspace_layout(kModeBalanced, num_seqs, num_heads, num_kv_heads, head_dim, 1,
+                                    ds->num_sms * kMaxWarpsPerSM)
                        .total;
     L->dws = take(L->dws_bytes);
     L->total = at;
@@ -633,7 +641,7 @@ size_t pa_decode_shared_prefix_workspace_size(int num_seqs, int group_size, int 
 {
     SharedLayout L;
     if (!shared_layout(num_seqs, group_size, prefix_len, num_heads, num_kv_heads, head_dim,
-                       max_blocks_per_seq, true, &L))
+                       max_blocks_per_seq, &L))
         return 0;
     return L.total;
 }
@@ -665,7 +673,7 @@ int pa_decode_shared_prefix(void *out, const void *q, void *k_cache, void *v_cac
         return PA_ERR_INVALID_ARG;
     SharedLayout L;
     if (!shared_layout(num_seqs, group_size, prefix_len, num_heads, num_kv_heads, head_dim,
-                       max_blocks_per_seq, append, &L))
+                       max_blocks_per_seq, &L))
         return PA_ERR_INVALID_ARG;
     if (!workspace || workspace_bytes < L.total || !aligned(workspace, 256))
         return PA_ERR_WORKSPACE;
@@ -677,49 +685,73 @@ int pa_decode_shared_prefix(void *out, const void *q, void *k_cache, void *v_cac
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
     SharedParams sp{};
-    sp.q = q;
-    sp.block_tables = block_tables;
     sp.seq_lens = seq_lens;
-    sp.k_new = k_new;
-    sp.v_new = v_new;
-    sp.slot_mapping = slot_mapping;
     sp.num_seqs = num_seqs;
     sp.group_size = group_size;
     sp.prefix_tiles = prefix_len / kBlockSize;
     sp.num_heads = num_heads;
     sp.num_kv_heads = num_kv_heads;
     sp.head_dim = head_dim;
-    sp.max_blocks = max_blocks_per_seq;
-    sp.nvb = L.nvb;
-    sp.npre = L.npre;
-    sp.vmax_blocks = L.vmax_blocks;
-    sp.q_v = ws + L.qv;
-    sp.tables_v = reinterpret_cast<int32_t *>(ws + L.tv);
     sp.lens_v = reinterpret_cast<int32_t *>(ws + L.lv);
-    sp.k_new_v = append ? ws + L.kn : nullptr;
-    sp.v_new_v = append ? ws + L.vn : nullptr;
-    sp.slots_v = append ? reinterpret_cast<int64_t *>(ws + L.sl) : nullptr;
     sp.err = ds->err;
     sp.pm = reinterpret_cast<float *>(ws + L.pm);
     sp.pl = reinterpret_cast<float *>(ws + L.pl);
     sp.po = reinterpret_cast<float *>(ws + L.po);
+    sp.xm = reinterpret_cast<float *>(ws + L.xm);
+    sp.xl = reinterpret_cast<float *>(ws + L.xl);
+    sp.xo = reinterpret_cast<float *>(ws + L.xo);
+    sp.nchunks = L.nchunks;
+    sp.cols = L.cols;
     sp.out = out;
-    rc = cuda_status(launch_shared_prep(sp, L.nv, st));
+    // the prefix: every query column of a group over the group's shared
+    // blocks, each block read once
+    const long long pool_rows = (long long)num_blocks * num_kv_heads * kBlockSize;
+    if (pool_rows >= (1LL << 31))
+        return PA_ERR_UNSUPPORTED;
+    CUtensorMap tmk, tmv;
+    rc = make_pool_map(&tmk, k_cache, dtype, head_dim, pool_rows);
+    if (rc == PA_OK)
+        rc = make_pool_map(&tmv, v_cache, dtype, head_dim, pool_rows);
     if (rc != PA_OK)
         return rc;
-    // one decode over the virtual batch: the groups' prefixes (16 columns of
-    // samples x heads each) and every sequence's own tokens past the prefix
+    PrefixParams xp{};
+    xp.q = q;
+    xp.block_tables = block_tables;
+    xp.num_heads = num_heads;
+    xp.num_kv_heads = num_kv_heads;
+    xp.max_blocks = max_blocks_per_seq;
+    xp.num_blocks = num_blocks;
+    xp.group_size = group_size;
+    xp.num_groups = num_seqs / group_size;
+    xp.cols = L.cols;
+    xp.col_blocks = L.col_blocks;
+    xp.prefix_tiles = prefix_len / kBlockSize;
+    xp.chunk_tiles = L.chunk_tiles;
+    xp.nchunks = L.nchunks;
+    xp.scale_log2 = scale * 1.4426950408889634f;
+    xp.err = ds->err;
+    xp.xm = reinterpret_cast<float *>(ws + L.xm);
+    xp.xl = reinterpret_cast<float *>(ws + L.xl);
+    xp.xo = reinterpret_cast<float *>(ws + L.xo);
+    rc = cuda_status(launch_prefix_attn(xp, tmk, tmv, dtype == PA_DTYPE_BF16, head_dim, st));
+    if (rc != PA_OK)
+        return rc;
+    rc = cuda_status(launch_shared_prep(sp, st));
+    if (rc != PA_OK)
+        return rc;
+    // the suffixes: every sequence's own tokens past the prefix (and its new
+    // token), one decode with partial outputs over the sequences' tables from
+    // the first block past the prefix on (rows keep their stride)
     DecodeExtra x;
-    x.k_new = sp.k_new_v;
-    x.v_new = sp.v_new_v;
-    x.slot_mapping = sp.slots_v;
+    x.k_new = k_new;
+    x.v_new = v_new;
+    x.slot_mapping = slot_mapping;
     x.out_m = reinterpret_cast<float *>(ws + L.pm);
     x.out_l = reinterpret_cast<float *>(ws + L.pl);
     x.out_o = reinterpret_cast<float *>(ws + L.po);
-    rc = decode_impl(nullptr, sp.q_v, k_cache, v_cache, sp.tables_v, sp.lens_v, L.nv,
-                     num_kv_heads * kSharedCols, num_kv_heads, head_dim, block_size,
-                     L.vmax_blocks, num_blocks, scale, dtype, 0, ws + L.dws, L.dws_bytes, stream,
-                     x);
+    rc = decode_impl(nullptr, q, k_cache, v_cache, block_tables + sp.prefix_tiles, sp.lens_v,
+                     num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                     num_blocks, scale, dtype, 0, ws + L.dws, L.dws_bytes, stream, x);
     if (rc != PA_OK)
         return rc;
     return cuda_status(launch_shared_merge(sp, dtype == PA_DTYPE_BF16, st));

@@ -817,10 +817,8 @@ inline void fill_kernel_set(KernelSet *ks)
     constexpr int S = 2;
     constexpr int W = D == 128 ? (NT == 1 ? 10 : 8) : 12;
     ks->decode = reinterpret_cast<const void *>(&decode_mma_kernel<T, D, NT, W, S, false>);
-    // partial outputs (the shared-prefix decode's virtual batch, 16 columns)
-    ks->decode_partial =
-        NT == 2 ? reinterpret_cast<const void *>(&decode_mma_kernel<T, D, NT, W, S, NT == 2>)
-                : nullptr;
+    // partial outputs (m, l, normalised o: the shared-prefix decode's suffixes)
+    ks->decode_partial = reinterpret_cast<const void *>(&decode_mma_kernel<T, D, NT, W, S, true>);
     ks->warps = W;
     ks->smem_fixed = MmaLayout<D, NT, W, S>::fixed;
     ks->prep = reinterpret_cast<const void *>(&decode_prep_kernel<kPrepThreads>);

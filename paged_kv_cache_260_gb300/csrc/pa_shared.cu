@@ -1,23 +1,20 @@
-// pa_shared.cu -- the two helper kernels of pa_decode_shared_prefix.
+// pa_shared.cu -- the helper kernels of pa_decode_shared_prefix.
 //
 // Parallel samples of one prompt share the prompt's KV blocks by reference
 // (block sharing with copy-on-write, section 系统实现要点 of the vLLM reading
 // notes; the page-sharing row of its OS-paging table).  Decoding each sample
 // on its own streams the shared blocks once per sample.  pa_decode_shared_prefix
-// instead decodes the shared prefix once per group of samples, as "virtual
-// sequences" that each hold up to 16 query columns (sample, head) of one
-// group and kv head and read the prefix through the group's first table.
-// The samples' own suffixes are further virtual sequences of the same
-// decode launch, and each (sample, head)'s two partial results are combined
-// with the log-sum-exp rule (the same split-K merge the decode uses,
+// instead attends every query column (sample, head) of a group over the
+// shared prefix at once, reading each prefix block once (prefix_attn_kernel,
+// pa_prefix.cu), decodes the samples' own suffixes (their tables past the
+// prefix) in one decode launch, and combines each (sample, head)'s partial results with
+// the log-sum-exp rule (the same split-K merge the decode uses,
 // FlashDecoding in the ICML tutorial notes, section "内核优化").
 //
-//  * shared_prep_kernel gathers the virtual batch of one decode: the prefix
-//    sequences (query columns, the group's prefix table row) and the suffix
-//    sequences (each sample's heads, its table past the prefix, its new
-//    token).
-//  * shared_merge_kernel combines each (sample, head)'s prefix partial with
-//    its suffix partial into the output.
+//  * shared_prep_kernel writes the suffix decode's lengths (each sequence's
+//    tokens past the prefix).
+//  * shared_merge_kernel combines each (sample, head)'s prefix partials (one
+//    per key chunk) with its suffix partial into the output.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <math.h>
@@ -40,77 +37,24 @@ __device__ __forceinline__ void grid_dependents_launch_()
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-constexpr int kCols = 16;   // query columns of a virtual sequence per kv head
 
-// Block (v, kv head) fills virtual sequence v for that kv head.
-//  * v < npre, a prefix sequence of group g = v / nvb, b = v % nvb: column c'
-//    holds the group's column c = 16 b + c' (sample c / G, head c % G), zero
-//    past the group's columns; its table is the group's first table up to
-//    the prefix, its length the prefix.
-//  * v >= npre, the suffix of sequence s = v - npre: columns 0..G-1 hold its
-//    heads; its table is its own past the prefix, its length what lies past
-//    the prefix, and it carries the sequence's new token.
+// One thread per sequence: the length of its suffix, the tokens past the
+// shared prefix (the suffix decode reads the sequence's own table from the
+// first block past the prefix on).
 __global__ void __launch_bounds__(256) shared_prep_kernel(const SharedParams p)
 {
     grid_dependents_launch_();
     grid_dependency_wait_();
-    const int v = blockIdx.x, h = blockIdx.y;
-    const int G = p.num_heads / p.num_kv_heads;
-    const int vec = p.head_dim / 8;                  // 16-byte vectors per query row
-    const uint4 *q = static_cast<const uint4 *>(p.q);
-    uint4 *qv = static_cast<uint4 *>(p.q_v);
-    const bool pre = v < p.npre;
-    const int g = pre ? v / p.nvb : 0, b = pre ? v - g * p.nvb : 0, s = pre ? 0 : v - p.npre;
-    for (int i = threadIdx.x; i < kCols * vec; i += blockDim.x) {
-        const int cc = i / vec, x = i - cc * vec;
-        uint4 val = make_uint4(0u, 0u, 0u, 0u);
-        if (pre) {
-            const int c = b * kCols + cc;
-            if (c < p.group_size * G)
-                val = q[((size_t)(g * p.group_size + c / G) * p.num_heads + h * G + c % G) * vec + x];
-        } else if (cc < G) {
-            val = q[((size_t)s * p.num_heads + h * G + cc) * vec + x];
-        }
-        qv[(((size_t)v * p.num_kv_heads + h) * kCols + cc) * vec + x] = val;
-    }
-    if (!pre && p.k_new_v) {
-        const uint4 *kn = static_cast<const uint4 *>(p.k_new);
-        const uint4 *vn = static_cast<const uint4 *>(p.v_new);
-        const size_t src = ((size_t)s * p.num_kv_heads + h) * vec, dst = ((size_t)v * p.num_kv_heads + h) * vec;
-        for (int x = threadIdx.x; x < vec; x += blockDim.x) {
-            static_cast<uint4 *>(p.k_new_v)[dst + x] = kn[src + x];
-            static_cast<uint4 *>(p.v_new_v)[dst + x] = vn[src + x];
-        }
-    }
-    if (h != 0)
+    const int s = blockIdx.x * blockDim.x + threadIdx.x;
+    if (s >= p.num_seqs)
         return;
-    int32_t *row = p.tables_v + (size_t)v * p.vmax_blocks;
-    if (pre) {
-        const int32_t *src = p.block_tables + (size_t)g * p.group_size * p.max_blocks;
-        for (int t = threadIdx.x; t < p.vmax_blocks; t += blockDim.x)
-            row[t] = t < p.prefix_tiles ? src[t] : 0;
-        if (threadIdx.x == 0) {
-            p.lens_v[v] = p.prefix_tiles * 16;
-            if (p.slots_v)
-                p.slots_v[v] = -1;
-        }
-        return;
+    int L = p.seq_lens[s] - p.prefix_tiles * 16;
+    if (L < 0) {                                     // shorter than the shared prefix
+        if (p.err)
+            atomicOr(p.err, PA_DEVERR_SEQLEN_RANGE);
+        L = 0;
     }
-    const int32_t *src = p.block_tables + (size_t)s * p.max_blocks + p.prefix_tiles;
-    const int rest = p.max_blocks - p.prefix_tiles;
-    for (int t = threadIdx.x; t < p.vmax_blocks; t += blockDim.x)
-        row[t] = t < rest ? src[t] : 0;
-    if (threadIdx.x == 0) {
-        int L = p.seq_lens[s] - p.prefix_tiles * 16;
-        if (L < 0) {                                 // shorter than the shared prefix
-            if (p.err)
-                atomicOr(p.err, PA_DEVERR_SEQLEN_RANGE);
-            L = 0;
-        }
-        p.lens_v[v] = L;
-        if (p.slots_v)
-            p.slots_v[v] = p.slot_mapping[s];
-    }
+    p.lens_v[s] = L;
 }
 
 template <typename T>
@@ -123,15 +67,18 @@ __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x)
     return __float2bfloat16_rn(x);
 }
 
-// One warp per (sample, query head):
-//     M = max(m_1, m_2), w_i = l_i exp(m_i - M), out = (w_1 o_1 + w_2 o_2) / (w_1 + w_2)
-// over the prefix partial (its prefix sequence's column) and the suffix
-// partial (its suffix sequence's column).
+// One warp per (sample, query head), over its partials (m_i, l_i, o_i) --
+// the prefix's key chunks and the suffix:
+//     M = max_i m_i,  w_i = l_i exp(m_i - M),  out = sum_i w_i o_i / sum_i w_i
+// Lane i reads partial i's m and l (32 at a time), so the weights need one
+// warp reduction, and the o rows are then summed eight at a time with their
+// loads in flight together.
 template <typename T>
 __global__ void __launch_bounds__(256) shared_merge_kernel(const SharedParams p)
 {
     grid_dependents_launch_();
     grid_dependency_wait_();
+    constexpr uint32_t FULL = 0xffffffffu;
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
     const int rows = p.num_seqs * p.num_heads;
     if (warp >= rows)
@@ -140,19 +87,68 @@ __global__ void __launch_bounds__(256) shared_merge_kernel(const SharedParams p)
     const int G = p.num_heads / p.num_kv_heads;
     const int g = s / p.group_size, smp = s - g * p.group_size;
     const int h = hq / G, c = smp * G + hq % G;
-    const size_t prow = ((size_t)(g * p.nvb + c / kCols) * p.num_kv_heads + h) * kCols + c % kCols;
-    const size_t srow = ((size_t)(p.npre + s) * p.num_kv_heads + h) * kCols + hq % G;
-    const float m1 = p.pm[prow], l1 = p.pl[prow];
-    const float m2 = p.pm[srow], l2 = p.pl[srow];
-    const float M = fmaxf(m1, m2);
-    const float w1 = l1 > 0.f ? l1 * expf(m1 - M) : 0.f;
-    const float w2 = l2 > 0.f ? l2 * expf(m2 - M) : 0.f;
-    const float inv = w1 + w2 > 0.f ? 1.f / (w1 + w2) : 0.f;
+    const size_t cstride = (size_t)(p.num_seqs / p.group_size) * p.num_kv_heads * p.cols;
+    const size_t xrow = ((size_t)g * p.num_kv_heads + h) * p.cols + c;   // chunk 0
+    const size_t srow = (size_t)warp;                                     // the suffix
+    const int np = p.nchunks + 1;                    // partial np - 1 is the suffix
+    auto row_of = [&](int i) { return i < p.nchunks ? xrow + (size_t)i * cstride : srow; };
+    auto m_of = [&](int i) { return i < p.nchunks ? p.xm[row_of(i)] : p.pm[srow]; };
+    auto l_of = [&](int i) { return i < p.nchunks ? p.xl[row_of(i)] : p.pl[srow]; };
+    auto o_of = [&](int i) { return i < p.nchunks ? p.xo + row_of(i) * p.head_dim
+                                                  : p.po + srow * p.head_dim; };
+    // M over the non-empty partials
+    float M = -INFINITY;
+    for (int i = lane; i < np; i += 32) {
+        if (l_of(i) > 0.f)
+            M = fmaxf(M, m_of(i));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        M = fmaxf(M, __shfl_xor_sync(FULL, M, off));
+    constexpr int V = 4;                             // channels a lane, head_dim <= 128
+    float W = 0.f, acc[V] = {0.f, 0.f, 0.f, 0.f};
+    for (int base = 0; base < np; base += 32) {
+        const int i = base + lane;
+        float w = 0.f;
+        if (i < np) {
+            const float l = l_of(i);
+            w = l > 0.f ? l * expf(m_of(i) - M) : 0.f;   // an empty partial weighs nothing
+        }
+        const int cnt = min(32, np - base);
+        for (int k0 = 0; k0 < cnt; k0 += 8) {
+            // eight rows' loads in flight at once; every row is written by
+            // the call, and an empty one is dropped by its weight below
+            float ov[8][V];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                if (k0 + u < cnt) {
+                    const float *o = o_of(base + k0 + u);
+#pragma unroll
+                    for (int v = 0; v < V; ++v) {
+                        const int d = lane + 32 * v;
+                        ov[u][v] = d < p.head_dim ? o[d] : 0.f;
+                    }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                if (k0 + u < cnt) {
+                    const float wk = __shfl_sync(FULL, w, k0 + u);
+                    W += wk;
+#pragma unroll
+                    for (int v = 0; v < V; ++v)
+                        acc[v] += wk > 0.f ? wk * ov[u][v] : 0.f;
+                }
+            }
+        }
+    }
+    const float inv = W > 0.f ? 1.f / W : 0.f;
     T *out = static_cast<T *>(p.out) + (size_t)warp * p.head_dim;
-    for (int d = lane; d < p.head_dim; d += 32) {
-        const float o1 = w1 > 0.f ? p.po[prow * p.head_dim + d] : 0.f;
-        const float o2 = w2 > 0.f ? p.po[srow * p.head_dim + d] : 0.f;
-        out[d] = from_f<T>((w1 * o1 + w2 * o2) * inv);
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+        const int d = lane + 32 * v;
+        if (d < p.head_dim)
+            out[d] = from_f<T>(acc[v] * inv);
     }
 }
 
@@ -177,10 +173,10 @@ cudaError_t launch_pdl(const void *fn, dim3 grid, dim3 block, cudaStream_t st, c
 
 // Both are programmatic dependent launches: scheduled while the preceding
 // kernel drains, touching no global memory before it has completed.
-cudaError_t launch_shared_prep(const SharedParams &p, int num_vseqs, cudaStream_t st)
+cudaError_t launch_shared_prep(const SharedParams &p, cudaStream_t st)
 {
     return launch_pdl(reinterpret_cast<const void *>(&shared_prep_kernel),
-                      dim3(num_vseqs, p.num_kv_heads), dim3(256), st, p);
+                      dim3((p.num_seqs + 255) / 256), dim3(256), st, p);
 }
 
 cudaError_t launch_shared_merge(const SharedParams &p, bool bf16, cudaStream_t st)

@@ -2,6 +2,7 @@
 // its helper kernels (pa_shared.cu).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -11,31 +12,41 @@ namespace pa {
 struct SharedParams {
     // the batch: groups of group_size consecutive sequences share their first
     // prefix_tiles blocks
-    const void *q;                 // [num_seqs][num_heads][head_dim]
-    const int32_t *block_tables;   // [num_seqs][max_blocks]
     const int32_t *seq_lens;       // [num_seqs]
-    const void *k_new, *v_new;     // [num_seqs][num_kv_heads][head_dim], or null
-    const int64_t *slot_mapping;   // [num_seqs], or null
     int num_seqs, group_size, prefix_tiles;
-    int num_heads, num_kv_heads, head_dim, max_blocks;
-    // The virtual batch, one decode: first nvb prefix sequences per group
-    // (16 query columns (sample, head) per kv head, the group's first table
-    // up to the prefix), then one suffix sequence per sequence (its heads in
-    // the first G columns, its table past the prefix).
-    int nvb, npre;                 // prefix sequences per group, in all
-    int vmax_blocks;               // table row length of the virtual batch
-    void *q_v;                     // [nv][num_kv_heads][16][head_dim]
-    int32_t *tables_v;             // [nv][vmax_blocks]
-    int32_t *lens_v;               // [nv]
-    void *k_new_v, *v_new_v;       // [nv][num_kv_heads][head_dim] (append only)
-    int64_t *slots_v;              // [nv] (append only; -1 for prefix sequences)
+    int num_heads, num_kv_heads, head_dim;
+    int32_t *lens_v;               // [num_seqs]: tokens past the prefix (the suffix decode's lengths)
     uint32_t *err;                 // device error bits
-    // the merge: partials [nv][num_kv_heads * 16] (m, l, o normalised), fp32
+    // the merge: the suffix partials [num_seqs][num_heads] (m, l, o
+    // normalised, fp32), and the prefix partials of prefix_attn_kernel
+    // [nchunks][num_groups * num_kv_heads][cols] (m, l; o with head_dim more)
     const float *pm, *pl, *po;
+    const float *xm, *xl, *xo;
+    int nchunks, cols;             // key chunks of the prefix; group_size * G
     void *out;                     // [num_seqs][num_heads][head_dim]
 };
 
-cudaError_t launch_shared_prep(const SharedParams &p, int num_vseqs, cudaStream_t st);
+// Attention of every query column (sample, head) of a group over the
+// group's shared prefix, each prefix tile read once for all of them.
+struct PrefixParams {
+    const void *q;                 // [num_seqs][num_heads][head_dim]
+    const int32_t *block_tables;   // [num_seqs][max_blocks]; a group's first row names the prefix
+    int num_heads, num_kv_heads, max_blocks, num_blocks;
+    int group_size, num_groups;
+    int cols;                      // query columns of a (group, kv head): group_size * G
+    int col_blocks;                // blocks of kPrefixCols columns per (group, kv head)
+    int prefix_tiles, chunk_tiles, nchunks;
+    float scale_log2;
+    uint32_t *err;
+    float *xm, *xl, *xo;           // partials [nchunks][num_groups * num_kv_heads][cols]
+};
+
+constexpr int kPrefixCols = 64;    // query columns of one prefix thread block
+
+cudaError_t launch_shared_prep(const SharedParams &p, cudaStream_t st);
 cudaError_t launch_shared_merge(const SharedParams &p, bool bf16, cudaStream_t st);
+// work items: nchunks * num_groups * num_kv_heads * col_blocks thread blocks
+cudaError_t launch_prefix_attn(const PrefixParams &p, const CUtensorMap &tmk,
+                               const CUtensorMap &tmv, bool bf16, int head_dim, cudaStream_t st);
 
 }  // namespace pa

@@ -2,9 +2,10 @@
 
 Parallel samples of one prompt share the prompt's blocks (copy-on-write of
 the last, partly filled or written-to block).  The shared-prefix decode
-reads each group's shared blocks once, as virtual sequences of up to 16
-query columns, decodes every sample's own tokens separately and merges the
-two partial results.  Every case runs the whole step (copy_blocks, then the
+reads each group's shared blocks once for all of the group's query columns
+(sample x head, in blocks of up to 64, the prefix in key chunks when it is
+long), decodes every sample's own tokens separately and merges the partial
+results.  Every case runs the whole step (copy_blocks, then the
 decode with the new tokens appended) on NaN-poisoned pools and compares
 with the oracle's step within the decode tolerance; the pools must come out
 bit-identical to the oracle's.
@@ -66,6 +67,8 @@ def test_parallel_sampling_config(pa, append):
     (4, 5, 1008, 12, 4, 128, "f16"),   # 15 columns
     (2, 4, 64, 64, 4, 128, "bf16"),    # group 16 x 4 samples = 64 columns
     (2, 4, 200, 16, 4, 64, "bf16"),    # unaligned, head_dim 64
+    (1, 16, 2064, 16, 2, 128, "bf16"), # 128 columns (two column blocks), 2048 shared tokens in key chunks
+    (2, 6, 1040, 24, 8, 64, "f16"),    # 18 columns (a half-used warp), head_dim 64, two key chunks
 ])
 def test_shapes(pa, prompts, samples, prompt_len, hq, hkv, d, dtype):
     suffix = None if prompt_len % 16 == 0 else [0] * (prompts * samples)
