@@ -8,7 +8,8 @@
 // head) pair, group_size * G of them -- attend over the same K/V tiles.  A
 // thread block takes up to kPrefixCols of those columns and a chunk of the
 // prefix's tiles: one producer warp streams each tile once by TMA into a ring
-// of stages, and every consumer warp (8 columns each) multiplies the staged
+// of stages (two pool blocks, 32 keys, a stage), and every consumer warp (8
+// columns each) multiplies the staged
 // tile against its columns with the decode's tensor-core steps (mma.sync
 // m16n8k16, online softmax in base 2).  A consumer's steps on one tile form a
 // dependency chain, so the block is sized to its columns (up to 8 consumer
@@ -44,8 +45,9 @@ struct PrefixShape {
     static constexpr int NB = D / 64;                     // 64-column boxes per tile
     static constexpr int BOX = kBlockSize * 128;          // 16 rows x 128 B
     static constexpr int TILE = NB * BOX;                 // K (or V) of one tile
-    static constexpr int STAGE = 2 * TILE;
-    static constexpr int NSTG = D == 128 ? 8 : 16;        // ring depth
+    // a stage holds two tiles (32 keys): K and V of the first, then of the second
+    static constexpr int STAGE = 4 * TILE;
+    static constexpr int NSTG = D == 128 ? 4 : 8;         // ring depth
     static constexpr int KS = D / 16;                     // QK k-steps; PV m-tiles
     // +1024: the base is aligned up to the swizzle atom; then full[NSTG],
     // empty[NSTG] and the abort flag
@@ -97,6 +99,7 @@ prefix_attn_kernel(const PrefixParams p, const __grid_constant__ CUtensorMap tmk
     const int g = pair / Hkv, h = pair - g * Hkv;
     const int t0 = kc * p.chunk_tiles;
     const int n = min(p.prefix_tiles, t0 + p.chunk_tiles) - t0;   // tiles of the chunk (>= 1)
+    const int nsteps = (n + 1) / 2;                                // stages of two tiles
     const int c_lo = cb * kPrefixCols;
     const int ncols = min(kPrefixCols, p.cols - c_lo);            // columns of this block
     const int nw = (ncols + 7) / 8;                                // consumer warps at work
@@ -123,12 +126,14 @@ prefix_attn_kernel(const PrefixParams p, const __grid_constant__ CUtensorMap tmk
         auto fetch = [&](int i0) { return i0 + lane < n ? __ldg(table + i0 + lane) : 0; };
         int cur = fetch(0), nxt = fetch(32);
         int issued = 0;
-        for (int i = 0; i < n; ++i) {
-            if (i > 0 && (i & 31) == 0) {
+        for (int i = 0; i < nsteps; ++i) {
+            const int t = 2 * i;                                   // the stage's first tile
+            if (t > 0 && (t & 31) == 0) {
                 cur = nxt;
-                nxt = fetch(i + 32);
+                nxt = fetch(t + 32);
             }
-            int phys = __shfl_sync(FULL, cur, i & 31);
+            const bool two = t + 1 < n;
+            int phys[2] = {__shfl_sync(FULL, cur, t & 31), __shfl_sync(FULL, cur, (t + 1) & 31)};
             const int st = i % NS;
             bool ok = true;
             if (lane == 0)
@@ -141,17 +146,23 @@ prefix_attn_kernel(const PrefixParams p, const __grid_constant__ CUtensorMap tmk
                 break;
             }
             if (lane == 0) {
-                if ((unsigned)phys >= (unsigned)p.num_blocks) {
-                    record_error(p.err, PA_DEVERR_TABLE_RANGE);
-                    phys = 0;
-                }
-                const int row = (phys * Hkv + h) * kBlockSize;
                 const uint32_t dst = sbase + st * Sh::STAGE;
-                mbar_arrive_expect_tx(full_bar(st), (uint32_t)Sh::STAGE);
+                mbar_arrive_expect_tx(full_bar(st), (uint32_t)((two ? 4 : 2) * Sh::TILE));
 #pragma unroll
-                for (int bx = 0; bx < Sh::NB; ++bx) {
-                    tma_load_2d(dst + bx * Sh::BOX, &tmk, 64 * bx, row, full_bar(st), pol);
-                    tma_load_2d(dst + Sh::TILE + bx * Sh::BOX, &tmv, 64 * bx, row, full_bar(st), pol);
+                for (int u = 0; u < 2; ++u) {
+                    if (u == 1 && !two)
+                        break;
+                    if ((unsigned)phys[u] >= (unsigned)p.num_blocks) {
+                        record_error(p.err, PA_DEVERR_TABLE_RANGE);
+                        phys[u] = 0;
+                    }
+                    const int row = (phys[u] * Hkv + h) * kBlockSize;
+                    const uint32_t kd = dst + u * 2 * Sh::TILE;
+#pragma unroll
+                    for (int bx = 0; bx < Sh::NB; ++bx) {
+                        tma_load_2d(kd + bx * Sh::BOX, &tmk, 64 * bx, row, full_bar(st), pol);
+                        tma_load_2d(kd + Sh::TILE + bx * Sh::BOX, &tmv, 64 * bx, row, full_bar(st), pol);
+                    }
                 }
             }
             issued = i + 1;
@@ -197,8 +208,9 @@ prefix_attn_kernel(const PrefixParams p, const __grid_constant__ CUtensorMap tmk
         for (int c = 0; c < 4; ++c)
             o[mt][c] = 0.f;
 
-    for (int i = 0; i < n; ++i) {
+    for (int i = 0; i < nsteps; ++i) {
         const int st = i % NS;
+        const bool two = 2 * i + 1 < n;                           // the stage's second tile
         if (!__all_sync(FULL, !*abort_flag && mbar_wait_bounded(full_bar(st), (i / NS) & 1))) {
             if (lane == 0 && !*abort_flag) {
                 *abort_flag = 1;
@@ -206,20 +218,29 @@ prefix_attn_kernel(const PrefixParams p, const __grid_constant__ CUtensorMap tmk
             }
             return;                                   // no partial: the call has failed
         }
-        const uint32_t kst = sbase + st * Sh::STAGE, vst = kst + Sh::TILE;
-        // S = K . Q^T, two accumulators (shorter chains)
+        const uint32_t ka = sbase + st * Sh::STAGE, va = ka + Sh::TILE;
+        const uint32_t kb = va + Sh::TILE, vb = kb + Sh::TILE;
+        // S = K . Q^T for both tiles, one accumulator each (two chains)
         float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
             uint32_t a[4];
-            ldsm_x4(kst + (ks >> 2) * Sh::BOX + swz_(krow, 2 * (ks & 3) + kcs), a[0], a[1], a[2], a[3]);
-            M::run((ks & 1) ? sb : sa, a, qf[ks][0], qf[ks][1]);
+            const uint32_t off = (ks >> 2) * Sh::BOX + swz_(krow, 2 * (ks & 3) + kcs);
+            ldsm_x4(ka + off, a[0], a[1], a[2], a[3]);
+            M::run(sa, a, qf[ks][0], qf[ks][1]);
+            if (two) {
+                ldsm_x4(kb + off, a[0], a[1], a[2], a[3]);
+                M::run(sb, a, qf[ks][0], qf[ks][1]);
+            }
         }
-        const float x0 = (sa[0] + sb[0]) * p.scale_log2;   // token r,   column 2qd
-        const float x1 = (sa[1] + sb[1]) * p.scale_log2;   // token r,   column 2qd+1
-        const float x2 = (sa[2] + sb[2]) * p.scale_log2;   // token r+8, column 2qd
-        const float x3 = (sa[3] + sb[3]) * p.scale_log2;   // token r+8, column 2qd+1
-        float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+        // scores: tile a tokens r, r+8; tile b the same (-inf without it)
+        const float x0 = sa[0] * p.scale_log2, x1 = sa[1] * p.scale_log2;
+        const float x2 = sa[2] * p.scale_log2, x3 = sa[3] * p.scale_log2;
+        const float y0 = two ? sb[0] * p.scale_log2 : -INFINITY;
+        const float y1 = two ? sb[1] * p.scale_log2 : -INFINITY;
+        const float y2 = two ? sb[2] * p.scale_log2 : -INFINITY;
+        const float y3 = two ? sb[3] * p.scale_log2 : -INFINITY;
+        float mx0 = fmaxf(fmaxf(x0, x2), fmaxf(y0, y2)), mx1 = fmaxf(fmaxf(x1, x3), fmaxf(y1, y3));
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {
             mx0 = fmaxf(mx0, __shfl_xor_sync(FULL, mx0, off));
@@ -242,18 +263,27 @@ prefix_attn_kernel(const PrefixParams p, const __grid_constant__ CUtensorMap tmk
         }
         const float p0 = exp2f(x0 - m0), p1 = exp2f(x1 - m1);
         const float p2 = exp2f(x2 - m0), p3 = exp2f(x3 - m1);
-        l0 += p0 + p2;
-        l1 += p1 + p3;
+        const float q0 = exp2f(y0 - m0), q1 = exp2f(y1 - m1);
+        const float q2 = exp2f(y2 - m0), q3 = exp2f(y3 - m1);
+        l0 += (p0 + p2) + (q0 + q2);
+        l1 += (p1 + p3) + (q1 + q3);
         // P^T as the B operand: the tokens become columns
-        const uint32_t pb0 = movmatrix_trans(M::pack(p0, p1));
-        const uint32_t pb1 = movmatrix_trans(M::pack(p2, p3));
-        // O^T += V^T . P^T
+        const uint32_t pa0 = movmatrix_trans(M::pack(p0, p1));
+        const uint32_t pa1 = movmatrix_trans(M::pack(p2, p3));
+        const uint32_t pb0 = movmatrix_trans(M::pack(q0, q1));
+        const uint32_t pb1 = movmatrix_trans(M::pack(q2, q3));
+        // O^T += V^T . P^T, tile by tile (a missing second tile's stage holds
+        // stale rows: its products are skipped, not weighted by zero)
 #pragma unroll
         for (int mt = 0; mt < KS; ++mt) {
             uint32_t a[4];
-            ldsm_x4_trans(vst + (mt >> 2) * Sh::BOX + swz_(vrow, 2 * (mt & 3) + vcs), a[0], a[1],
-                          a[2], a[3]);
-            M::run(o[mt], a, pb0, pb1);
+            const uint32_t off = (mt >> 2) * Sh::BOX + swz_(vrow, 2 * (mt & 3) + vcs);
+            ldsm_x4_trans(va + off, a[0], a[1], a[2], a[3]);
+            M::run(o[mt], a, pa0, pa1);
+            if (two) {
+                ldsm_x4_trans(vb + off, a[0], a[1], a[2], a[3]);
+                M::run(o[mt], a, pb0, pb1);
+            }
         }
         // the stage is free once every lane has read it
         __syncwarp();
