@@ -155,7 +155,9 @@ def measured_hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-DECODE_SOURCES = ("pa_decode_mma.cuh", "pa_schedule.cuh", "pa_device.cuh", "pa_internal.h")
+# the decode, and the shared-prefix decode's prefix attention and helpers
+DECODE_SOURCES = ("pa_decode_mma.cuh", "pa_schedule.cuh", "pa_device.cuh", "pa_internal.h",
+                  "pa_prefix.cu", "pa_shared.cu", "pa_shared.h")
 PREFILL_SOURCES = ("pa_prefill.cuh", "pa_prefill_abi.h", "pa_tcgen05.cuh", "pa_device.cuh")
 
 
@@ -174,9 +176,10 @@ def decode_source_hash() -> str:
 
 
 def ncu_traffic(workload: str, table: str = "decode_dram_traffic.txt", names=DECODE_SOURCES):
-    """DRAM bytes per launch of the workload's dominant kernel from the
-    committed ncu summary, if it was taken on the current kernel sources
-    (else None)."""
+    """DRAM bytes per launch of the workload's dominant kernel (for the
+    shared-prefix decode, its prefix attention and its suffix decode
+    together) from the committed ncu summary, if it was taken on the current
+    kernel sources (else None)."""
     path = os.path.join(ROOT, "profiles", table)
     if not os.path.exists(path):
         return None
