@@ -358,6 +358,7 @@ struct DecodeExtra {
     const void *k_new = nullptr, *v_new = nullptr;
     const int64_t *slot_mapping = nullptr;
     float *out_m = nullptr, *out_l = nullptr, *out_o = nullptr;
+    const CUtensorMap *tmk = nullptr, *tmv = nullptr;   // the pools' maps, if already encoded
 };
 
 static int decode_impl(void *out, const void *q, const void *k_cache, const void *v_cache,
@@ -497,11 +498,16 @@ static int decode_impl(void *out, const void *q, const void *k_cache, const void
     p.scale_log2 = scale * 1.4426950408889634f;
 
     CUtensorMap tmk, tmv;
-    rc = make_pool_map(&tmk, k_cache, dtype, head_dim, pool_rows);
-    if (rc == PA_OK)
-        rc = make_pool_map(&tmv, v_cache, dtype, head_dim, pool_rows);
-    if (rc != PA_OK)
-        return rc;
+    if (x.tmk && x.tmv) {
+        tmk = *x.tmk;
+        tmv = *x.tmv;
+    } else {
+        rc = make_pool_map(&tmk, k_cache, dtype, head_dim, pool_rows);
+        if (rc == PA_OK)
+            rc = make_pool_map(&tmv, v_cache, dtype, head_dim, pool_rows);
+        if (rc != PA_OK)
+            return rc;
+    }
 
     // Every kernel here is a programmatic dependent launch: its blocks may be
     // scheduled while the preceding kernel on the stream drains, and they
@@ -685,14 +691,12 @@ int pa_decode_shared_prefix(void *out, const void *q, void *k_cache, void *v_cac
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
     SharedParams sp{};
-    sp.seq_lens = seq_lens;
     sp.num_seqs = num_seqs;
     sp.group_size = group_size;
     sp.prefix_tiles = prefix_len / kBlockSize;
     sp.num_heads = num_heads;
     sp.num_kv_heads = num_kv_heads;
     sp.head_dim = head_dim;
-    sp.lens_v = reinterpret_cast<int32_t *>(ws + L.lv);
     sp.err = ds->err;
     sp.pm = reinterpret_cast<float *>(ws + L.pm);
     sp.pl = reinterpret_cast<float *>(ws + L.pl);
@@ -733,10 +737,17 @@ int pa_decode_shared_prefix(void *out, const void *q, void *k_cache, void *v_cac
     xp.xm = reinterpret_cast<float *>(ws + L.xm);
     xp.xl = reinterpret_cast<float *>(ws + L.xl);
     xp.xo = reinterpret_cast<float *>(ws + L.xo);
-    rc = cuda_status(launch_prefix_attn(xp, tmk, tmv, dtype == PA_DTYPE_BF16, head_dim, st));
+    xp.seq_lens = seq_lens;
+    xp.lens_v = reinterpret_cast<int32_t *>(ws + L.lv);
+    xp.num_seqs = num_seqs;
+    const PrefixKernel pk = prefix_kernel(xp, dtype == PA_DTYPE_BF16, head_dim);
+    int dev = 0;
+    cudaGetDevice(&dev);
+    rc = ensure_smem(pk.fn, dev, pk.smem);
     if (rc != PA_OK)
         return rc;
-    rc = cuda_status(launch_shared_prep(sp, st));
+    void *xargs[] = {&xp, &tmk, &tmv};
+    rc = launch_dependent(pk.fn, dim3((unsigned)pk.blocks), dim3(pk.threads), pk.smem, st, xargs);
     if (rc != PA_OK)
         return rc;
     // the suffixes: every sequence's own tokens past the prefix (and its new
@@ -749,7 +760,9 @@ int pa_decode_shared_prefix(void *out, const void *q, void *k_cache, void *v_cac
     x.out_m = reinterpret_cast<float *>(ws + L.pm);
     x.out_l = reinterpret_cast<float *>(ws + L.pl);
     x.out_o = reinterpret_cast<float *>(ws + L.po);
-    rc = decode_impl(nullptr, q, k_cache, v_cache, block_tables + sp.prefix_tiles, sp.lens_v,
+    x.tmk = &tmk;
+    x.tmv = &tmv;
+    rc = decode_impl(nullptr, q, k_cache, v_cache, block_tables + sp.prefix_tiles, xp.lens_v,
                      num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
                      num_blocks, scale, dtype, 0, ws + L.dws, L.dws_bytes, stream, x);
     if (rc != PA_OK)

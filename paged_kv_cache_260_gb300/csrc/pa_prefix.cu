@@ -17,7 +17,8 @@
 // is a partial (m, l, normalised o) in the form the decode's partial output
 // uses, and the merge of pa_decode_shared_prefix folds the chunks' partials
 // with the sample's own suffix (split-K with the log-sum-exp rule, ICML
-// tutorial notes, section "内核优化").
+// tutorial notes, section "内核优化").  On the way, the kernel writes the
+// suffix decode's lengths (each sequence's tokens past the prefix).
 //
 // Prefix tiles hold 16 valid tokens each (the prefix is a whole number of
 // blocks), so no key is masked.  Every wait is bounded: one that gives up
@@ -118,6 +119,15 @@ prefix_attn_kernel(const PrefixParams p, const __grid_constant__ CUtensorMap tmk
     // kernel before this one, so no thread reads them before it completes
     grid_dependents_launch();
     grid_dependency_wait();
+    // the suffix decode's lengths: the tokens of each sequence past the prefix
+    for (int s = blockIdx.x * blockDim.x + tid; s < p.num_seqs; s += gridDim.x * blockDim.x) {
+        int L = __ldg(p.seq_lens + s) - p.prefix_tiles * kBlockSize;
+        if (L < 0) {                                 // shorter than the shared prefix
+            record_error(p.err, PA_DEVERR_SEQLEN_RANGE);
+            L = 0;
+        }
+        p.lens_v[s] = L;
+    }
 
     if (warp == pw) {
         // ---------------- producer: the chunk's tiles into the ring ----------
@@ -326,43 +336,22 @@ prefix_attn_kernel(const PrefixParams p, const __grid_constant__ CUtensorMap tmk
 
 }  // namespace
 
-namespace {
-
-template <typename T, int D>
-cudaError_t launch_t(const PrefixParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv,
-                     cudaStream_t st)
+PrefixKernel prefix_kernel(const PrefixParams &p, bool bf16, int head_dim)
 {
-    using Sh = PrefixShape<D>;
-    const void *fn = reinterpret_cast<const void *>(&prefix_attn_kernel<T, D>);
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::SMEM);
-    if (e != cudaSuccess)
-        return e;
-    cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3((unsigned)(p.nchunks * p.num_groups * p.num_kv_heads * p.col_blocks));
+    PrefixKernel k{};
+    if (head_dim == 128) {
+        k.fn = bf16 ? reinterpret_cast<const void *>(&prefix_attn_kernel<__nv_bfloat16, 128>)
+                    : reinterpret_cast<const void *>(&prefix_attn_kernel<__half, 128>);
+        k.smem = PrefixShape<128>::SMEM;
+    } else {
+        k.fn = bf16 ? reinterpret_cast<const void *>(&prefix_attn_kernel<__nv_bfloat16, 64>)
+                    : reinterpret_cast<const void *>(&prefix_attn_kernel<__half, 64>);
+        k.smem = PrefixShape<64>::SMEM;
+    }
     // consumer warps for the widest column block, and the producer
-    const int ncw = (std::min(p.cols, kPrefixCols) + 7) / 8;
-    cfg.blockDim = dim3(32 * (ncw + 1));
-    cfg.dynamicSmemBytes = Sh::SMEM;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    void *args[] = {const_cast<PrefixParams *>(&p), const_cast<CUtensorMap *>(&tmk),
-                    const_cast<CUtensorMap *>(&tmv)};
-    return cudaLaunchKernelExC(&cfg, fn, args);
-}
-
-}  // namespace
-
-cudaError_t launch_prefix_attn(const PrefixParams &p, const CUtensorMap &tmk,
-                               const CUtensorMap &tmv, bool bf16, int head_dim, cudaStream_t st)
-{
-    if (head_dim == 128)
-        return bf16 ? launch_t<__nv_bfloat16, 128>(p, tmk, tmv, st)
-                    : launch_t<__half, 128>(p, tmk, tmv, st);
-    return bf16 ? launch_t<__nv_bfloat16, 64>(p, tmk, tmv, st) : launch_t<__half, 64>(p, tmk, tmv, st);
+    k.threads = 32 * ((std::min(p.cols, kPrefixCols) + 7) / 8 + 1);
+    k.blocks = p.nchunks * p.num_groups * p.num_kv_heads * p.col_blocks;
+    return k;
 }
 
 }  // namespace pa

@@ -11,8 +11,6 @@
 // the log-sum-exp rule (the same split-K merge the decode uses,
 // FlashDecoding in the ICML tutorial notes, section "内核优化").
 //
-//  * shared_prep_kernel writes the suffix decode's lengths (each sequence's
-//    tokens past the prefix).
 //  * shared_merge_kernel combines each (sample, head)'s prefix partials (one
 //    per key chunk) with its suffix partial into the output.
 #include <cuda_bf16.h>
@@ -37,25 +35,6 @@ __device__ __forceinline__ void grid_dependents_launch_()
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-
-// One thread per sequence: the length of its suffix, the tokens past the
-// shared prefix (the suffix decode reads the sequence's own table from the
-// first block past the prefix on).
-__global__ void __launch_bounds__(256) shared_prep_kernel(const SharedParams p)
-{
-    grid_dependents_launch_();
-    grid_dependency_wait_();
-    const int s = blockIdx.x * blockDim.x + threadIdx.x;
-    if (s >= p.num_seqs)
-        return;
-    int L = p.seq_lens[s] - p.prefix_tiles * 16;
-    if (L < 0) {                                     // shorter than the shared prefix
-        if (p.err)
-            atomicOr(p.err, PA_DEVERR_SEQLEN_RANGE);
-        L = 0;
-    }
-    p.lens_v[s] = L;
-}
 
 template <typename T>
 __device__ __forceinline__ T from_f(float x);
@@ -173,12 +152,6 @@ cudaError_t launch_pdl(const void *fn, dim3 grid, dim3 block, cudaStream_t st, c
 
 // Both are programmatic dependent launches: scheduled while the preceding
 // kernel drains, touching no global memory before it has completed.
-cudaError_t launch_shared_prep(const SharedParams &p, cudaStream_t st)
-{
-    return launch_pdl(reinterpret_cast<const void *>(&shared_prep_kernel),
-                      dim3((p.num_seqs + 255) / 256), dim3(256), st, p);
-}
-
 cudaError_t launch_shared_merge(const SharedParams &p, bool bf16, cudaStream_t st)
 {
     const int rows = p.num_seqs * p.num_heads;

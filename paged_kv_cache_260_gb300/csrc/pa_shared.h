@@ -12,10 +12,8 @@ namespace pa {
 struct SharedParams {
     // the batch: groups of group_size consecutive sequences share their first
     // prefix_tiles blocks
-    const int32_t *seq_lens;       // [num_seqs]
     int num_seqs, group_size, prefix_tiles;
     int num_heads, num_kv_heads, head_dim;
-    int32_t *lens_v;               // [num_seqs]: tokens past the prefix (the suffix decode's lengths)
     uint32_t *err;                 // device error bits
     // the merge: the suffix partials [num_seqs][num_heads] (m, l, o
     // normalised, fp32), and the prefix partials of prefix_attn_kernel
@@ -39,14 +37,24 @@ struct PrefixParams {
     float scale_log2;
     uint32_t *err;
     float *xm, *xl, *xo;           // partials [nchunks][num_groups * num_kv_heads][cols]
+    // the suffix decode's lengths, written on the way: lens_v[s] =
+    // seq_lens[s] - 16 prefix_tiles (0 and PA_DEVERR_SEQLEN_RANGE if shorter)
+    const int32_t *seq_lens;
+    int32_t *lens_v;
+    int num_seqs;
 };
 
 constexpr int kPrefixCols = 64;    // query columns of one prefix thread block
 
-cudaError_t launch_shared_prep(const SharedParams &p, cudaStream_t st);
 cudaError_t launch_shared_merge(const SharedParams &p, bool bf16, cudaStream_t st);
-// work items: nchunks * num_groups * num_kv_heads * col_blocks thread blocks
-cudaError_t launch_prefix_attn(const PrefixParams &p, const CUtensorMap &tmk,
-                               const CUtensorMap &tmv, bool bf16, int head_dim, cudaStream_t st);
+// prefix_attn_kernel for the dtype and head size, launched with arguments
+// (PrefixParams, CUtensorMap K pool, CUtensorMap V pool): a grid of
+// nchunks * num_groups * num_kv_heads * col_blocks blocks
+struct PrefixKernel {
+    const void *fn;
+    size_t smem;                   // dynamic shared memory a block
+    int threads, blocks;
+};
+PrefixKernel prefix_kernel(const PrefixParams &p, bool bf16, int head_dim);
 
 }  // namespace pa
