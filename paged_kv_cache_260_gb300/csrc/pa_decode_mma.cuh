@@ -811,11 +811,15 @@ __global__ void __launch_bounds__(512) merge_part_kernel(const DecodeParams p)
 template <typename T, int D, int NT>
 inline void fill_kernel_set(KernelSet *ks)
 {
-    // one thread block per SM of W independent warps, two copy stages each:
-    // as many warps as fit in shared memory with the per-sequence arrays of
-    // kSeqsInSmem sequences (a 16-column query slot costs two warps at D=128)
+    // one thread block per SM of W independent warps, two copy stages each.
+    // At D=128 with 8 columns, 7 warps: a sweep of 6 to 10 (and 6 warps of
+    // three stages) measured 7 fastest on the batch-128 GQA, long-context
+    // and MHA decodes -- fewer bytes in flight per SM leave the SMs'
+    // shares of HBM more even.  Otherwise as many warps as fit in shared
+    // memory with the per-sequence arrays of kSeqsInSmem sequences (a
+    // 16-column query slot costs two warps at D=128).
     constexpr int S = 2;
-    constexpr int W = D == 128 ? (NT == 1 ? 10 : 8) : 12;
+    constexpr int W = D == 128 ? (NT == 1 ? 7 : 8) : 12;
     ks->decode = reinterpret_cast<const void *>(&decode_mma_kernel<T, D, NT, W, S, false>);
     // partial outputs (m, l, normalised o: the shared-prefix decode's suffixes)
     ks->decode_partial = reinterpret_cast<const void *>(&decode_mma_kernel<T, D, NT, W, S, true>);
