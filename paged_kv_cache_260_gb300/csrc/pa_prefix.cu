@@ -5,20 +5,21 @@
 // tables (block sharing, section 系统实现要点 of the vLLM reading notes; the
 // page-sharing row of its OS-paging table).  For the prefix they share, the
 // query columns of a group and kv head -- every (sample, query head of the kv
-// head) pair, group_size * G of them -- attend over the same K/V tiles.  A
-// thread block takes up to kPrefixCols of those columns and a chunk of the
-// prefix's tiles: one producer warp streams each tile once by TMA into a ring
-// of stages (two pool blocks, 32 keys, a stage), and every consumer warp (8
-// columns each) multiplies the staged
-// tile against its columns with the decode's tensor-core steps (mma.sync
-// m16n8k16, online softmax in base 2).  A consumer's steps on one tile form a
-// dependency chain, so the block is sized to its columns (up to 8 consumer
-// warps) and kept small in registers, and several blocks share an SM.  Each column's result over the chunk
-// is a partial (m, l, normalised o) in the form the decode's partial output
-// uses, and the merge of pa_decode_shared_prefix folds the chunks' partials
-// with the sample's own suffix (split-K with the log-sum-exp rule, ICML
-// tutorial notes, section "内核优化").  On the way, the kernel writes the
-// suffix decode's lengths (each sequence's tokens past the prefix).
+// head) pair, group_size * G of them -- attend over the same K/V tiles.
+//
+// A thread block takes up to kPrefixCols of those columns and a chunk of the
+// prefix's tiles.  One producer warp streams each tile once by TMA into a
+// ring of stages (two pool blocks, 32 keys, a stage), and every consumer warp
+// (8 columns each) multiplies the staged tiles against its columns with the
+// decode's tensor-core steps (mma.sync m16n8k16, online softmax in base 2).
+// A consumer's steps on one stage form a dependency chain, so the block is
+// sized to its columns (up to 8 consumer warps) and kept small in registers,
+// and several blocks share an SM.  Each column's result over the chunk is a
+// partial (m, l, normalised o) in the form the decode's partial output uses,
+// and the merge of pa_decode_shared_prefix folds the chunks' partials with
+// the sample's own suffix (split-K with the log-sum-exp rule, ICML tutorial
+// notes, section "内核优化").  On the way, the kernel writes the suffix
+// decode's lengths (each sequence's tokens past the prefix).
 //
 // Prefix tiles hold 16 valid tokens each (the prefix is a whole number of
 // blocks), so no key is masked.  Every wait is bounded: one that gives up

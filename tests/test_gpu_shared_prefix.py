@@ -122,3 +122,35 @@ def test_sequence_shorter_than_prefix_is_flagged(pa):
     dw.lens[1] = 20
     pa.decode_shared_prefix(dw.out, dw.q, dw.k, dw.v, dw.tables, dw.lens, 4, 48, w.scale)
     assert pa.get_device_error() & pa.DEVERR["SEQLEN_RANGE"]
+
+
+def test_bad_prefix_table_entry_is_reported(pa):
+    # a prefix entry past the pool: the prefix kernel reads a valid block in
+    # its place and records the table error
+    w = synth.parsamp(num_prompts=2, samples=4, prompt_len=512, max_suffix=10, seed=13)
+    dw = DevWorkload(w)
+    dw.tables[0, 3] = w.k_cache.shape[0] + 5          # group 0's first table names the prefix
+    pa.get_device_error()
+    pa.decode_shared_prefix(dw.out, dw.q, dw.k, dw.v, dw.tables, dw.lens, 4, 496, w.scale)
+    torch.cuda.synchronize()
+    assert pa.get_device_error() & pa.DEVERR["TABLE_RANGE"]
+
+
+def test_repeated_calls_give_the_same_bits(pa):
+    # the prefix chunks, the suffix split and the merge order are fixed by
+    # the shapes alone, so a repeated call reproduces the output bit for bit
+    w = synth.parsamp(num_prompts=4, samples=8, prompt_len=2048, max_suffix=100, seed=17)
+    dw = DevWorkload(w)
+    pa.copy_blocks(dw.k, dw.v, dw.pairs)
+    pa.reshape_and_cache(dw.k_new, dw.v_new, dw.k, dw.v, dw.slots)
+    outs = []
+    for _ in range(2):
+        out = torch.full_like(dw.q, float("nan"))
+        pa.decode_shared_prefix(out, dw.q, dw.k, dw.v, dw.tables, dw.lens, 8,
+                                shared_prefix_len(w), w.scale)
+        torch.cuda.synchronize()
+        outs.append(out)
+    assert pa.get_device_error() == 0
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    ref, _, _ = oracle.step(w)
+    assert max_err(outs[1], ref) <= TOL[w.dtype]
