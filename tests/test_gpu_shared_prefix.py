@@ -46,7 +46,7 @@ def run(pa, w, append=True, prefix_len=None, group=None):
 @pytest.mark.parametrize("append", [True, False])
 def test_parallel_sampling_config(pa, append):
     # 16 prompts x 8 samples, 40/8 heads (40 query columns per group and kv
-    # head: three virtual sequences), 1024-token prompt: 1008 shared tokens
+    # head: five 8-column warps), 1024-token prompt: 1008 shared tokens
     w = synth.parsamp(poison=True)
     dw, out = run(pa, w, append)
     assert pa.get_device_error() == 0
@@ -61,7 +61,7 @@ def test_parallel_sampling_config(pa, append):
 # oracle): such prompts take no suffix here; block-aligned prompts do.
 @pytest.mark.parametrize("prompts,samples,prompt_len,hq,hkv,d,dtype", [
     (2, 8, 40, 8, 2, 128, "f16"),      # unaligned prompt: 32 shared tokens, new token in the copy
-    (3, 2, 304, 32, 8, 128, "bf16"),   # 8 columns: one 8-column virtual sequence
+    (3, 2, 304, 32, 8, 128, "bf16"),   # 8 columns: one consumer warp
     (2, 3, 512, 16, 1, 64, "f16"),     # 48 columns, group 16, head_dim 64
     (1, 16, 128, 8, 8, 64, "bf16"),    # MHA, 16 samples: 16 columns
     (4, 5, 1008, 12, 4, 128, "f16"),   # 15 columns
