@@ -183,8 +183,29 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
 // The pool seen as a 2-D array [num_blocks * num_kv_heads * 16 rows][head_dim]
 // of 16-bit elements, read in boxes of 16 rows x 64 columns (128 bytes) with
 // the 128-byte swizzle.  One box row is one token's 64 channels.
+// The pool maps of recent calls: a map is fixed by the pool's address, element
+// type, head size and row count, so a serving loop that calls every step on
+// the same pools encodes each map once.
+struct PoolMapEntry {
+    const void *pool;
+    int dtype, head_dim;
+    long long rows;
+    CUtensorMap map;
+};
+constexpr int kPoolMaps = 8;
+PoolMapEntry g_pool_maps[kPoolMaps];
+int g_pool_map_count = 0, g_pool_map_next = 0;
+
 int make_pool_map(CUtensorMap *tm, const void *pool, int dtype, int head_dim, long long rows)
 {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    for (int i = 0; i < g_pool_map_count; ++i) {
+        const PoolMapEntry &e = g_pool_maps[i];
+        if (e.pool == pool && e.dtype == dtype && e.head_dim == head_dim && e.rows == rows) {
+            *tm = e.map;
+            return PA_OK;
+        }
+    }
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc)
         return PA_ERR_CUDA;
@@ -198,7 +219,14 @@ int make_pool_map(CUtensorMap *tm, const void *pool, int dtype, int head_dim, lo
                            2, const_cast<void *>(pool), gdim, gstride, box, estride,
                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+    if (r != CUDA_SUCCESS)
+        return PA_ERR_CUDA;
+    PoolMapEntry &e = g_pool_maps[g_pool_map_next];
+    e = PoolMapEntry{pool, dtype, head_dim, rows, *tm};
+    g_pool_map_next = (g_pool_map_next + 1) % kPoolMaps;
+    if (g_pool_map_count < kPoolMaps)
+        ++g_pool_map_count;
+    return PA_OK;
 }
 
 int launch_dependent(const void *func, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
