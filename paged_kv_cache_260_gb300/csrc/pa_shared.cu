@@ -18,33 +18,12 @@
 #include <math.h>
 #include <stdint.h>
 
+#include "pa_device.cuh"
 #include "pa_shared.h"
 #include "pagedattn.h"
 
 namespace pa {
 namespace {
-
-// Programmatic dependent launch: wait for the preceding grid, let the next
-// be scheduled early.
-__device__ __forceinline__ void grid_dependency_wait_()
-{
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-__device__ __forceinline__ void grid_dependents_launch_()
-{
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
-
-template <typename T>
-__device__ __forceinline__ T from_f(float x);
-template <>
-__device__ __forceinline__ __half from_f<__half>(float x) { return __float2half_rn(x); }
-template <>
-__device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x)
-{
-    return __float2bfloat16_rn(x);
-}
 
 // One warp per (sample, query head), over its partials (m_i, l_i, o_i) --
 // the prefix's key chunks and the suffix:
@@ -55,8 +34,8 @@ __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x)
 template <typename T>
 __global__ void __launch_bounds__(256) shared_merge_kernel(const SharedParams p)
 {
-    grid_dependents_launch_();
-    grid_dependency_wait_();
+    grid_dependents_launch();
+    grid_dependency_wait();
     constexpr uint32_t FULL = 0xffffffffu;
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
     const int rows = p.num_seqs * p.num_heads;
@@ -127,7 +106,7 @@ __global__ void __launch_bounds__(256) shared_merge_kernel(const SharedParams p)
     for (int v = 0; v < V; ++v) {
         const int d = lane + 32 * v;
         if (d < p.head_dim)
-            out[d] = from_f<T>(acc[v] * inv);
+            out[d] = Elem<T>::from_f(acc[v] * inv);
     }
 }
 
