@@ -769,6 +769,13 @@ def measure_decode(name: str, args, device, rank: int, world: int, partition=Non
     if region_avg:
         call_ms = t_max / args.steps
     achieved = unique_bytes / (call_ms * 1e-3) / 1e9
+    # the other bytes a call must move, beside the K/V: q and the output,
+    # the tables and lengths read, and the new tokens read and written
+    el = 2
+    io_bytes = (2 * w.num_seqs * w.num_heads * w.head_dim * el
+                + w.block_tables.size * 4 + w.num_seqs * 4
+                + (4 * w.num_seqs * w.num_kv_heads * w.head_dim * el
+                   if w.slot_mapping is not None else 0))
     carry = None
     if headline and big and use_graph and not args.no_l2_check:
         alt_ms, alt_steps = l2_carryover(w, st, args, device)
@@ -847,6 +854,11 @@ def measure_decode(name: str, args, device, rank: int, world: int, partition=Non
                                       "calls it ran back to back" if region_avg else
                                       "an event pair around each decode call"),
                      "call_ms_isolated": call_isolated,
+                     "io_bytes_per_launch": io_bytes,
+                     "io_basis": ("q and the output, the tables and lengths, the new "
+                                  "tokens read and written: bytes the call must move "
+                                  "beside the K/V, left out of achieved"),
+                     "all_bytes_gbps": (unique_bytes + io_bytes) / (call_ms * 1e-3) / 1e9,
                      "traffic": ncu_traffic(name)},
         "parity_vs_oracle": parity,
         "pool_utilisation": pool_utilisation(w),
