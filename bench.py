@@ -998,6 +998,204 @@ def run_swap(args):
     }), flush=True)
 
 
+CACHE_METRIC = "KV-cache maintenance kernels: HBM GB/s moved (bytes read + written)"
+CACHE_SOURCES = ("pa_cache.cu", "pa_cache.h", "pa_device.cuh")
+CACHE_CASES = {
+    "copy_cow": "copy_blocks, the parallel-sampling step's 112 copy-on-write pairs from 16 "
+                "source blocks (K and V of 8 kv heads, 64 KB a pair), L2 flushed before every "
+                "launch",
+    "copy_bulk": "copy_blocks, 4096 pairs of random distinct blocks of an 8192-block pool "
+                 "(8 kv heads, head_dim 128, bf16), back to back",
+    "reshape_step": "reshape_and_cache, the GQA batch-128 step's 128 new tokens (8 kv heads, "
+                    "head_dim 128, bf16), L2 flushed before every launch",
+    "reshape_blocks": "reshape_and_cache, a prefill's 65536 tokens filling 4096 whole blocks "
+                      "at random distinct ids of the same 8192-block pool, back to back",
+    "reshape_scatter": "reshape_and_cache, 65536 tokens into random distinct slots of the same "
+                       "8192-block pool (the decode's pattern at prefill size), back to back",
+}
+
+
+def run_cache(args):
+    """The two kernels that maintain the pool, timed alone: copy_blocks (the
+    copy-on-write of whole blocks) and reshape_and_cache (each new token's K/V
+    into its slot), at a config step's size and at a size large enough to be
+    bound by HBM.  GB/s counts the bytes read and written.  The step-size
+    pools are compared bit for bit with the oracle's; the bulk copies with
+    their sources."""
+    import torch
+    from paged_kv_cache_260_gb300 import _build
+    _build.build()
+    import paged_kv_cache_260_gb300 as pa
+    pa.load()
+    device = torch.device("cuda:0")
+    torch.cuda.set_device(device)
+    peak, peak_src = measured_hbm_peak()
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=device)
+    rng = np.random.default_rng(1010)
+    steps = max(1, min(args.steps, 100))
+    only = args.cache_case
+
+    def timed(fn, big):
+        g = capture([fn], device)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for _ in range(args.warmup):
+            g.replay()
+        torch.cuda.synchronize(device)
+        if big:                            # back to back, events around the replays
+            e0.record()
+            for _ in range(steps):
+                g.replay()
+            e1.record()
+            torch.cuda.synchronize(device)
+            return e0.elapsed_time(e1) / steps, "back to back (one-launch graph replays)"
+        total = 0.0                        # each launch alone after an L2 flush
+        for _ in range(steps):
+            flush.zero_()
+            e0.record()
+            g.replay()
+            e1.record()
+            torch.cuda.synchronize(device)
+            total += e0.elapsed_time(e1)
+        return total / steps, "L2 flushed before each launch, events around a one-launch graph replay"
+
+    def bits(t):
+        return t.view(torch.int16)
+
+    def host_bits(t):
+        return bits(t).cpu().numpy().view(np.uint16).copy()
+
+    def record(name, ms, timing, moved, exact):
+        gbs = moved / (ms * 1e-3) / 1e9
+        cases[name] = {"description": CACHE_CASES[name], "us_per_launch": ms * 1e3,
+                       "bytes_per_launch": moved, "gbps": gbs, "frac": gbs / peak,
+                       "bit_exact": exact, "timing": timing,
+                       "traffic": ncu_traffic(name, "cache_dram_traffic.txt", CACHE_SOURCES)}
+
+    cases = {}
+    import oracle
+    if only in (None, "copy_cow"):
+        w = make_workload("parsamp")
+        st = Step(w, device, 0, shared=False)
+        pairs = st.pairs
+        kh, vh = host_bits(st.k), host_bits(st.v)
+        oracle.copy_blocks(kh, vh, pairs.cpu().numpy())
+        pa.copy_blocks(st.k, st.v, pairs)
+        torch.cuda.synchronize(device)
+        exact = bool(np.array_equal(host_bits(st.k), kh) and np.array_equal(host_bits(st.v), vh))
+        ms, timing = timed(lambda: pa.copy_blocks(st.k, st.v, pairs), big=False)
+        # each distinct source block is read once (the samples of a group
+        # copy the same partly filled block), every destination written
+        nsrc = len(np.unique(pairs[:, 0].cpu().numpy()))
+        moved = 2 * (nsrc + pairs.shape[0]) * st.k[0].numel() * st.k.element_size()
+        record("copy_cow", ms, timing, moved, exact)
+        del st
+    nb, hkv, d = 8192, 8, 128
+    kp = vp = None
+    if only in (None, "copy_bulk", "reshape_blocks", "reshape_scatter"):
+        kp = torch.randint(-32768, 32767, (nb, hkv, 16, d), dtype=torch.int16, device=device)
+        vp = torch.randint(-32768, 32767, (nb, hkv, 16, d), dtype=torch.int16, device=device)
+        kp = kp.view(torch.bfloat16)
+        vp = vp.view(torch.bfloat16)
+    if only in (None, "copy_bulk"):
+        perm = rng.permutation(nb)
+        src, dst = perm[:nb // 2], perm[nb // 2:]
+        pairs = torch.from_numpy(np.stack([src, dst], 1).astype(np.int64)).to(device)
+        pa.copy_blocks(kp, vp, pairs)
+        torch.cuda.synchronize(device)
+        s_t, d_t = torch.from_numpy(src).to(device), torch.from_numpy(dst).to(device)
+        exact = bool(torch.equal(bits(kp)[d_t], bits(kp)[s_t]) and
+                     torch.equal(bits(vp)[d_t], bits(vp)[s_t]))
+        ms, timing = timed(lambda: pa.copy_blocks(kp, vp, pairs), big=True)
+        moved = 2 * 2 * len(src) * kp[0].numel() * kp.element_size()
+        record("copy_bulk", ms, timing, moved, exact)
+    if only in (None, "reshape_step"):
+        w = make_workload("gqa8b")
+        st = Step(w, device, 0)
+        kh, vh = host_bits(st.k), host_bits(st.v)
+        oracle.reshape_and_cache(kh, vh, host_bits(st.k_new), host_bits(st.v_new),
+                                 st.slots.cpu().numpy())
+        pa.reshape_and_cache(st.k_new, st.v_new, st.k, st.v, st.slots)
+        torch.cuda.synchronize(device)
+        exact = bool(np.array_equal(host_bits(st.k), kh) and np.array_equal(host_bits(st.v), vh))
+        ms, timing = timed(lambda: pa.reshape_and_cache(st.k_new, st.v_new, st.k, st.v, st.slots),
+                           big=False)
+        moved = 2 * 2 * st.k_new.numel() * st.k_new.element_size()
+        record("reshape_step", ms, timing, moved, exact)
+        del st
+    for name in ("reshape_blocks", "reshape_scatter"):
+        if only not in (None, name):
+            continue
+        ntok = 65536
+        if name == "reshape_blocks":
+            blocks = rng.choice(nb, ntok // 16, replace=False).astype(np.int64)
+            slots_np = (blocks[:, None] * 16 + np.arange(16)[None, :]).reshape(-1)
+        else:
+            slots_np = rng.choice(nb * 16, ntok, replace=False).astype(np.int64)
+        slots = torch.from_numpy(slots_np).to(device)
+        kn = torch.randint(-32768, 32767, (ntok, hkv, d), dtype=torch.int16,
+                           device=device).view(torch.bfloat16)
+        vn = torch.randint(-32768, 32767, (ntok, hkv, d), dtype=torch.int16,
+                           device=device).view(torch.bfloat16)
+        pa.reshape_and_cache(kn, vn, kp, vp, slots)
+        torch.cuda.synchronize(device)
+        blk, off = slots // 16, slots % 16
+        exact = bool(torch.equal(bits(kp)[blk, :, off, :], bits(kn)) and
+                     torch.equal(bits(vp)[blk, :, off, :], bits(vn)))
+        ms, timing = timed(lambda: pa.reshape_and_cache(kn, vn, kp, vp, slots), big=True)
+        moved = 2 * 2 * kn.numel() * kn.element_size()
+        record(name, ms, timing, moved, exact)
+    assert pa.get_device_error() == 0
+    head = "copy_bulk" if "copy_bulk" in cases else next(iter(cases))
+    c = cases[head]
+    print(json.dumps({
+        "metric": CACHE_METRIC, "value": c["gbps"], "unit": "GB/s", "n_gpus": 1,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": c["us_per_launch"] * 1e-3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": CACHE_CASES[head], "case": head},
+        "roofline": {"bound": "hbm", "achieved": c["gbps"], "peak": peak, "unit": "GB/s",
+                     "frac": c["frac"],
+                     "peak_source": (peak_src + " (MEASURED_PEAKS.json hbm_gbs, copy burst)"
+                                     if peak_src == "measured" else "fallback 6.8 TB/s"),
+                     "bytes_basis": "bytes read + written per launch",
+                     "traffic": c["traffic"]},
+        "cases": cases,
+        "parity_vs_oracle": {"bit_exact": all(x["bit_exact"] for x in cases.values())},
+        "gpu_launches": steps * len(cases),
+    }), flush=True)
+
+
+def run_reference_cache(args):
+    """The oracle's copy_blocks on the bulk case, on the host: the same
+    4096 pairs of an 8192-block pool, bytes read + written over time."""
+    import oracle
+    nb, hkv, d = 8192, 8, 128
+    rng = np.random.default_rng(1010)
+    k = rng.integers(0, 65536, (nb, hkv, 16, d), dtype=np.uint16)
+    v = rng.integers(0, 65536, (nb, hkv, 16, d), dtype=np.uint16)
+    perm = rng.permutation(nb)
+    pairs = np.stack([perm[:nb // 2], perm[nb // 2:]], 1).astype(np.int64)
+    moved = 2 * 2 * (nb // 2) * hkv * 16 * d * 2
+    steps = max(1, min(args.steps, 20))
+    for _ in range(min(args.warmup, 2)):
+        oracle.copy_blocks(k, v, pairs)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        oracle.copy_blocks(k, v, pairs)
+    dt = (time.perf_counter() - t0) / steps
+    value = moved / dt / 1e9
+    print(json.dumps({
+        "impl": "reference", "metric": CACHE_METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": 1, "steps": steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u16",
+        "data": "synthetic", "config": {"workload": CACHE_CASES["copy_bulk"], "case": "copy_bulk"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": "the oracle's copy_blocks, one host thread, the whole case"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
 PREFILL_METRIC = ("paged chunked prefill: causal attention TFLOP/s on tcgen05 tensor cores, "
                   "% of GB300 dense bf16 peak")
 PREFILL_DESCRIPTION = {
@@ -1276,7 +1474,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=list(DESCRIPTION) + ["swap", "prefill", "prefill_long"],
+    ap.add_argument("--workload", choices=list(DESCRIPTION) + ["swap", "cache", "prefill",
+                                                              "prefill_long"],
                     default=None,
                     help="one workload alone (default: the GQA batch-128 headline, with the "
                          "other decode workloads nested in the same line)")
@@ -1292,6 +1491,8 @@ def main(argv=None):
                     help="parallel sampling: pa_decode_shared_prefix (on) or pa_decode_append "
                          "(off); auto: on for the long-prompt workload")
     ap.add_argument("--only-headline", action="store_true")
+    ap.add_argument("--cache-case", choices=list(CACHE_CASES), default=None,
+                    help="--workload cache: one case alone (for a profiler)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
@@ -1301,10 +1502,14 @@ def main(argv=None):
         elif args.workload == "swap":
             print(json.dumps({"impl": "reference", "unavailable": "swap_blocks moves bytes "
                               "between memories; the oracle has no timed counterpart"}))
+        elif args.workload == "cache":
+            run_reference_cache(args)
         else:
             run_reference(args)
     elif args.workload == "swap":
         run_swap(args)
+    elif args.workload == "cache":
+        run_cache(args)
     elif args.workload and args.workload.startswith("prefill"):
         run_prefill(args)
     else:

@@ -8,40 +8,59 @@ namespace pa {
 
 // ---------------------------------------------------------------------------
 // reshape_and_cache: token i's K/V rows (all kv heads) -> pool slot
-// slot_mapping[i].  One thread per 16-byte vector: consecutive threads write
-// consecutive vectors of one (token, kv head) row, so stores are coalesced.
+// slot_mapping[i].  The input is read as one flat run of 16-byte vectors (K of
+// every token, then V); a row of head_dim * 2 bytes is 2^row_shift vectors.
+// A block takes U * blockDim.x consecutive vectors at a time, each thread U of
+// them blockDim.x apart: every load instruction of a warp is coalesced, and a
+// thread has its U loads in flight before its stores.  (Striding a thread's
+// vectors across the whole grid instead spreads a warp over U distant regions
+// and ran 11 % slower on a bulk write.)
 // ---------------------------------------------------------------------------
+template <int U>
 __global__ void __launch_bounds__(256)
 reshape_and_cache_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new,
                          uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
                          const int64_t *__restrict__ slot_mapping, int num_tokens,
-                         int num_kv_heads, int row_vecs, long long num_slots, uint32_t *err)
+                         int num_kv_heads, int row_shift, long long num_slots, uint32_t *err)
 {
     grid_dependents_launch();   // a dependent decode may be scheduled now; it waits for us
-    const long long per_token = (long long)num_kv_heads * row_vecs;   // vectors of K per token
-    const long long total = 2LL * num_tokens * per_token;            // K and V
-    for (long long x = blockIdx.x * (long long)blockDim.x + threadIdx.x; x < total;
-         x += (long long)gridDim.x * blockDim.x) {
-        const bool is_v = x >= (long long)num_tokens * per_token;
-        const long long y = is_v ? x - (long long)num_tokens * per_token : x;
-        const int i = (int)(y / per_token);
-        const long long r = y % per_token;          // = kv_head * row_vecs + vec
-        const int kvh = (int)(r / row_vecs);
-        const int vec = (int)(r % row_vecs);
-        const int64_t slot = __ldg(slot_mapping + i);
-        if (slot < 0)
-            continue;                               // padding token
-        if (slot >= num_slots) {
-            if (vec == 0 && kvh == 0 && !is_v)
-                record_error(err, PA_DEVERR_SLOT_RANGE);
-            continue;
+    using idx = unsigned long long;                 // unsigned: the divisions stay cheap
+    const idx half = ((idx)num_tokens * (idx)num_kv_heads) << row_shift;  // vectors of K
+    const idx total = 2 * half;
+    const idx vmask = ((idx)1 << row_shift) - 1;
+    const idx heads = (idx)num_kv_heads;
+    const idx step = (idx)gridDim.x * blockDim.x * U;
+    for (idx base = (idx)blockIdx.x * blockDim.x * U + threadIdx.x; base < total; base += step) {
+        uint4 t[U];
+        uint4 *to[U];                                     // null: nothing to store
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const idx x = base + (idx)u * blockDim.x;
+            to[u] = nullptr;
+            if (x >= total)
+                continue;
+            const bool is_v = x >= half;
+            const idx y = is_v ? x - half : x;            // vector within K (or V)
+            const idx row = y >> row_shift;
+            const idx i = row / heads;                    // token
+            const idx kvh = row - i * heads;
+            const int64_t slot = __ldg(slot_mapping + i);
+            t[u] = __ldg((is_v ? v_new : k_new) + y);
+            if (slot < 0)
+                continue;                                 // padding token
+            if (slot >= num_slots) {
+                if ((y & vmask) == 0 && kvh == 0 && !is_v)
+                    record_error(err, PA_DEVERR_SLOT_RANGE);
+                continue;
+            }
+            const idx blk = (idx)slot / kBlockSize, off = (idx)slot % kBlockSize;
+            const idx dst = (((blk * heads + kvh) * kBlockSize + off) << row_shift) + (y & vmask);
+            to[u] = (is_v ? v_cache : k_cache) + dst;
         }
-        const long long blk = slot / kBlockSize, off = slot % kBlockSize;
-        const long long dst = ((blk * num_kv_heads + kvh) * kBlockSize + off) * row_vecs + vec;
-        if (is_v)
-            v_cache[dst] = __ldg(v_new + y);
-        else
-            k_cache[dst] = __ldg(k_new + y);
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (to[u])
+                *to[u] = t[u];
     }
 }
 
@@ -179,6 +198,15 @@ __global__ void bounded_wait_selftest_kernel(uint64_t limit_ns, uint32_t *err)
 // ---------------------------------------------------------------------------
 // launchers
 // ---------------------------------------------------------------------------
+template <typename F>
+static int resident_blocks(F *fn, int threads)
+{
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, threads, 0) != cudaSuccess || n < 1)
+        n = 1;
+    return n;
+}
+
 static int grid_for(long long work, int threads, int num_sms)
 {
     long long g = (work + threads - 1) / threads;
@@ -193,12 +221,26 @@ cudaError_t launch_reshape_and_cache(const void *k_new, const void *v_new, void 
                                      int num_kv_heads, int head_dim, int num_blocks,
                                      uint32_t *err, int num_sms, cudaStream_t stream)
 {
-    const int row_vecs = head_dim * 2 / 16;
-    const long long total = 2LL * num_tokens * num_kv_heads * row_vecs;
-    reshape_and_cache_kernel<<<grid_for(total, 256, num_sms), 256, 0, stream>>>(
-        static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new),
-        static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), slot_mapping, num_tokens,
-        num_kv_heads, row_vecs, (long long)num_blocks * kBlockSize, err);
+    const int row_shift = head_dim == 64 ? 3 : 4;           // 16-byte vectors per row, log2
+    const long long total = (2LL * num_tokens * num_kv_heads) << row_shift;
+    // one wave of resident blocks at most, looping; four vectors a thread
+    // when that still gives every SM a block, else one (a decode step's few
+    // tokens spread over more blocks)
+    const long long slots = (long long)num_blocks * kBlockSize;
+    const long long need4 = (total + 1023) / 1024, need1 = (total + 255) / 256;
+    if (need4 >= num_sms) {
+        static const int resident = resident_blocks(reshape_and_cache_kernel<4>, 256);
+        const long long cap = (long long)num_sms * resident;
+        reshape_and_cache_kernel<4><<<(int)(need4 < cap ? need4 : cap), 256, 0, stream>>>(
+            static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new),
+            static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), slot_mapping,
+            num_tokens, num_kv_heads, row_shift, slots, err);
+    } else {
+        reshape_and_cache_kernel<1><<<(int)need1, 256, 0, stream>>>(
+            static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new),
+            static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), slot_mapping,
+            num_tokens, num_kv_heads, row_shift, slots, err);
+    }
     return cudaGetLastError();
 }
 

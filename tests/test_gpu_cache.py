@@ -83,6 +83,31 @@ def test_reshape_and_cache_slot_past_pool(pa):
     assert pa.get_device_error() == pa.DEVERR["SLOT_RANGE"]
 
 
+@pytest.mark.parametrize("D,hkv,layout", [(128, 4, "blocks"), (64, 3, "scatter")])
+def test_reshape_and_cache_many_tokens(pa, D, hkv, layout):
+    # a prefill-sized write: several grid strides of the kernel and a ragged
+    # tail, with padding tokens; whole blocks in order or random distinct slots
+    rng = np.random.default_rng(77 + D)
+    nb, ntok = 2600, 20011
+    if layout == "blocks":
+        blocks = rng.choice(nb, -(-ntok // 16), replace=False)
+        slots = (blocks[:, None] * 16 + np.arange(16)[None, :]).reshape(-1)[:ntok]
+    else:
+        slots = rng.choice(nb * 16, ntok, replace=False)
+    slots = slots.astype(np.int64)
+    slots[rng.choice(ntok, 37, replace=False)] = -1
+    k = rng.integers(0, 1 << 16, (nb, hkv, 16, D), dtype=np.uint16)
+    v = rng.integers(0, 1 << 16, (nb, hkv, 16, D), dtype=np.uint16)
+    kn = rng.integers(0, 1 << 16, (ntok, hkv, D), dtype=np.uint16)
+    vn = rng.integers(0, 1 << 16, (ntok, hkv, D), dtype=np.uint16)
+    dk, dv = dev_bits(k, "bf16"), dev_bits(v, "bf16")
+    pa.reshape_and_cache(dev_bits(kn, "bf16"), dev_bits(vn, "bf16"), dk, dv,
+                         torch.from_numpy(slots).cuda())
+    assert oracle.reshape_and_cache(k, v, kn, vn, slots) == 0
+    assert np.array_equal(host_bits(dk), k) and np.array_equal(host_bits(dv), v)
+    assert pa.get_device_error() == 0
+
+
 @pytest.mark.parametrize("D", [64, 128])
 def test_copy_blocks_bit_exact(pa, D):
     w = synth.parsamp(num_prompts=3, samples=5, prompt_len=72, max_suffix=30, num_heads=8,
