@@ -6,8 +6,9 @@ and the decode (with its split-K merge).  The default run measures the GQA
 batch-128 decode (128 sequences, 32 query / 8 kv heads, head_dim 128, bf16,
 lognormal lengths) as the headline, and the other four decode workloads
 (long-context split-K, MHA 7B-shaped, parallel sampling, tiny) the same way,
-nested under "workloads" in the same line.  ``--workload`` runs one workload
-alone (also the chunked-prefill and swap lines).
+nested under "workloads" in the same line, and the pool-maintenance kernels
+(copy_blocks, reshape_and_cache) alone under "pool_kernels".  ``--workload``
+runs one workload alone (also the chunked-prefill, swap and cache lines).
 
 Prints ONE JSON line (rank 0):
   value      effective KV-read GB/s of the whole job: sum over ranks of the
@@ -896,11 +897,22 @@ def run_ours(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, args.steps, args.warmup)
     nested = {}
+    cache = None
     if args.workload is None and not args.only_headline:
         for name in NESTED:
             r = measure_decode(name, args, device, rank, world)
             r.pop("_w")
             nested[name] = r
+        # the pool-maintenance kernels alone (each rank on its own GPU)
+        cases = measure_cache(args, device)
+        cache = {"metric": CACHE_METRIC, "unit": "GB/s",
+                 "bit_exact": all(c["bit_exact"] for c in cases.values()),
+                 "cases": {k: {f: c[f] for f in ("us_per_launch", "bytes_per_launch", "gbps",
+                                                  "frac", "bit_exact", "traffic")}
+                           for k, c in cases.items()},
+                 "peak": measured_hbm_peak()[0],
+                 "timing": "bulk cases back to back, step-size cases one launch after an L2 "
+                           "flush (`--workload cache` describes each case)"}
     if rank != 0:
         return
     line = {
@@ -921,6 +933,8 @@ def run_ours(args):
     line["cpu_baseline"] = cpu
     if nested:
         line["workloads"] = nested
+    if cache is not None:
+        line["pool_kernels"] = cache
     print(json.dumps(line), flush=True)
 
 
@@ -1015,25 +1029,19 @@ CACHE_CASES = {
 }
 
 
-def run_cache(args):
+def measure_cache(args, device, only=None):
     """The two kernels that maintain the pool, timed alone: copy_blocks (the
     copy-on-write of whole blocks) and reshape_and_cache (each new token's K/V
     into its slot), at a config step's size and at a size large enough to be
     bound by HBM.  GB/s counts the bytes read and written.  The step-size
     pools are compared bit for bit with the oracle's; the bulk copies with
-    their sources."""
+    their sources.  Returns {case: result}."""
     import torch
-    from paged_kv_cache_260_gb300 import _build
-    _build.build()
     import paged_kv_cache_260_gb300 as pa
-    pa.load()
-    device = torch.device("cuda:0")
-    torch.cuda.set_device(device)
-    peak, peak_src = measured_hbm_peak()
+    peak, _ = measured_hbm_peak()
     flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=device)
     rng = np.random.default_rng(1010)
     steps = max(1, min(args.steps, 100))
-    only = args.cache_case
 
     def timed(fn, big):
         g = capture([fn], device)
@@ -1144,7 +1152,26 @@ def run_cache(args):
         ms, timing = timed(lambda: pa.reshape_and_cache(kn, vn, kp, vp, slots), big=True)
         moved = 2 * 2 * kn.numel() * kn.element_size()
         record(name, ms, timing, moved, exact)
+        del kn, vn
+    del kp, vp, flush
+    torch.cuda.empty_cache()
     assert pa.get_device_error() == 0
+    return cases
+
+
+def run_cache(args):
+    """`--workload cache`: measure_cache's cases as one line whose value is
+    the bulk copy's."""
+    import torch
+    from paged_kv_cache_260_gb300 import _build
+    _build.build()
+    import paged_kv_cache_260_gb300 as pa
+    pa.load()
+    device = torch.device("cuda:0")
+    torch.cuda.set_device(device)
+    peak, peak_src = measured_hbm_peak()
+    steps = max(1, min(args.steps, 100))
+    cases = measure_cache(args, device, args.cache_case)
     head = "copy_bulk" if "copy_bulk" in cases else next(iter(cases))
     c = cases[head]
     print(json.dumps({
