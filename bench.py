@@ -302,9 +302,10 @@ class Step:
     def _count_launches(self):
         n = int(self.pairs is not None)                 # copy_blocks
         if self.shared:
-            # prefix attention, suffix decode + merge, final merge (and the
-            # decode's per-sequence arrays above 2048 sequences)
-            return n + 4 + (1 if self.w.num_seqs > 2048 else 0)
+            # prefix attention, suffix decode, final merge (which also folds
+            # the suffix runs the decode cut), and the decode's per-sequence
+            # arrays above 2048 sequences
+            return n + 3 + (1 if self.w.num_seqs > 2048 else 0)
         n += 1                                          # decode (append fused in)
         if self.ps >= 0:
             n += 1                                      # merge of cut runs / partitions

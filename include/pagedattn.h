@@ -250,8 +250,9 @@ int pa_decode_append(void *out, const void *q, void *k_cache, void *v_cache,
  *   workspace    at least pa_decode_shared_prefix_workspace_size(...) bytes,
  *                256-byte aligned, caller-owned, no initialisation needed
  * Other arguments as pa_decode.  Launches: the prefix attention (which also
- * writes the suffix lengths), the suffix decode (with its merge) and the
- * final merge, all programmatic dependent launches.  A sequence shorter than prefix_len sets
+ * writes the suffix lengths), the suffix decode and the final merge (which
+ * also folds the pieces of the suffix runs the decode's split cut), all
+ * programmatic dependent launches.  A sequence shorter than prefix_len sets
  * PA_DEVERR_SEQLEN_RANGE.
  */
 size_t pa_decode_shared_prefix_workspace_size(int num_seqs, int group_size, int prefix_len,

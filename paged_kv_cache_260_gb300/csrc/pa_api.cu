@@ -381,12 +381,22 @@ size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, i
         .total;
 }
 
+// Where a balanced decode leaves the pieces of the runs it cut.
+struct CutPieces {
+    const float *sm = nullptr, *sl = nullptr, *so = nullptr;
+};
+
 // What a decode does beyond pa_decode: the fused append, partial outputs.
 struct DecodeExtra {
     const void *k_new = nullptr, *v_new = nullptr;
     const int64_t *slot_mapping = nullptr;
     float *out_m = nullptr, *out_l = nullptr, *out_o = nullptr;
     const CUtensorMap *tmk = nullptr, *tmv = nullptr;   // the pools' maps, if already encoded
+    // partial outputs, balanced split: record per run whether and where it
+    // was cut ([num_seqs][num_kv_heads] pairs of ints) and leave the cut
+    // pieces to the caller's merge (no merge_cut); *pieces says where they are
+    int32_t *cut_of_run = nullptr;
+    CutPieces *pieces = nullptr;
 };
 
 static int decode_impl(void *out, const void *q, const void *k_cache, const void *v_cache,
@@ -422,6 +432,8 @@ static int decode_impl(void *out, const void *q, const void *k_cache, const void
     rc = decode_mode(partition_size, &mode, &pt);
     if (rc != PA_OK)
         return rc;
+    if (x.cut_of_run && (mode != kModeBalanced || !x.out_o || !x.pieces))
+        return PA_ERR_INVALID_ARG;
 
     KernelSet ks{};
     bool found;
@@ -496,6 +508,7 @@ static int decode_impl(void *out, const void *q, const void *k_cache, const void
     p.out_m = x.out_m;
     p.out_l = x.out_l;
     p.out_o = x.out_o;
+    p.cut_of_run = x.cut_of_run;
     char *ws = static_cast<char *>(workspace);
     if (wl.total > 0) {
         p.ws_m = reinterpret_cast<float *>(ws + wl.m_off);
@@ -551,6 +564,12 @@ static int decode_impl(void *out, const void *q, const void *k_cache, const void
     rc = launch_dependent(decode_fn, dim3(grid), dim3(warps * 32), smem, st, args);
     if (rc != PA_OK || mode == kModeWhole)
         return rc;
+    if (x.cut_of_run) {                  // the caller's merge folds the cut pieces
+        x.pieces->sm = p.ws_sm;
+        x.pieces->sl = p.ws_sl;
+        x.pieces->so = p.ws_so;
+        return PA_OK;
+    }
     void *margs[] = {&p};
     // one warp per query head of the group: small blocks, so all of them can
     // be resident beside the decode while it drains
@@ -603,7 +622,7 @@ namespace pa {
 namespace {
 
 struct SharedLayout {
-    size_t lv, pm, pl, po, xm, xl, xo, dws, dws_bytes, total;
+    size_t lv, cr, pm, pl, po, xm, xl, xo, dws, dws_bytes, total;
     int cols, col_blocks, chunk_tiles, nchunks;
 };
 
@@ -650,6 +669,7 @@ bool shared_layout(int num_seqs, int group_size, int prefix_len, int num_heads, 
         return off;
     };
     L->lv = take((size_t)num_seqs * sizeof(int32_t));
+    L->cr = take((size_t)num_seqs * num_kv_heads * 2 * sizeof(int32_t));
     L->pm = take(rows * sizeof(float));
     L->pl = take(rows * sizeof(float));
     L->po = take(rows * head_dim * sizeof(float));
@@ -790,11 +810,20 @@ int pa_decode_shared_prefix(void *out, const void *q, void *k_cache, void *v_cac
     x.out_o = reinterpret_cast<float *>(ws + L.po);
     x.tmk = &tmk;
     x.tmv = &tmv;
+    // runs the balanced split cuts are folded by the final merge, piece by
+    // piece, instead of by a merge of their own
+    CutPieces pieces;
+    x.cut_of_run = reinterpret_cast<int32_t *>(ws + L.cr);
+    x.pieces = &pieces;
     rc = decode_impl(nullptr, q, k_cache, v_cache, block_tables + sp.prefix_tiles, xp.lens_v,
                      num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
                      num_blocks, scale, dtype, 0, ws + L.dws, L.dws_bytes, stream, x);
     if (rc != PA_OK)
         return rc;
+    sp.cut_of_run = x.cut_of_run;
+    sp.sm = pieces.sm;
+    sp.sl = pieces.sl;
+    sp.so = pieces.so;
     return cuda_status(launch_shared_merge(sp, dtype == PA_DTYPE_BF16, st));
 }
 

@@ -509,11 +509,18 @@ __device__ __forceinline__ void decode_worker(const DecodeParams &p, const CUten
                 }
             }
         }
+        if (PARTIAL && whole && p.cut_of_run && lane == 0)
+            reinterpret_cast<int2 *>(p.cut_of_run)[(size_t)s * p.num_kv_heads + h] =
+                make_int2(-1, 0);
         if (!whole) {
             // the unit (run, or partition in fixed mode) this piece belongs to
             const int u0 = cons.F + (p.mode == kModeFixed ? cons.part * cons.pt : 0);
             const int nu = p.mode == kModeFixed ? min(cons.pt, cons.nt - cons.part * cons.pt) : cons.nt;
             if (!wp && u0 >= cons.A && u0 + nu > cons.B) {
+                if (PARTIAL && p.cut_of_run && lane == 0)
+                    reinterpret_cast<int2 *>(p.cut_of_run)[(size_t)s * p.num_kv_heads + h] =
+                        make_int2(worker, 2 * cut_last_worker(u0, nu, cons.R) +
+                                              (u0 != worker * cons.R ? 1 : 0));
                 desc.s = s;
                 desc.h = h;
                 desc.part = cons.part;
@@ -602,6 +609,10 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
                     p.out_m[(size_t)s * Hq + e] = -INFINITY;
                     p.out_l[(size_t)s * Hq + e] = 0.f;
                 }
+                if (p.cut_of_run)
+                    for (int e = tid; e < p.num_kv_heads; e += W * 32)
+                        reinterpret_cast<int2 *>(p.cut_of_run)[(size_t)s * p.num_kv_heads + e] =
+                            make_int2(-1, 0);
             } else {
                 T *o = reinterpret_cast<T *>(p.out) + (size_t)s * Hq * D;
                 for (int e = tid; e < Hq * D; e += W * 32)
@@ -641,7 +652,7 @@ __global__ void __launch_bounds__(512) merge_cut_kernel(const DecodeParams p)
         return;
     const int s = __ldcg(&dp->s), h = __ldcg(&dp->h), part = __ldcg(&dp->part);
     const int u0 = __ldcg(&dp->u0), nu = __ldcg(&dp->nu), R = __ldcg(&dp->R), np = __ldcg(&dp->np);
-    const int c0 = blockIdx.x, c1 = (u0 + nu - 1) / R;
+    const int c0 = blockIdx.x, c1 = cut_last_worker(u0, nu, R);
     const int npieces = c1 - c0 + 1;
 
     float Mx = -INFINITY, Ws = 0.f, acc[V];
@@ -654,8 +665,7 @@ __global__ void __launch_bounds__(512) merge_cut_kernel(const DecodeParams p)
         for (int i = 0; i < CH; ++i) {
             if (base + i < npieces) {
                 const int c = c0 + base + i;
-                const int slot = (c == c0 && u0 != c0 * R) ? 2 * c + 1 : 2 * c;
-                const size_t row = slot_row(G, slot, g);
+                const size_t row = slot_row(G, cut_piece_slot(c, c0, u0 != c0 * R), g);
                 mv[i] = __ldcg(p.ws_sm + row);
                 lv[i] = __ldcg(p.ws_sl + row);
                 const float *src = p.ws_so + row * D + lane * V;

@@ -40,6 +40,12 @@ struct DecodeParams {
     float *out_m;          // partial-output mode (non-null): each (sequence, query head)'s
     float *out_l;          //   m, l and normalised o go to row s * num_heads + h of these
     float *out_o;          //   [num_seqs][num_heads](x head_dim) fp32 arrays instead of `out`
+    int32_t *cut_of_run;   // partial-output mode, balanced split (or null): per run
+                           //   r = s * num_kv_heads + h two ints, [2r] = -1 if the run is
+                           //   empty or one worker covered it whole, else the first worker
+                           //   c0 of its pieces, and [2r + 1] = 2 * last worker + (c0's
+                           //   piece in its last slot); the caller then folds the pieces
+                           //   itself and no merge_cut runs
     uint32_t *err;         // device error bits (PA_DEVERR_*)
     int num_seqs;
     int num_heads;

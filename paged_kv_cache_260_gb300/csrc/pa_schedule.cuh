@@ -234,4 +234,18 @@ struct CutDesc {
     int nu, R, np, valid; // tiles of the unit, tiles per worker, partitions of the run, flag
 };
 
+// The pieces of a cut unit [u0, u0 + nu) whose descriptor is worker c0's:
+// one in each of workers c0 .. cut_last_worker; worker c's piece is in its
+// first slot (2c), except worker c0's when the unit starts inside its range
+// (c0_last: its last slot, 2c0 + 1).
+__device__ __forceinline__ int cut_last_worker(int u0, int nu, int R)
+{
+    return (u0 + nu - 1) / R;
+}
+
+__device__ __forceinline__ int cut_piece_slot(int c, int c0, bool c0_last)
+{
+    return (c == c0 && c0_last) ? 2 * c + 1 : 2 * c;
+}
+
 }  // namespace pa

@@ -12,13 +12,15 @@
 // FlashDecoding in the ICML tutorial notes, section "内核优化").
 //
 //  * shared_merge_kernel combines each (sample, head)'s prefix partials (one
-//    per key chunk) with its suffix partial into the output.
+//    per key chunk) with its suffix partial -- or, where the suffix decode's
+//    balanced split cut the run, with the run's pieces -- into the output.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <math.h>
 #include <stdint.h>
 
 #include "pa_device.cuh"
+#include "pa_schedule.cuh"
 #include "pa_shared.h"
 #include "pagedattn.h"
 
@@ -26,7 +28,8 @@ namespace pa {
 namespace {
 
 // One warp per (sample, query head), over its partials (m_i, l_i, o_i) --
-// the prefix's key chunks and the suffix:
+// the prefix's key chunks, then the suffix (one row, or the pieces of a cut
+// run in the decode's worker slots):
 //     M = max_i m_i,  w_i = l_i exp(m_i - M),  out = sum_i w_i o_i / sum_i w_i
 // Lane i reads partial i's m and l (32 at a time), so the weights need one
 // warp reduction, and the o rows are then summed eight at a time with their
@@ -47,16 +50,41 @@ __global__ void __launch_bounds__(256) shared_merge_kernel(const SharedParams p)
     const int h = hq / G, c = smp * G + hq % G;
     const size_t cstride = (size_t)(p.num_seqs / p.group_size) * p.num_kv_heads * p.cols;
     const size_t xrow = ((size_t)g * p.num_kv_heads + h) * p.cols + c;   // chunk 0
-    const size_t srow = (size_t)warp;                                     // the suffix
-    const int np = p.nchunks + 1;                    // partial np - 1 is the suffix
-    auto row_of = [&](int i) { return i < p.nchunks ? xrow + (size_t)i * cstride : srow; };
-    auto m_of = [&](int i) { return i < p.nchunks ? p.xm[row_of(i)] : p.pm[srow]; };
-    auto l_of = [&](int i) { return i < p.nchunks ? p.xl[row_of(i)] : p.pl[srow]; };
-    auto o_of = [&](int i) { return i < p.nchunks ? p.xo + row_of(i) * p.head_dim
-                                                  : p.po + srow * p.head_dim; };
+    // the prefix chunks' m and l (partial `lane` of the first 32), loaded
+    // while the suffix's record is looked up
+    const int nx = p.nchunks;
+    float mr = -INFINITY, lr = 0.f;
+    if (lane < nx) {
+        mr = p.xm[xrow + (size_t)lane * cstride];
+        lr = p.xl[xrow + (size_t)lane * cstride];
+    }
+    // the suffix: row `warp` of pm/pl/po, or the pieces of a cut run
+    const int2 cut = __ldcg(reinterpret_cast<const int2 *>(p.cut_of_run) +
+                            (size_t)s * p.num_kv_heads + h);
+    const int c0 = cut.x;
+    const bool c0_last = cut.y & 1;
+    const int nsuf = c0 >= 0 ? (cut.y >> 1) - c0 + 1 : 1;
+    const float *sm = c0 >= 0 ? p.sm : p.pm;
+    const float *sl = c0 >= 0 ? p.sl : p.pl;
+    const float *so = c0 >= 0 ? p.so : p.po;
+    const int np = nx + nsuf;                        // partials nx.. are the suffix's
+    auto row_of = [&](int i) -> size_t {
+        if (i < nx)
+            return xrow + (size_t)i * cstride;
+        if (c0 < 0)
+            return (size_t)warp;
+        return (size_t)cut_piece_slot(c0 + (i - nx), c0, c0_last) * G + hq % G;
+    };
+    auto m_of = [&](int i) { return i < nx ? p.xm[row_of(i)] : __ldcg(sm + row_of(i)); };
+    auto l_of = [&](int i) { return i < nx ? p.xl[row_of(i)] : __ldcg(sl + row_of(i)); };
+    auto o_of = [&](int i) { return (i < nx ? p.xo : so) + row_of(i) * p.head_dim; };
+    if (lane >= nx && lane < np) {
+        mr = m_of(lane);
+        lr = l_of(lane);
+    }
     // M over the non-empty partials
-    float M = -INFINITY;
-    for (int i = lane; i < np; i += 32) {
+    float M = lr > 0.f ? mr : -INFINITY;
+    for (int i = 32 + lane; i < np; i += 32) {
         if (l_of(i) > 0.f)
             M = fmaxf(M, m_of(i));
     }
@@ -69,8 +97,9 @@ __global__ void __launch_bounds__(256) shared_merge_kernel(const SharedParams p)
         const int i = base + lane;
         float w = 0.f;
         if (i < np) {
-            const float l = l_of(i);
-            w = l > 0.f ? l * expf(m_of(i) - M) : 0.f;   // an empty partial weighs nothing
+            const float l = base == 0 ? lr : l_of(i);
+            const float m = base == 0 ? mr : m_of(i);
+            w = l > 0.f ? l * expf(m - M) : 0.f;     // an empty partial weighs nothing
         }
         const int cnt = min(32, np - base);
         for (int k0 = 0; k0 < cnt; k0 += 8) {

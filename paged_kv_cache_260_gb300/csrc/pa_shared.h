@@ -20,6 +20,13 @@ struct SharedParams {
     // [nchunks][num_groups * num_kv_heads][cols] (m, l; o with head_dim more)
     const float *pm, *pl, *po;
     const float *xm, *xl, *xo;
+    // a suffix run r = (s, kv head h) that the decode's balanced split cut
+    // has no row in pm/pl/po: cut_of_run[2r] >= 0 is the first worker c0 of
+    // its pieces and cut_of_run[2r + 1] = 2 * last worker + (c0's piece in
+    // its last slot); each piece is in a worker slot of sm/sl/so
+    // ([2 * workers][G] rows)
+    const int32_t *cut_of_run;
+    const float *sm, *sl, *so;
     int nchunks, cols;             // key chunks of the prefix; group_size * G
     void *out;                     // [num_seqs][num_heads][head_dim]
 };

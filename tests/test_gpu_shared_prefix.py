@@ -154,3 +154,20 @@ def test_repeated_calls_give_the_same_bits(pa):
     assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
     ref, _, _ = oracle.step(w)
     assert max_err(outs[1], ref) <= TOL[w.dtype]
+
+
+@pytest.mark.parametrize("prompt_len,hq,hkv,suffix", [
+    (64, 8, 2, [3000, 5000]),     # suffix runs cut into far more than 32 pieces
+    (16384, 4, 1, [700, 1500]),   # and a prefix in more than 32 key chunks
+])
+def test_long_suffixes_cut_into_many_pieces(pa, prompt_len, hq, hkv, suffix):
+    # the suffix decode's balanced split cuts each long suffix run into many
+    # pieces, which the final merge folds together with the prefix chunks
+    w = synth.parsamp(poison=True, num_prompts=1, samples=2, prompt_len=prompt_len,
+                      num_heads=hq, num_kv_heads=hkv, head_dim=128, dtype="bf16", seed=23,
+                      suffix_lens=suffix)
+    dw, out = run(pa, w)
+    assert pa.get_device_error() == 0
+    ref, k_ref, v_ref = oracle.step(w)
+    assert max_err(out, ref) <= TOL[w.dtype]
+    assert np.array_equal(host_bits(dw.k), k_ref) and np.array_equal(host_bits(dw.v), v_ref)
