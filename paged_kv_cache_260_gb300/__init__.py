@@ -49,6 +49,9 @@ class PagedAttnError(RuntimeError):
 def load(path: str = LIB_PATH):
     """Load the library (once).  Raises if it has not been built."""
     global _lib
+    L = _lib
+    if L is not None:                    # every call after the first
+        return L
     with _lock:
         if _lib is not None:
             return _lib
@@ -120,14 +123,30 @@ def _dtype_code(t) -> int:
 
 
 def _ptr(t):
-    return None if t is None else C.c_void_p(t.data_ptr())
+    # a plain int: the argtypes (c_void_p) convert it
+    return None if t is None else t.data_ptr()
+
+
+_current_raw_stream = None
 
 
 def _stream(stream):
-    torch = _torch()
-    if stream is None:
-        stream = torch.cuda.current_stream()
-    return C.c_void_p(stream.cuda_stream)
+    """The stream's handle; by default the current device's current stream,
+    read as a raw handle (building a torch.cuda.Stream object for it costs a
+    few microseconds a call)."""
+    global _current_raw_stream
+    if stream is not None:
+        return stream.cuda_stream
+    if _current_raw_stream is None:
+        torch = _torch()
+        raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+        dev = getattr(torch._C, "_cuda_getDevice", None)
+        if raw is not None and dev is not None:
+            torch.cuda.init()
+            _current_raw_stream = lambda: raw(dev())
+        else:
+            _current_raw_stream = lambda: torch.cuda.current_stream().cuda_stream
+    return _current_raw_stream()
 
 
 def _scratch(nbytes, device, stream):
