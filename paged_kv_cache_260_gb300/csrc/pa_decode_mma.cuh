@@ -91,15 +91,6 @@ __device__ __forceinline__ size_t slot_row(int G, int slot, int g)
     return (size_t)slot * G + g;
 }
 
-// Whether this thread's strided share of the flags holds a set one.
-__device__ __forceinline__ bool share_any_of(const uint8_t *share, int n, int tid, int nth)
-{
-    bool any = false;
-    for (int s = tid; s < n; s += nth)
-        any |= share[s] != 0;
-    return any;
-}
-
 // Large batches: the per-sequence arrays (clamped lengths, unit prefix,
 // first-block-shared flags) are built once into the workspace by this
 // one-block kernel, instead of by every decode block into its shared memory;
@@ -110,8 +101,8 @@ __global__ void __launch_bounds__(NTH) decode_prep_kernel(const DecodeParams p)
     // the decode that follows may be scheduled now; it waits for this grid
     grid_dependents_launch();
     grid_dependency_wait();
-    build_prefix<NTH>(p, p.ws_pre, p.ws_lens, p.ws_share);
-    const bool any = __syncthreads_or(share_any_of(p.ws_share, p.num_seqs, threadIdx.x, NTH));
+    const bool any =
+        __syncthreads_or(build_prefix<NTH, 4, 2>(p, p.ws_pre, p.ws_lens, p.ws_share));
     if (threadIdx.x == 0)
         p.ws_share[p.num_seqs] = any ? 1 : 0;
 }
@@ -578,25 +569,22 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
     const uint8_t *share;
     bool any_share = false;
     if (seq_global) {
-        // built by decode_prep_kernel, the grid this one waited for
+        // built by decode_prep_kernel, the grid this one waited for, which
+        // leaves after the flags whether any is set
         pre = p.ws_pre;
         lens = p.ws_lens;
         share = p.ws_share;
+        any_share = __syncthreads_or(tid == 0 && share[n] != 0);
     } else {
         int32_t *spre = reinterpret_cast<int32_t *>(bars + W * S);
         int32_t *slens = spre + n + 1;
         uint8_t *sshare = reinterpret_cast<uint8_t *>(slens + n);
-        build_prefix<W * 32>(p, spre, slens, sshare);
+        // the barrier also publishes the arrays
+        any_share = __syncthreads_or(build_prefix<W * 32, 1, 4>(p, spre, slens, sshare));
         pre = spre;
         lens = slens;
         share = sshare;
     }
-    // whether any sequence shares its first block (the prep kernel leaves
-    // the answer after the flags); the barrier also publishes the arrays
-    if (seq_global)
-        any_share = __syncthreads_or(tid == 0 && share[n] != 0);
-    else
-        any_share = __syncthreads_or(share_any_of(share, n, tid, W * 32));
 
     // sequences without tokens get zeros (no piece ever covers them); in
     // partial-output mode an empty partial result (m = -inf, l = 0)

@@ -168,63 +168,138 @@ __device__ __forceinline__ int seq_units(int L, int mode)
     return mode == kModeWhole ? (nt > 0 ? 1 : 0) : nt;
 }
 
-// Clamp the lengths into shared memory and build the exclusive unit prefix.
-// Also flag each sequence whose first block is named by a neighbouring
-// sequence's table too (share[s] = 1): sequences forked from one prompt
-// (parallel samples) share their prompt's blocks and sit next to each other
-// in the batch.  Only flagged sequences pay for per-tile sharing checks.
-template <int NT>
-__device__ __forceinline__ void build_prefix(const DecodeParams &p, int32_t *pre, int32_t *lens,
+// Clamp the lengths and build the exclusive unit prefix (into shared memory
+// in the decode kernel, into the workspace in the prep kernel for large
+// batches).  Also flag each sequence whose first block is named by a
+// neighbouring sequence's table too (share[s] = 1): sequences forked from one
+// prompt (parallel samples) share their prompt's blocks and sit next to each
+// other in the batch.  Only flagged sequences pay for per-tile sharing checks.
+// Returns whether any of this thread's sequences is flagged.
+//
+// The block walks the batch in rows of K * NT consecutive sequences, thread
+// t taking sequences row + K t .. row + K t + K - 1, so a warp's loads cover
+// one contiguous stretch (a thread owning a long run of consecutive
+// sequences made each warp load touch 32 cache lines).  The neighbours at a
+// thread's ends come from the adjacent lanes by shuffle, at a warp's ends
+// from plain loads.  Each row's units are scanned across the block and added
+// to the running total of the rows before it; RW rows' loads are issued at
+// once.  The large-batch prep kernel takes K = 4 (a quarter of the rows and
+// block barriers); a decode block, whose batch is at most a few rows, K = 1
+// (with K = 4 one warp would hold a small batch's every sequence).
+template <int NT, int K, int RW>
+__device__ __forceinline__ bool build_prefix(const DecodeParams &p, int32_t *pre, int32_t *lens,
                                              uint8_t *share)
 {
     constexpr int NW = NT / 32;
+    constexpr int ROW = K * NT;
+    constexpr uint32_t FULL = 0xffffffffu;
     __shared__ int warp_sum[NW];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int n = p.num_seqs;
-    const int per = (n + NT - 1) / NT;
-    const int lo = min(n, tid * per), hi = min(n, lo + per);
     const int maxlen = p.max_blocks * kBlockSize;
     const size_t mb = (size_t)p.max_blocks;
-    int sum = 0;
-    bool bad = false;
-    for (int s = lo; s < hi; ++s) {
+    int carry = 0;
+    bool bad = false, any = false;
+    for (int base = 0; base < n; base += RW * ROW) {
         // every load below is in bounds whatever the lengths hold
-        int L = __ldg(p.seq_lens + s);
-        const int Lp = s > 0 ? __ldg(p.seq_lens + s - 1) : 0;
-        const int Ln = s + 1 < n ? __ldg(p.seq_lens + s + 1) : 0;
-        const int b0 = __ldg(p.block_tables + s * mb);
-        const int bp = s > 0 ? __ldg(p.block_tables + (s - 1) * mb) : -1;
-        const int bn = s + 1 < n ? __ldg(p.block_tables + (s + 1) * mb) : -1;
-        if (L < 0 || L > maxlen) {
-            bad = true;
-            L = L < 0 ? 0 : maxlen;
+        int Lr[RW][K], br[RW][K], Le[RW], be[RW];
+#pragma unroll
+        for (int r = 0; r < RW; ++r) {
+            const int s0 = base + r * ROW + K * tid;
+#pragma unroll
+            for (int k = 0; k < K; ++k) {
+                const int s = s0 + k;
+                Lr[r][k] = 0;
+                br[r][k] = -1;
+                if (s < n) {
+                    Lr[r][k] = __ldg(p.seq_lens + s);
+                    br[r][k] = __ldg(p.block_tables + s * mb);
+                }
+            }
+            // the warp's ends: lane 0 needs sequence s0 - 1, lane 31 s0 + K
+            const int e = lane == 0 ? s0 - 1 : s0 + K;
+            Le[r] = 0;
+            be[r] = -1;
+            if ((lane == 0 || lane == 31) && e >= 0 && e < n) {
+                Le[r] = __ldg(p.seq_lens + e);
+                be[r] = __ldg(p.block_tables + e * mb);
+            }
         }
-        lens[s] = L;
-        share[s] = (uint8_t)(L > 0 && ((Lp > 0 && bp == b0) || (Ln > 0 && bn == b0)));
-        sum += seq_units(L, p.mode);
+#pragma unroll
+        for (int r = 0; r < RW; ++r) {
+            const int row = base + r * ROW;
+            if (row >= n)
+                break;                                   // the same for the whole block
+            const int s0 = row + K * tid;
+            // raw neighbour values (a sequence past the end reads as empty)
+            int Lp = __shfl_up_sync(FULL, Lr[r][K - 1], 1);
+            int bp = __shfl_up_sync(FULL, br[r][K - 1], 1);
+            int Ln = __shfl_down_sync(FULL, Lr[r][0], 1);
+            int bn = __shfl_down_sync(FULL, br[r][0], 1);
+            if (lane == 0) {
+                Lp = Le[r];
+                bp = be[r];
+            }
+            if (lane == 31) {
+                Ln = Le[r];
+                bn = be[r];
+            }
+            int u[K], sum = 0;
+#pragma unroll
+            for (int k = 0; k < K; ++k) {
+                const int s = s0 + k;
+                u[k] = 0;
+                if (s < n) {
+                    int L = Lr[r][k];
+                    if (L < 0 || L > maxlen) {
+                        bad = true;
+                        L = L < 0 ? 0 : maxlen;
+                    }
+                    const int lp = k > 0 ? Lr[r][k - 1] : Lp, bpk = k > 0 ? br[r][k - 1] : bp;
+                    const int ln = k + 1 < K ? Lr[r][k + 1] : Ln;
+                    const int bnk = k + 1 < K ? br[r][k + 1] : bn;
+                    const bool sh = L > 0 && ((lp > 0 && bpk == br[r][k]) ||
+                                              (ln > 0 && bnk == br[r][k]));
+                    lens[s] = L;
+                    share[s] = (uint8_t)sh;
+                    any |= sh;
+                    u[k] = seq_units(L, p.mode);
+                }
+                sum += u[k];
+            }
+            int incl = sum;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(FULL, incl, o);
+                if (lane >= o)
+                    incl += y;
+            }
+            if (lane == 31)
+                warp_sum[warp] = incl;
+            __syncthreads();
+            int before = 0, total = 0;
+#pragma unroll
+            for (int w = 0; w < NW; ++w) {
+                const int x = warp_sum[w];
+                before += w < warp ? x : 0;
+                total += x;
+            }
+            int run = carry + before + incl - sum;
+#pragma unroll
+            for (int k = 0; k < K; ++k) {
+                if (s0 + k < n)
+                    pre[s0 + k] = run;
+                run += u[k];
+            }
+            carry += total;
+            __syncthreads();                             // warp_sum is reused
+        }
     }
     if (bad && blockIdx.x == 0)
         record_error(p.err, PA_DEVERR_SEQLEN_RANGE);
-    int incl = sum;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o)
-            incl += y;
-    }
-    if (lane == 31)
-        warp_sum[warp] = incl;
-    __syncthreads();
-    int before = 0;
-    for (int w = 0; w < warp; ++w)
-        before += warp_sum[w];
-    int run = before + incl - sum;
-    for (int s = lo; s < hi; ++s) {
-        pre[s] = run;
-        run += seq_units(lens[s], p.mode);
-    }
-    if (tid == NT - 1)
-        pre[n] = before + incl;
+    if (tid == 0)
+        pre[n] = carry;
+    return any;
 }
 
 // A cut unit (a run in balanced mode, a partition in fixed mode) as recorded
