@@ -58,3 +58,26 @@ def test_steps_per_graph_divides_steps():
     for k in (1, 7, 10, 64, 20000, 97):
         d = bench.pick_steps_per_graph(k)
         assert k % d == 0 and 1 <= d <= 32
+
+
+def _bench_line(*args):
+    import json
+    import subprocess
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args],
+                       capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def test_reference_arm_lines_on_cpu():
+    # the oracle's copy_blocks on the bulk pool case: the contract's keys,
+    # its own e2e and cpu_baseline, no GPU needed
+    d = _bench_line("--impl", "reference", "--workload", "cache", "--steps", "1",
+                    "--warmup", "1")
+    assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["value"] > 0
+    assert d["higher_is_better"] is True and d["cpu_baseline"]["kind"] == "oracle"
+    assert d["e2e"]["value"] == d["value"] and d["e2e"]["h2d_bytes_per_step"] == 0
+    assert d["config"]["case"] == "copy_bulk"
+    # swapping has no oracle timing: an `unavailable` line, exit 0
+    d = _bench_line("--impl", "reference", "--workload", "swap")
+    assert d["impl"] == "reference" and "unavailable" in d
