@@ -264,7 +264,7 @@ int cuda_status(cudaError_t e) { return e == cudaSuccess ? PA_OK : PA_ERR_CUDA; 
 
 struct WorkspaceLayout {
     size_t m_off, l_off, o_off, sm_off, sl_off, so_off, desc_off, pre_off, lens_off, share_off,
-        total;
+        blk_off, total;
     bool seq_global;
 };
 
@@ -278,7 +278,8 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 //   cut), then one cut descriptor per worker;
 //   any mode, batches above kSeqsInSmem: the unit prefix [num_seqs + 1] and
 //   the clamped lengths [num_seqs], int32, and the first-block-shared flags
-//   [num_seqs] plus one "any flag set" byte, built by the prep kernel.
+//   [num_seqs] plus one "any flag set" byte, built by the prep kernels, and
+//   the prep blocks' unit counts and flags [ceil(num_seqs / kPrepSeqs)][2].
 WorkspaceLayout workspace_layout(int mode, int num_seqs, int num_heads, int num_kv_heads,
                                  int head_dim, int p_max, int workers)
 {
@@ -311,6 +312,9 @@ WorkspaceLayout workspace_layout(int mode, int num_seqs, int num_heads, int num_
         at = round_up(at + sizeof(int32_t) * (size_t)num_seqs, 256);
         w.share_off = at;
         at = round_up(at + (size_t)num_seqs + 1, 256);
+        w.blk_off = at;
+        at = round_up(at + 2 * sizeof(int32_t) * (((size_t)num_seqs + kPrepSeqs - 1) / kPrepSeqs),
+                      256);
     }
     w.total = at;
     return w;
@@ -523,6 +527,7 @@ static int decode_impl(void *out, const void *q, const void *k_cache, const void
             p.ws_pre = reinterpret_cast<int32_t *>(ws + wl.pre_off);
             p.ws_lens = reinterpret_cast<int32_t *>(ws + wl.lens_off);
             p.ws_share = reinterpret_cast<uint8_t *>(ws + wl.share_off);
+            p.ws_blk = reinterpret_cast<int32_t *>(ws + wl.blk_off);
         }
     }
     p.err = ds->err;
@@ -557,7 +562,10 @@ static int decode_impl(void *out, const void *q, const void *k_cache, const void
     void *args[] = {&p, &tmk, &tmv};
     if (wl.seq_global) {
         void *pargs[] = {&p};
-        rc = launch_dependent(ks.prep, dim3(1), dim3(kPrepThreads), 0, st, pargs);
+        const dim3 pgrid((num_seqs + kPrepSeqs - 1) / kPrepSeqs);
+        rc = launch_dependent(ks.prep, pgrid, dim3(kPrepThreads), 0, st, pargs);
+        if (rc == PA_OK)
+            rc = launch_dependent(ks.prep_fix, pgrid, dim3(kPrepThreads), 0, st, pargs);
         if (rc != PA_OK)
             return rc;
     }

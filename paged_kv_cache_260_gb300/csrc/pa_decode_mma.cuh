@@ -92,19 +92,73 @@ __device__ __forceinline__ size_t slot_row(int G, int slot, int g)
 }
 
 // Large batches: the per-sequence arrays (clamped lengths, unit prefix,
-// first-block-shared flags) are built once into the workspace by this
-// one-block kernel, instead of by every decode block into its shared memory;
-// share[num_seqs] is left set when any flag is.
+// first-block-shared flags) are built once into the workspace by two kernels
+// of kPrepSeqs-sequence blocks, instead of by every decode block into its
+// shared memory.  decode_prep_kernel builds its block's sequences with the
+// prefix counted from the block's first, and leaves the block's unit count
+// and any-flag in ws_blk; decode_prep_fix_kernel adds the counts of the
+// blocks before it, and its last block writes the batch's total
+// (pre[num_seqs]) and whether any flag is set (share[num_seqs]).  Neither
+// waits for another block of its own grid.
 template <int NTH>
 __global__ void __launch_bounds__(NTH) decode_prep_kernel(const DecodeParams p)
 {
-    // the decode that follows may be scheduled now; it waits for this grid
+    static_assert(4 * NTH == kPrepSeqs, "one row of four sequences a thread per block");
+    // the kernel that follows may be scheduled now; it waits for this grid
     grid_dependents_launch();
     grid_dependency_wait();
-    const bool any =
-        __syncthreads_or(build_prefix<NTH, 4, 2>(p, p.ws_pre, p.ws_lens, p.ws_share));
-    if (threadIdx.x == 0)
+    const int begin = blockIdx.x * kPrepSeqs, end = min(p.num_seqs, begin + kPrepSeqs);
+    int total;
+    const bool any = __syncthreads_or(
+        build_prefix<NTH, 4, 1>(p, begin, end, p.ws_pre, p.ws_lens, p.ws_share, &total));
+    if (threadIdx.x == 0) {
+        p.ws_blk[2 * blockIdx.x] = total;
+        p.ws_blk[2 * blockIdx.x + 1] = any ? 1 : 0;
+    }
+}
+
+template <int NTH>
+__global__ void __launch_bounds__(NTH) decode_prep_fix_kernel(const DecodeParams p)
+{
+    grid_dependents_launch();
+    grid_dependency_wait();
+    __shared__ int red[NTH / 32][2];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int b = blockIdx.x, last = gridDim.x - 1;
+    // the unit count of the blocks before this one (and, in the last block,
+    // whether any block flagged a sequence)
+    int off = 0, any = 0;
+    // (written by the grid before: read through L2)
+    for (int i = tid; i < b; i += NTH)
+        off += __ldcg(p.ws_blk + 2 * i);
+    if (b == last)
+        for (int i = tid; i <= last; i += NTH)
+            any |= __ldcg(p.ws_blk + 2 * i + 1);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        off += __shfl_xor_sync(0xffffffffu, off, o);
+        any |= __shfl_xor_sync(0xffffffffu, any, o);
+    }
+    if (lane == 0) {
+        red[warp][0] = off;
+        red[warp][1] = any;
+    }
+    __syncthreads();
+    off = 0;
+    any = 0;
+#pragma unroll
+    for (int w = 0; w < NTH / 32; ++w) {
+        off += red[w][0];
+        any |= red[w][1];
+    }
+    const int begin = b * kPrepSeqs, end = min(p.num_seqs, begin + kPrepSeqs);
+    if (off != 0)
+        for (int s = begin + tid; s < end; s += NTH)
+            p.ws_pre[s] = __ldcg(p.ws_pre + s) + off;
+    if (b == last && tid == 0) {
+        p.ws_pre[p.num_seqs] = off + __ldcg(p.ws_blk + 2 * b);
         p.ws_share[p.num_seqs] = any ? 1 : 0;
+    }
 }
 
 // L2 policy for a tile that another sequence's table also names (a block
@@ -580,7 +634,12 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
         int32_t *slens = spre + n + 1;
         uint8_t *sshare = reinterpret_cast<uint8_t *>(slens + n);
         // the barrier also publishes the arrays
-        any_share = __syncthreads_or(build_prefix<W * 32, 1, 4>(p, spre, slens, sshare));
+        int total;
+        any_share = __syncthreads_or(build_prefix<W * 32, 1, 4>(p, 0, n, spre, slens, sshare,
+                                                                   &total));
+        if (tid == 0)
+            spre[n] = total;
+        __syncthreads();
         pre = spre;
         lens = slens;
         share = sshare;
@@ -824,6 +883,7 @@ inline void fill_kernel_set(KernelSet *ks)
     ks->warps = W;
     ks->smem_fixed = MmaLayout<D, NT, W, S>::fixed;
     ks->prep = reinterpret_cast<const void *>(&decode_prep_kernel<kPrepThreads>);
+    ks->prep_fix = reinterpret_cast<const void *>(&decode_prep_fix_kernel<kPrepThreads>);
     ks->merge_cut = reinterpret_cast<const void *>(&merge_cut_kernel<T, D>);
     ks->merge_part = reinterpret_cast<const void *>(&merge_part_kernel<T, D>);
 }

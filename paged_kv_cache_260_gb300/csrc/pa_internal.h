@@ -37,6 +37,8 @@ struct DecodeParams {
     int32_t *ws_pre;       // large batches: unit prefix [num_seqs + 1] in the workspace, or null
     int32_t *ws_lens;      //   clamped lengths [num_seqs] (null: all three in shared memory)
     uint8_t *ws_share;     //   and first-block-shared flags [num_seqs]
+    int32_t *ws_blk;       //   the prep kernels' per-block unit count and any-flag
+                           //   [ceil(num_seqs / kPrepSeqs)][2]
     float *out_m;          // partial-output mode (non-null): each (sequence, query head)'s
     float *out_l;          //   m, l and normalised o go to row s * num_heads + h of these
     float *out_o;          //   [num_seqs][num_heads](x head_dim) fp32 arrays instead of `out`
@@ -66,7 +68,8 @@ struct KernelSet {
     const void *decode_partial;  // the same writing fp32 partial results (16 columns only)
     int warps;
     size_t smem_fixed;       // dynamic shared memory excluding the per-sequence arrays
-    const void *prep;        // large batches: builds the per-sequence arrays in the workspace
+    const void *prep;        // large batches: build the per-sequence arrays in the workspace,
+    const void *prep_fix;    //   block by block, then add the earlier blocks' unit counts
     const void *merge_cut;   // combines the pieces of cut units
     const void *merge_part;  // fixed mode: merges partitions into the output
 };
@@ -83,7 +86,8 @@ inline size_t decode_smem_bytes(size_t smem_fixed, int num_seqs)
 // shared memory (every variant fits them under the 227 KiB limit); larger
 // ones have them built once in the workspace by the prep kernel.
 constexpr int kSeqsInSmem = 2048;
-constexpr int kPrepThreads = 1024;
+constexpr int kPrepThreads = 256;
+constexpr int kPrepSeqs = 4 * kPrepThreads;   // sequences a prep block builds
 constexpr int kMaxWarpsPerSM = 16;    // decode workers <= SMs * this (workspace sizing)
 constexpr int kMinTiles = 2;          // split modes: least tiles per worker (warp)
 constexpr int kMaxGroup = 16;         // query heads per kv head: two 8-column tiles

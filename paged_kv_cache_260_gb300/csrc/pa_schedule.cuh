@@ -174,21 +174,25 @@ __device__ __forceinline__ int seq_units(int L, int mode)
 // neighbouring sequence's table too (share[s] = 1): sequences forked from one
 // prompt (parallel samples) share their prompt's blocks and sit next to each
 // other in the batch.  Only flagged sequences pay for per-tile sharing checks.
-// Returns whether any of this thread's sequences is flagged.
+// This builds sequences [begin, end) with the prefix counted from begin
+// (neighbours are looked up in the whole batch), leaves the range's unit
+// count in *total and returns whether any of this thread's sequences is
+// flagged; pre[end] is not written.
 //
-// The block walks the batch in rows of K * NT consecutive sequences, thread
+// The block walks the range in rows of K * NT consecutive sequences, thread
 // t taking sequences row + K t .. row + K t + K - 1, so a warp's loads cover
 // one contiguous stretch (a thread owning a long run of consecutive
 // sequences made each warp load touch 32 cache lines).  The neighbours at a
 // thread's ends come from the adjacent lanes by shuffle, at a warp's ends
 // from plain loads.  Each row's units are scanned across the block and added
 // to the running total of the rows before it; RW rows' loads are issued at
-// once.  The large-batch prep kernel takes K = 4 (a quarter of the rows and
-// block barriers); a decode block, whose batch is at most a few rows, K = 1
-// (with K = 4 one warp would hold a small batch's every sequence).
+// once.  The large-batch prep kernels take K = 4 (one row of 1024
+// sequences a block); a decode block, whose batch is at most a few rows,
+// K = 1 (with K = 4 one warp would hold a small batch's every sequence).
 template <int NT, int K, int RW>
-__device__ __forceinline__ bool build_prefix(const DecodeParams &p, int32_t *pre, int32_t *lens,
-                                             uint8_t *share)
+__device__ __forceinline__ bool build_prefix(const DecodeParams &p, int begin, int end,
+                                             int32_t *pre, int32_t *lens, uint8_t *share,
+                                             int *total_out)
 {
     constexpr int NW = NT / 32;
     constexpr int ROW = K * NT;
@@ -200,7 +204,7 @@ __device__ __forceinline__ bool build_prefix(const DecodeParams &p, int32_t *pre
     const size_t mb = (size_t)p.max_blocks;
     int carry = 0;
     bool bad = false, any = false;
-    for (int base = 0; base < n; base += RW * ROW) {
+    for (int base = begin; base < end; base += RW * ROW) {
         // every load below is in bounds whatever the lengths hold
         int Lr[RW][K], br[RW][K], Le[RW], be[RW];
 #pragma unroll
@@ -228,7 +232,7 @@ __device__ __forceinline__ bool build_prefix(const DecodeParams &p, int32_t *pre
 #pragma unroll
         for (int r = 0; r < RW; ++r) {
             const int row = base + r * ROW;
-            if (row >= n)
+            if (row >= end)
                 break;                                   // the same for the whole block
             const int s0 = row + K * tid;
             // raw neighbour values (a sequence past the end reads as empty)
@@ -249,7 +253,7 @@ __device__ __forceinline__ bool build_prefix(const DecodeParams &p, int32_t *pre
             for (int k = 0; k < K; ++k) {
                 const int s = s0 + k;
                 u[k] = 0;
-                if (s < n) {
+                if (s < end) {
                     int L = Lr[r][k];
                     if (L < 0 || L > maxlen) {
                         bad = true;
@@ -287,7 +291,7 @@ __device__ __forceinline__ bool build_prefix(const DecodeParams &p, int32_t *pre
             int run = carry + before + incl - sum;
 #pragma unroll
             for (int k = 0; k < K; ++k) {
-                if (s0 + k < n)
+                if (s0 + k < end)
                     pre[s0 + k] = run;
                 run += u[k];
             }
@@ -295,10 +299,9 @@ __device__ __forceinline__ bool build_prefix(const DecodeParams &p, int32_t *pre
             __syncthreads();                             // warp_sum is reused
         }
     }
-    if (bad && blockIdx.x == 0)
+    if (bad && (blockIdx.x == 0 || begin > 0))
         record_error(p.err, PA_DEVERR_SEQLEN_RANGE);
-    if (tid == 0)
-        pre[n] = carry;
+    *total_out = carry;
     return any;
 }
 
