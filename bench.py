@@ -307,7 +307,13 @@ class Step:
             # arrays above 2048 sequences
             return n + 3 + (1 if self.w.num_seqs > 2048 else 0)
         n += 1                                          # decode (append fused in)
-        if self.ps >= 0:
+        # the library decodes short runs whole when each gets a warp of its
+        # own (tables at most 8 blocks wide, at most four runs per SM)
+        import torch
+        sms = torch.cuda.get_device_properties(self.dev).multi_processor_count
+        whole = self.ps < 0 or (self.ps == 0 and self.tables.shape[1] <= 8 and
+                                self.w.num_seqs * self.k.shape[1] <= 4 * sms)
+        if not whole:
             n += 1                                      # merge of cut runs / partitions
         if self.ps > 0 and self.tables.shape[1] * 16 > self.ps:
             n += 1                                      # merge of partitions per run

@@ -107,7 +107,10 @@ size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads,
  *   -1  no split: one warp reduces each (sequence, kv head) run whole;
  *    0  balanced split: the grid is sized to the GPU and every warp gets the
  *       same number of 16-token tiles; runs cut by a tile-range boundary are
- *       finished by a log-sum-exp merge;
+ *       finished by a log-sum-exp merge.  A batch whose tables are at most
+ *       kWholeMaxBlocks = 8 blocks wide and whose (sequence, kv head) runs
+ *       number at most four per SM is decoded as with -1 instead (every run
+ *       short and on a warp of its own: no merge to wait for);
  *   >0  fixed partitions of partition_size tokens (a multiple of 16); each
  *       partition's partial result is merged with the log-sum-exp rule
  *           M = max_p m_p,  w_p = l_p exp(m_p - M),  o = sum_p w_p o_p / sum_p w_p.

@@ -90,6 +90,10 @@ constexpr int kPrepThreads = 256;
 constexpr int kPrepSeqs = 4 * kPrepThreads;   // sequences a prep block builds
 constexpr int kMaxWarpsPerSM = 16;    // decode workers <= SMs * this (workspace sizing)
 constexpr int kMinTiles = 2;          // split modes: least tiles per worker (warp)
+// Balanced mode falls back to whole runs when every table is at most this
+// many blocks wide and the runs number at most kWholeRunsPerSM per SM.
+constexpr int kWholeMaxBlocks = 8;
+constexpr int kWholeRunsPerSM = 4;
 constexpr int kMaxGroup = 16;         // query heads per kv head: two 8-column tiles
 
 bool decode_kernels_f16(int head_dim, KernelSet *ks);       // groups 1..8
