@@ -171,3 +171,33 @@ def test_long_suffixes_cut_into_many_pieces(pa, prompt_len, hq, hkv, suffix):
     ref, k_ref, v_ref = oracle.step(w)
     assert max_err(out, ref) <= TOL[w.dtype]
     assert np.array_equal(host_bits(dw.k), k_ref) and np.array_equal(host_bits(dw.v), v_ref)
+
+
+def test_workspace_reused_between_split_and_whole_suffix_decodes(pa):
+    # One workspace, filled with 0xff bytes before every call, serves a batch
+    # whose suffix runs the balanced split cuts (wide tables), then one whose
+    # tables are narrow enough to be decoded a run a warp, then the first
+    # again: the record of which runs were cut must never leak from a call
+    # into the next.
+    wa = synth.parsamp(poison=True, num_prompts=2, samples=4, prompt_len=512, max_suffix=200,
+                       num_heads=8, num_kv_heads=2, seed=41)
+    wb = synth.parsamp(poison=True, num_prompts=2, samples=4, prompt_len=48, max_suffix=40,
+                       num_heads=8, num_kv_heads=2, seed=42)
+    assert wa.block_tables.shape[1] > 8 >= wb.block_tables.shape[1]
+    need = max(pa.decode_shared_prefix_workspace_size(w.num_seqs, w.meta["samples"],
+                                                      shared_prefix_len(w), w.num_heads,
+                                                      w.num_kv_heads, w.head_dim,
+                                                      w.block_tables.shape[1]) for w in (wa, wb))
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    for w in (wa, wb, wa):
+        dw = DevWorkload(w)
+        pa.copy_blocks(dw.k, dw.v, dw.pairs)
+        ws.fill_(0xff)
+        out = torch.full_like(dw.q, float("nan"))
+        pa.decode_shared_prefix(out, dw.q, dw.k, dw.v, dw.tables, dw.lens, w.meta["samples"],
+                                shared_prefix_len(w), w.scale, k_new=dw.k_new, v_new=dw.v_new,
+                                slot_mapping=dw.slots, workspace=ws)
+        torch.cuda.synchronize()
+        assert pa.get_device_error() == 0
+        ref, _, _ = oracle.step(w)
+        assert max_err(out, ref) <= TOL[w.dtype]
