@@ -301,11 +301,13 @@ class Step:
 
     def _count_launches(self):
         n = int(self.pairs is not None)                 # copy_blocks
+        # above 2048 sequences two kernels build the decode's per-sequence
+        # arrays in the workspace
+        n += 2 if self.w.num_seqs > 2048 else 0
         if self.shared:
             # prefix attention, suffix decode, final merge (which also folds
-            # the suffix runs the decode cut), and the decode's per-sequence
-            # arrays above 2048 sequences
-            return n + 3 + (1 if self.w.num_seqs > 2048 else 0)
+            # the suffix runs the decode cut)
+            return n + 3
         n += 1                                          # decode (append fused in)
         # the library decodes short runs whole when each gets a warp of its
         # own (tables at most 8 blocks wide, at most four runs per SM)
