@@ -132,8 +132,8 @@ size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads,
  * 256-byte aligned, caller-owned; its contents need no initialisation.  Calls
  * that share a workspace must be ordered on one stream.  The split modes
  * always need one; with no split (-1) a workspace is needed only for batches
- * of more than 2048 sequences, whose per-sequence lengths and tile prefix a
- * one-block kernel builds there first (smaller batches keep them in shared
+ * of more than 2048 sequences, whose per-sequence lengths and tile prefix
+ * two small kernels build there first (smaller batches keep them in shared
  * memory).  A batch has no size limit beyond 32-bit tile indices
  * (num_seqs * max_blocks_per_seq * num_kv_heads < 2^31).
  */

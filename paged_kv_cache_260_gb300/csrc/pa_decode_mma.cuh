@@ -35,8 +35,8 @@
 //    (movmatrix), so every lane owns the same heads in S and in O: the
 //    online-softmax rescale needs no data exchange between lanes.
 //  * Large batches (more than kSeqsInSmem sequences) keep the per-sequence
-//    lengths and unit prefix in the workspace, built once by a one-block
-//    kernel, instead of in every block's shared memory.
+//    lengths and unit prefix in the workspace, built once by two small
+//    kernels, instead of in every block's shared memory.
 #pragma once
 
 #include <cuda.h>
